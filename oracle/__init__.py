@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the causal fast-weight memory recurrence.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+never imports, links or calls it, and the two share no code.
+
+The arithmetic lives in ``fw_oracle.c`` (plain sequential double-precision
+loops, one token at a time, see its header for the passages it follows).  This
+module only builds that file with gcc, loads it with ctypes and moves numpy
+arrays in and out.  Inputs are widened to float64 exactly (bf16 and fp32 values
+are exactly representable in float64), so the oracle sees the same numbers as
+the GPU.
+
+Pins: every function here is pinned by the CPU tests in
+``tests/test_oracle_pins.py`` (exact recall, textbook NLMS, ridge fixed point,
+first-token boundary, masked quadratic form of linear attention, orthonormal
+recall, per-step descent, norm bound, hand-worked golden cases).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fw_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PHI = {"identity": 0, "elu1": 1}
+MODE = {"falcon1": 0, "linattn": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile fw_oracle.c into liboracle.so next to it (gcc, -O2, no fast-math)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            L = ctypes.c_long
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.orc_falcon1.argtypes = [L, L, I, I, P, P, P, P, P, P, P, I, D, P, P, I]
+            lib.orc_linattn.argtypes = [L, L, I, I, P, P, P, P, I, P, P, I]
+            lib.orc_step.argtypes = [L, I, I, I, P, P, P, P, P, I, D, P, P, I]
+            for f in (lib.orc_falcon1, lib.orc_linattn, lib.orc_step):
+                f.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor: widen exactly on the CPU
+        import torch
+        a = a.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def falcon1(q, k, v, beta, lam, S0=None, k_init=None, phi="identity", eps=1e-6,
+            nthreads=None):
+    """Falcon-1 prefill.  q,k [..., T, dk]; v [..., T, dv]; beta, lam [..., T];
+    S0 [..., dk, dv] or None (zero state); k_init [..., dk] or None (x_1 = 0).
+    Returns (o [..., T, dv], S_T [..., dk, dv]) as float64 numpy arrays."""
+    q, k, v, beta, lam = map(_f64, (q, k, v, beta, lam))
+    S0, k_init = _f64(S0), _f64(k_init)
+    lead = q.shape[:-2]
+    T, dk = q.shape[-2:]
+    dv = v.shape[-1]
+    nc = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T,) and lam.shape == lead + (T,)
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (dk, dv))
+    _load().orc_falcon1(nc, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                        _ptr(S0), _ptr(k_init), PHI[phi], float(eps), _ptr(o), _ptr(S),
+                        nthreads or default_threads())
+    return o, S
+
+
+def linattn(q, k, v, S0=None, phi="elu1", nthreads=None):
+    """Plain causal linear attention.  Returns (o, S_T) as float64 arrays."""
+    q, k, v = map(_f64, (q, k, v))
+    S0 = _f64(S0)
+    lead = q.shape[:-2]
+    T, dk = q.shape[-2:]
+    dv = v.shape[-1]
+    nc = int(np.prod(lead)) if lead else 1
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (dk, dv))
+    _load().orc_linattn(nc, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(S0), PHI[phi],
+                        _ptr(o), _ptr(S), nthreads or default_threads())
+    return o, S
+
+
+def step(q, k_prev, v, beta, lam, S, mode="falcon1", phi="identity", eps=1e-6,
+         nthreads=None):
+    """One decode step.  q,k_prev [..., dk]; v [..., dv]; beta, lam [...] (may be
+    None in linattn mode); S [..., dk, dv].  Returns (o, S_new) as new arrays."""
+    q, k_prev, v = map(_f64, (q, k_prev, v))
+    beta, lam = _f64(beta), _f64(lam)
+    S = _f64(S).copy()
+    lead = q.shape[:-1]
+    dk = q.shape[-1]
+    dv = v.shape[-1]
+    ns = int(np.prod(lead)) if lead else 1
+    o = np.zeros(lead + (dv,))
+    _load().orc_step(ns, dk, dv, MODE[mode], _ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta),
+                     _ptr(lam), PHI[phi], float(eps), _ptr(S), _ptr(o),
+                     nthreads or default_threads())
+    return o, S

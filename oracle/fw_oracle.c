@@ -1,0 +1,262 @@
+/*
+ * fw_oracle.c -- plain, slow, fp64 CPU oracle for the causal fast-weight
+ * memory recurrence.  TEST INFRASTRUCTURE ONLY: this file is built and called
+ * by the test suite, by the package's smoke check and by the benchmark's CPU
+ * baseline leg.  No product code path links, loads or calls it, and it shares
+ * no code, header or constant with the CUDA library.
+ *
+ * Everything is computed in double precision, one token at a time, exactly in
+ * the order the pages state the rule.  Chains (one (batch, head) pair each)
+ * are independent; the only parallelism is a pthread pool over chains.
+ *
+ * Sources (page title, section):
+ *  - "Fast Weight Attention for Continual Learning" (paper reading), §3.2 and
+ *    §4.2: instantaneous ridge loss l_t(S) = 1/2 |S^T x_t - y_t|^2
+ *    + (lambda_t/2)|S|_F^2 and its one normalised gradient step (Falcon-1)
+ *        S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t r_t^T,
+ *        r_t = y_t - S_{t-1}^T x_t,
+ *        eta_t = beta_t / (|x_t|^2 + lambda_t + eps).
+ *  - same page, §1.4 and §4.1: read after write (o_t = S_t^T q_t), the
+ *    shifted training pair (x_t, y_t) = (phi(k_{t-1}), v_t), and the boundary
+ *    x_1 := 0, eta_1 := 0 (the first token's write is a no-op).
+ *  - "Attention is also an FFN" blog, §2.1 and §4.1: plain linear attention
+ *    S_i = S_{i-1} + phi(k_i) v_i^T, y_i = phi(q_i)^T S_i, with the feature
+ *    map phi(x) = elu(x) + 1, and the state kept in floating point.
+ *
+ * Readings where the pages leave a step open:
+ *  - phi is applied to the key only in Falcon-1 mode (the read uses q_t as
+ *    is); in linear-attention mode it is applied to both q and k, never to v.
+ *  - gamma_t = 1 - eta_t lambda_t is used as is, without a clamp; it can be
+ *    zero or negative when lambda_t is large against |x_t|^2.
+ *  - a decode step has no notion of position: it applies the formula with
+ *    the key it is given (a caller starting a sequence passes beta = 0).
+ *  - an optional k_init replaces the zero pair of the first token (so that a
+ *    prefill can continue a previous one); then eta_1 follows the formula.
+ *
+ * Layouts (all contiguous, row-major, double):
+ *   q, k   [nc][T][dk]     v, o   [nc][T][dv]     beta, lam [nc][T]
+ *   S0, S  [nc][dk][dv]    k_init [nc][dk]
+ * S[i][j] is key row i, value column j; reads are o_j = sum_i S[i][j] q_i.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_PHI_IDENTITY = 0, ORC_PHI_ELU1 = 1 };
+enum { ORC_FALCON1 = 0, ORC_LINATTN = 1 };
+
+/* elu(z) + 1: z + 1 for z > 0, exp(z) for z <= 0 (blog §4.1). */
+static double orc_phi(int phi, double z)
+{
+    if (phi == ORC_PHI_ELU1) return z > 0.0 ? z + 1.0 : exp(z);
+    return z;
+}
+
+/* One Falcon-1 chain, token by token. */
+static void falcon1_chain(long T, int dk, int dv, const double *q, const double *k,
+                          const double *v, const double *beta, const double *lam,
+                          const double *S0, const double *k_init, int phi, double eps,
+                          double *o, double *S, double *x, double *r)
+{
+    long t;
+    int i, j;
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)dk * dv);
+    else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+
+    for (t = 0; t < T; ++t) {
+        double eta = 0.0, gamma, n = 0.0;
+        const double *kprev = (t > 0) ? k + (t - 1) * dk : k_init;
+        if (kprev) {
+            for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kprev[i]);
+            for (i = 0; i < dk; ++i) n += x[i] * x[i];
+            eta = beta[t] / (n + lam[t] + eps);
+        } else {
+            for (i = 0; i < dk; ++i) x[i] = 0.0; /* x_1 := 0, eta_1 := 0 */
+        }
+        gamma = 1.0 - eta * lam[t];
+        /* residual against the state before the write */
+        for (j = 0; j < dv; ++j) {
+            double a = 0.0;
+            for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
+            r[j] = v[t * dv + j] - a;
+        }
+        /* the write */
+        for (i = 0; i < dk; ++i)
+            for (j = 0; j < dv; ++j)
+                S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
+        /* read after write */
+        for (j = 0; j < dv; ++j) {
+            double c = 0.0;
+            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * q[t * dk + i];
+            o[t * dv + j] = c;
+        }
+    }
+}
+
+/* One plain linear-attention chain: S += phi(k_t) v_t^T, o_t = S^T phi(q_t). */
+static void linattn_chain(long T, int dk, int dv, const double *q, const double *k,
+                          const double *v, const double *S0, int phi,
+                          double *o, double *S, double *x, double *qt)
+{
+    long t;
+    int i, j;
+    if (S0) memcpy(S, S0, sizeof(double) * (size_t)dk * dv);
+    else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+    for (t = 0; t < T; ++t) {
+        for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, k[t * dk + i]);
+        for (i = 0; i < dk; ++i) qt[i] = orc_phi(phi, q[t * dk + i]);
+        for (i = 0; i < dk; ++i)
+            for (j = 0; j < dv; ++j)
+                S[(size_t)i * dv + j] += x[i] * v[t * dv + j];
+        for (j = 0; j < dv; ++j) {
+            double c = 0.0;
+            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * qt[i];
+            o[t * dv + j] = c;
+        }
+    }
+}
+
+/* One decode step of one state (in place). */
+static void step_one(int mode, int dk, int dv, const double *q, const double *kp,
+                     const double *v, double beta, double lam, int phi, double eps,
+                     double *S, double *o, double *x, double *r)
+{
+    int i, j;
+    if (mode == ORC_LINATTN) {
+        for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kp[i]);
+        for (i = 0; i < dk; ++i)
+            for (j = 0; j < dv; ++j) S[(size_t)i * dv + j] += x[i] * v[j];
+        for (j = 0; j < dv; ++j) {
+            double c = 0.0;
+            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * orc_phi(phi, q[i]);
+            o[j] = c;
+        }
+        return;
+    }
+    {
+        double n = 0.0, eta, gamma;
+        for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kp[i]);
+        for (i = 0; i < dk; ++i) n += x[i] * x[i];
+        eta = beta / (n + lam + eps);
+        gamma = 1.0 - eta * lam;
+        for (j = 0; j < dv; ++j) {
+            double a = 0.0;
+            for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
+            r[j] = v[j] - a;
+        }
+        for (i = 0; i < dk; ++i)
+            for (j = 0; j < dv; ++j)
+                S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
+        for (j = 0; j < dv; ++j) {
+            double c = 0.0;
+            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * q[i];
+            o[j] = c;
+        }
+    }
+}
+
+/* ---- thread pool over independent chains ------------------------------- */
+
+typedef struct {
+    int kind; /* 0 prefill falcon1, 1 prefill linattn, 2 step */
+    long nc, T;
+    int dk, dv, phi, mode;
+    double eps;
+    const double *q, *k, *v, *beta, *lam, *S0, *k_init;
+    double *o, *S;
+    long next;
+    pthread_mutex_t mu;
+} orc_job;
+
+static void *orc_worker(void *arg)
+{
+    orc_job *J = (orc_job *)arg;
+    int dk = J->dk, dv = J->dv;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(dk + dv + dk));
+    double *r = x + dk, *qt = r + dv;
+    for (;;) {
+        long c;
+        pthread_mutex_lock(&J->mu);
+        c = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (c >= J->nc) break;
+        if (J->kind == 0) {
+            falcon1_chain(J->T, dk, dv, J->q + c * J->T * dk, J->k + c * J->T * dk,
+                          J->v + c * J->T * dv, J->beta + c * J->T, J->lam + c * J->T,
+                          J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
+                          J->k_init ? J->k_init + (size_t)c * dk : NULL, J->phi, J->eps,
+                          J->o + c * J->T * dv, J->S + (size_t)c * dk * dv, x, r);
+        } else if (J->kind == 1) {
+            linattn_chain(J->T, dk, dv, J->q + c * J->T * dk, J->k + c * J->T * dk,
+                          J->v + c * J->T * dv, J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
+                          J->phi, J->o + c * J->T * dv, J->S + (size_t)c * dk * dv, x, qt);
+        } else {
+            step_one(J->mode, dk, dv, J->q + (size_t)c * dk, J->k + (size_t)c * dk,
+                     J->v + (size_t)c * dv, J->beta ? J->beta[c] : 0.0,
+                     J->lam ? J->lam[c] : 0.0, J->phi, J->eps,
+                     J->S + (size_t)c * dk * dv, J->o + (size_t)c * dv, x, r);
+        }
+    }
+    free(x);
+    return NULL;
+}
+
+static void orc_run(orc_job *J, int nthreads)
+{
+    int i;
+    pthread_t th[256];
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > J->nc) nthreads = (int)(J->nc > 0 ? J->nc : 1);
+    J->next = 0;
+    pthread_mutex_init(&J->mu, NULL);
+    if (nthreads == 1) {
+        orc_worker(J);
+    } else {
+        for (i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, orc_worker, J);
+        for (i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    }
+    pthread_mutex_destroy(&J->mu);
+}
+
+/* ---- exported entry points --------------------------------------------- */
+
+/* Falcon-1 prefill over nc independent chains.  S0, k_init may be NULL. */
+void orc_falcon1(long nc, long T, int dk, int dv, const double *q, const double *k,
+                 const double *v, const double *beta, const double *lam, const double *S0,
+                 const double *k_init, int phi, double eps, double *o, double *S_T,
+                 int nthreads)
+{
+    orc_job J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 0; J.nc = nc; J.T = T; J.dk = dk; J.dv = dv; J.phi = phi; J.eps = eps;
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.lam = lam; J.S0 = S0; J.k_init = k_init;
+    J.o = o; J.S = S_T;
+    orc_run(&J, nthreads);
+}
+
+/* Plain linear-attention prefill over nc chains.  S0 may be NULL. */
+void orc_linattn(long nc, long T, int dk, int dv, const double *q, const double *k,
+                 const double *v, const double *S0, int phi, double *o, double *S_T,
+                 int nthreads)
+{
+    orc_job J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 1; J.nc = nc; J.T = T; J.dk = dk; J.dv = dv; J.phi = phi;
+    J.q = q; J.k = k; J.v = v; J.S0 = S0; J.o = o; J.S = S_T;
+    orc_run(&J, nthreads);
+}
+
+/* One decode step for ns independent states; S is updated in place. */
+void orc_step(long ns, int dk, int dv, int mode, const double *q, const double *k_prev,
+              const double *v, const double *beta, const double *lam, int phi, double eps,
+              double *S, double *o, int nthreads)
+{
+    orc_job J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 2; J.nc = ns; J.T = 1; J.dk = dk; J.dv = dv; J.mode = mode; J.phi = phi;
+    J.eps = eps; J.q = q; J.k = k_prev; J.v = v; J.beta = beta; J.lam = lam;
+    J.o = o; J.S = S;
+    orc_run(&J, nthreads);
+}
