@@ -1,0 +1,428 @@
+"""Benchmark of the fast-weight recurrence on GB300.
+
+One timed "step" is one fw_prefill over the Falcon-1 bf16 workload
+(B=8, H=16, T=4096, d=128, fp32 state; the chunked tensor-core kernel when it
+takes the call), the path that runs every prefill row: feature map and
+pairing, norms and gates, decay products, Gram and triangular solve,
+residuals, outputs and state carry.  The JSON line also carries the other
+workloads (linear attention, long context, fp32, decode) as sub-results.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (the chains are independent: no collective on the data path); the
+value is all ranks' tokens over the slowest rank's time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_token_mixer_gb300 import inputs as I  # noqa: E402
+
+HEADLINE = "falcon1_bf16"
+METRIC = "fast-weight prefill tokens/s and decode steps/s on 1 GB300, % of roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# FP32 FMA peak for a SIMT-bound kernel: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz.
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def algorithmic_bytes_prefill(w):
+    """Bytes a prefill must move: q, k, v read and o written once, beta and
+    lambda read once (Falcon-1), S0 read (when given) and S_T written once."""
+    esz = 2 if w.dtype == torch.bfloat16 else 4
+    ht = w.B * w.H * w.T
+    per_ht = 4 * w.d * esz + (8 if w.mode == "falcon1" else 0)
+    state = w.B * w.H * w.d * w.d * 4
+    return ht * per_ht + state * (2 if w.s0_std > 0 else 1)
+
+
+def matmul_flops_prefill(w, C=64):
+    """Dense matmul FLOPs of the chunked form per launch: Falcon-1
+    10 C d + 6 d^2 per head-token, linear attention 4 C d + 4 d^2."""
+    ht = w.B * w.H * w.T
+    if w.mode == "falcon1":
+        return ht * (10 * C * w.d + 6 * w.d * w.d)
+    return ht * (4 * C * w.d + 4 * w.d * w.d)
+
+
+def recurrence_flops(w):
+    """Flops of the recurrence itself: about 6 d^2 per head-token."""
+    return w.B * w.H * w.T * 6 * w.d * w.d
+
+
+class Clocks:
+    """Sample SM clocks and throttle reasons with nvidia-smi while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[3:7]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def timed(fn, K, W, stream):
+    """W untimed warm-up calls, then K calls each bracketed by CUDA events on
+    the launching stream.  Returns (total ms of the region, per-call ms)."""
+    for _ in range(W):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in ev]
+
+
+def bench_prefill(w, K, W, dev, fw, algo="auto"):
+    x = I.prefill_inputs(w, device=dev)
+    o = torch.empty_like(x["q"])
+    S_T = torch.empty(w.B, w.H, w.d, w.d, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fn():
+        fw.prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], x["S0"], mode=w.mode,
+                   phi=w.phi, eps=w.eps, algo=algo, o=o, S_T=S_T, stream=stream)
+
+    total, per = timed(fn, K, W, stream)
+    fw.check(stream)
+    kern_ms = statistics.mean(per)
+    toks = w.B * w.T
+    res = {
+        "tokens_per_s": toks * K / (total / 1e3),
+        "head_tokens_per_s": toks * w.H * K / (total / 1e3),
+        "ms_per_step": total / K,
+        "kernel_ms": kern_ms,
+        "hbm_gbs": algorithmic_bytes_prefill(w) / (kern_ms / 1e3) / 1e9,
+        "matmul_tflops": matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12,
+        "recurrence_tflops": recurrence_flops(w) / (kern_ms / 1e3) / 1e12,
+        "algo": algo,
+    }
+    return res, x
+
+
+def e2e_prefill(w, K, W, dev, fw, x_dev):
+    """Same metric through the public call with host buffers: every step copies
+    its inputs from pinned host memory to the device, runs fw_prefill and
+    reads o and S_T back into pinned host memory."""
+    host = {k: (t.cpu().pin_memory() if t is not None else None) for k, t in x_dev.items()}
+    dbuf = {k: (torch.empty_like(t) if t is not None else None) for k, t in x_dev.items()}
+    o = torch.empty_like(x_dev["q"])
+    S_T = torch.empty(w.B, w.H, w.d, w.d, device=dev)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = o.numel() * o.element_size() + S_T.numel() * 4
+
+    def fn():
+        for k, t in host.items():
+            if t is not None:
+                dbuf[k].copy_(t, non_blocking=True)
+        fw.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["beta"], dbuf["lam"], dbuf["S0"],
+                   mode=w.mode, phi=w.phi, eps=w.eps, o=o, S_T=S_T, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S_T, non_blocking=True)
+
+    total, _ = timed(fn, K, W, stream)
+    return {"value": w.B * w.T * K / (total / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def bench_decode(K_steps, W, dev, fw):
+    cfg = I.DECODE
+    Bn, H, d = cfg["batch"], cfg["H"], cfg["d"]
+    x = I.decode_inputs(K_steps, Bn, H, d, device=dev)
+    S = torch.zeros(Bn, H, d, d, device=dev)
+    o = torch.empty(Bn, H, d, device=dev, dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    i = [0]
+
+    def fn():
+        s = i[0] % K_steps
+        fw.step(x["q"][s], x["k_prev"][s], x["v"][s], x["beta"][s], x["lam"][s], S,
+                eps=cfg["eps"], o=o, stream=stream)
+        i[0] += 1
+
+    total, per = timed(fn, K_steps, W, stream)
+    fw.check(stream)
+    kern_ms = statistics.mean(per)
+    nbytes = Bn * H * (2 * d * d * 4 + 4 * d * 2 + 8)
+    return {"steps_per_s": K_steps / (total / 1e3), "tokens_per_s": Bn * K_steps / (total / 1e3),
+            "kernel_ms": kern_ms, "hbm_gbs": nbytes / (kern_ms / 1e3) / 1e9,
+            "bytes_per_step": nbytes, "steps": K_steps}
+
+
+def cpu_baseline(w, budget_s=8.0):
+    """The fp64 oracle as it stands, on this host's cores, on a bounded sample
+    of the workload's chains (same T, same per-token work)."""
+    import oracle
+    oracle.build()
+    n_all = w.B * w.H
+    threads = oracle.default_threads()
+    n = min(n_all, max(1, threads))
+    sub = I.prefill_inputs(w.with_shape(B=1, H=n))
+    t0 = time.perf_counter()
+    if w.mode == "falcon1":
+        oracle.falcon1(sub["q"], sub["k"], sub["v"], sub["beta"], sub["lam"], S0=sub["S0"],
+                       eps=w.eps, nthreads=threads)
+    else:
+        oracle.linattn(sub["q"], sub["k"], sub["v"], phi=w.phi, nthreads=threads)
+    dt = time.perf_counter() - t0
+    # tokens/s of the whole workload: chains are independent, so the sample's
+    # head-token rate carries over; one token = H head-tokens.
+    ht_rate = n * w.T / dt
+    return {"value": ht_rate / w.H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d chains (B*H), full T=%d, d=%d, fp64, %.2f s" %
+                      (n, n_all, w.T, w.d, dt)}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle as it stands, timed on the host cores."""
+    import oracle
+    oracle.build()
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    n = max(1, min(w.B * w.H, threads))
+    sub = I.prefill_inputs(w.with_shape(B=1, H=n))
+
+    def fn():
+        oracle.falcon1(sub["q"], sub["k"], sub["v"], sub["beta"], sub["lam"], S0=sub["S0"],
+                       eps=w.eps, nthreads=threads) if w.mode == "falcon1" else \
+            oracle.linattn(sub["q"], sub["k"], sub["v"], phi=w.phi, nthreads=threads)
+
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    val = n * w.T * args.steps / dt / w.H
+    sample = "%d of %d chains per step (B*H), full T=%d, d=%d, fp64" % (n, w.B * w.H, w.T, w.d)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "mode": w.mode},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from linear_token_mixer_gb300 import build as B
+    B.build()
+    from linear_token_mixer_gb300 import fw
+    fw.lib()
+    peaks = _peaks()
+    w = I.WORKLOADS[args.workload]
+
+    # ---- headline: timed region bracketed by barrier + synchronize
+    x = I.prefill_inputs(w, device=dev)
+    o = torch.empty_like(x["q"])
+    S_T = torch.empty(w.B, w.H, w.d, w.d, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fw.prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], x["S0"], mode=w.mode,
+                   phi=w.phi, eps=w.eps, o=o, S_T=S_T, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        time.sleep(0.3)
+        t_start = time.perf_counter()
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t_host = time.perf_counter() - t_start
+        # keep the GPU busy while the clock sampler catches at least a few samples
+        if t_host < 0.5:
+            t_end = time.perf_counter() + 0.5
+            while time.perf_counter() < t_end:
+                step()
+            torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    fw.check(stream)
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms_total = ev[0][0].elapsed_time(ev[-1][1])
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    kern_ms = statistics.mean(per)
+    tokens = w.B * w.T * args.steps * world
+    value = tokens / (ms_total / 1e3)
+
+    algo_bytes = algorithmic_bytes_prefill(w)
+    achieved_gbs = algo_bytes / (kern_ms / 1e3) / 1e9
+    chunked = w.dtype == torch.bfloat16 and w.d == 128
+    if chunked:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm"], "traffic": None,
+                "kernel": "chunked prefill", "peak_source": peaks["src"],
+                "algorithmic_bytes_per_launch": algo_bytes}
+    else:
+        tf = recurrence_flops(w) / (kern_ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
+                "frac": tf / ALU_FP32_TFLOPS, "traffic": None, "kernel": "recurrent (SIMT)",
+                "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"}
+    mm_tf = matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d,
+                   "mode": w.mode, "state": "fp32", "global_batch": w.B * world,
+                   "seq_len": w.T, "parallelism": "replicas x%d (independent chains)" % world,
+                   "l2": "inputs larger than L2 (%.0f MB moved per step)" % (algo_bytes / 1e6)},
+        "roofline": roof,
+        "tensor": {"matmul_tflops": mm_tf, "peak": peaks["bf16"],
+                   "frac": mm_tf / peaks["bf16"], "chunk": 64,
+                   "note": "dense matmul FLOPs of the chunked form (10Cd+6d^2 per head-token)"},
+        "gpu_launches": args.steps,
+        "kernel_ms": kern_ms,
+    }
+
+    if rank == 0:
+        out["clocks"] = clk.summary()
+        out["e2e"] = e2e_prefill(w, max(3, args.steps // 2), 3, dev, fw, x)
+        if not args.no_cpu:
+            out["cpu_baseline"] = cpu_baseline(w)
+        if not args.no_extra:
+            extra = {}
+            for name in ("linattn_bf16", "falcon1_long", "falcon1_fp32"):
+                wn = I.WORKLOADS[name]
+                r, _ = bench_prefill(wn, 5 if name != "falcon1_long" else 3, 3, dev, fw)
+                r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
+                extra[name] = r
+            dec = bench_decode(I.DECODE["steps"], 3, dev, fw)
+            dec["hbm_frac"] = dec["hbm_gbs"] / peaks["hbm"]
+            extra["decode"] = dec
+            out["workloads"] = extra
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

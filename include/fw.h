@@ -1,0 +1,167 @@
+/*
+ * fw.h -- C ABI of the GB300 (sm_103a) fast-weight memory recurrence library
+ * (libfw.so).
+ *
+ * The library computes the causal fast-weight memory recurrence of the
+ * "Fast Weight Attention for Continual Learning" paper reading (Falcon-1,
+ * §3.2 and §4.2): every token writes into a d_k x d_v fp32 state S with one
+ * normalised gradient step on the instantaneous ridge loss
+ *
+ *     l_t(S) = 1/2 |S^T x_t - y_t|^2 + (lambda_t / 2) |S|_F^2,
+ *     r_t    = y_t - S_{t-1}^T x_t,
+ *     eta_t  = beta_t / (|x_t|^2 + lambda_t + eps),
+ *     S_t    = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t r_t^T,
+ *
+ * on the shifted training pair (x_t, y_t) = (phi(k_{t-1}), v_t) with the
+ * boundary x_1 := 0, eta_1 := 0 (§4.1), and reads after the write,
+ * o_t = S_t^T q_t (§1.4).  FW_LINATTN selects plain causal linear attention,
+ * S_t = S_{t-1} + phi(k_t) v_t^T, o_t = S_t^T phi(q_t) ("Attention is also an
+ * FFN" blog, §2.1 and §4.1), the special case without residual or decay.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  Rows are contiguous, row-major.
+ *   - q, k, v, o:  [B][H][T][d] (prefill) or [B][H][d] (step), element type
+ *     FW_F32 (float) or FW_BF16 (bfloat16), d innermost.
+ *   - beta, lambda: float [B][H][T] (prefill) or [B][H] (step).  Ignored (may
+ *     be NULL) in FW_LINATTN mode.
+ *   - S0, S_T, S: float [B][H][d_k][d_v], S[i][j] = key row i, value column j,
+ *     so a read is o_j = sum_i S[i][j] q_i (the blog's y = q @ S).
+ *   - Pointers must be 16-byte aligned (vector and TMA loads).
+ *   - Every call validates its arguments before any launch, enqueues its work
+ *     on `stream` and returns without synchronising.  A non-zero return means
+ *     nothing was launched (except FW_ERR_CUDA, see fw_last_cuda_error()).
+ *   - Waits inside kernels are bounded; a wait that runs out sets a device
+ *     error word instead of hanging.  fw_check() reads and clears it.
+ *   - Inputs are never written (except S in fw_step, updated in place).
+ */
+#ifndef FW_H_
+#define FW_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FW_VERSION 100 /* 1.0.0 */
+
+typedef enum { FW_F32 = 0, FW_BF16 = 1 } fw_dtype;
+
+/* FW_FALCON1: shifted pair, residual write, normalised step and decay.
+ * FW_LINATTN: same-step pair, additive write S += phi(k) v^T, no eta/gamma. */
+typedef enum { FW_FALCON1 = 0, FW_LINATTN = 1 } fw_mode;
+
+/* Feature map phi.  FW_FALCON1 applies it to the key only (the read uses q as
+ * given); FW_LINATTN applies it to both q and k, never to v.
+ * FW_PHI_ELU1: elu(z) + 1 = z + 1 for z > 0, exp(z) for z <= 0. */
+typedef enum { FW_PHI_IDENTITY = 0, FW_PHI_ELU1 = 1 } fw_phi;
+
+/* Kernel choice for fw_prefill_ex.  FW_ALGO_AUTO picks the chunked
+ * tensor-core kernel when it supports the call (bf16, d_k = d_v = 128) and the
+ * per-token SIMT recurrence otherwise. */
+typedef enum { FW_ALGO_AUTO = 0, FW_ALGO_RECURRENT = 1, FW_ALGO_CHUNKED = 2 } fw_algo;
+
+typedef struct {
+    int64_t B;   /* batch, >= 1 */
+    int64_t H;   /* heads, >= 1 */
+    int64_t T;   /* tokens per chain; >= 1 for prefill, must be 1 for fw_step */
+    int32_t d_k; /* key width, 64 or 128 */
+    int32_t d_v; /* value width, equal to d_k */
+} fw_shape;
+
+enum {
+    FW_OK = 0,
+    FW_ERR_NULL = -1,        /* a required pointer is NULL */
+    FW_ERR_SHAPE = -2,       /* B, H or T < 1, d_k not in {64,128}, d_v != d_k, T != 1 in fw_step */
+    FW_ERR_DTYPE = -3,       /* unknown fw_dtype */
+    FW_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+    FW_ERR_MODE = -5,        /* unknown fw_mode, fw_phi or fw_algo */
+    FW_ERR_CUDA = -6,        /* a CUDA call failed; see fw_last_cuda_error() */
+    FW_ERR_TIMEOUT = -7,     /* a bounded device wait ran out (reported by fw_check) */
+    FW_ERR_UNSUPPORTED = -8, /* FW_ALGO_CHUNKED asked for a call it does not support */
+    FW_ERR_ARG = -9,         /* eps negative or not finite, or o aliases an input */
+    FW_ERR_DEVICE = -10      /* the current device is not an sm_103 GPU */
+};
+
+/*
+ * fw_prefill -- run the recurrence over T tokens for B*H independent chains.
+ *
+ * Passage: "Fast Weight Attention for Continual Learning" paper reading,
+ * §3.2/§4.1/§4.2 (FW_FALCON1); "Attention is also an FFN" blog §2.1
+ * (FW_LINATTN).  Chunked evaluation follows the same page's §4.4 (intra-chunk
+ * triangular solve, short inter-chunk recurrence, parallel outputs).
+ *
+ *   q, k, v  in   [B][H][T][d] of `dtype`
+ *   beta     in   float [B][H][T]   (FW_FALCON1; beta_t in [0, 2) keeps the
+ *                                     write stable, other values are computed
+ *                                     literally)
+ *   lambda   in   float [B][H][T]   (FW_FALCON1; >= 0)
+ *   S0       in   float [B][H][d][d] or NULL for a zero start state
+ *   o        out  [B][H][T][d] of `dtype` (rounded to nearest even for bf16);
+ *                 must not overlap any input
+ *   S_T      out  float [B][H][d][d], the state after token T; may equal S0
+ *   eps      in   >= 0, added to the step's denominator (FW_FALCON1)
+ * Returns FW_OK or a negative FW_ERR_* code.
+ */
+int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
+               const float *lambda, const float *S0, void *o, float *S_T,
+               const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+               cudaStream_t stream);
+
+/*
+ * fw_prefill_ex -- fw_prefill with two more arguments.
+ *   k_init  in  [B][H][d] of `dtype` or NULL.  FW_FALCON1 only: the key that
+ *               precedes this call's first token (the last key of a previous
+ *               prefill of the same sequence).  Given, the first token's pair
+ *               is (phi(k_init), v_1) with the normal step; NULL keeps the
+ *               boundary x_1 = 0, eta_1 = 0.  Ignored in FW_LINATTN mode.
+ *   algo    in  FW_ALGO_AUTO, or force one kernel (FW_ERR_UNSUPPORTED if the
+ *               chunked kernel cannot take the call).
+ */
+int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
+                  const float *lambda, const float *S0, const void *k_init, void *o,
+                  float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
+                  fw_phi phi, float eps, fw_algo algo, cudaStream_t stream);
+
+/*
+ * fw_step -- one decode step for B*H independent states, S updated in place.
+ *
+ * Passage: the Falcon-1 write of "Fast Weight Attention for Continual
+ * Learning" paper reading §3.2 with the pair (phi(k_prev), v) and the read
+ * after the write; the blog's forward_step (§4.1) for FW_LINATTN, where
+ * `k_prev` is the current token's key.  A step knows no position: to start a
+ * sequence with steps pass beta = 0 (an empty first write).
+ *
+ *   q, k_prev, v  in      [B][H][d] of `dtype`
+ *   beta, lambda  in      float [B][H] (FW_FALCON1)
+ *   S             in/out  float [B][H][d][d]
+ *   o             out     [B][H][d] of `dtype`, o = S_new^T q
+ *   shape         T must be 1
+ */
+int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
+            const float *lambda, float *S, void *o, const fw_shape *shape, fw_dtype dtype,
+            fw_mode mode, fw_phi phi, float eps, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word.
+ * Returns FW_OK, FW_ERR_TIMEOUT, or FW_ERR_CUDA. */
+int fw_check(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fw_status_string(int status);
+
+/* FW_VERSION of the built library. */
+int fw_version(void);
+
+/* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
+int fw_last_cuda_error(void);
+
+/* Testing hook: iteration limit of every bounded device wait (default 2^26
+ * polls, about a second).  Values < 1 restore the default. */
+void fw_set_wait_limit(long long polls);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FW_H_ */

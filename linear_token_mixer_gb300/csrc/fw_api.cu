@@ -1,0 +1,222 @@
+// fw_api.cu -- the C ABI of libfw.so: argument validation, kernel choice,
+// device error word.  See include/fw.h for the contract of every call.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "fw_internal.cuh"
+
+namespace fw {
+namespace {
+
+// Device error word: set by kernels whose bounded waits run out.
+__device__ int g_dev_error;
+
+thread_local int g_last_cuda_error = 0;
+std::atomic<long long> g_wait_limit{1LL << 26};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int *g_err_ptr[kMaxDevices];
+int g_dev_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 not sm_103
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return FW_ERR_CUDA;
+}
+
+// Resolve (once per device) the device address of the error word and check
+// the architecture.  Returns FW_OK or an error.
+int device_setup(int **err_ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return FW_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) {
+            g_dev_ok[dev] = -1;
+        } else {
+            void *p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_dev_error)) != cudaSuccess) return cuda_fail(e);
+            g_err_ptr[dev] = static_cast<int *>(p);
+            g_dev_ok[dev] = 1;
+        }
+    }
+    if (g_dev_ok[dev] < 0) return FW_ERR_DEVICE;
+    *err_ptr = g_err_ptr[dev];
+    return FW_OK;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps) {
+    if (!shape) return FW_ERR_NULL;
+    if (shape->B < 1 || shape->H < 1 || shape->T < 1) return FW_ERR_SHAPE;
+    if (shape->d_k != 64 && shape->d_k != 128) return FW_ERR_SHAPE;
+    if (shape->d_v != shape->d_k) return FW_ERR_SHAPE;
+    if (shape->B > (int64_t)1 << 31 || shape->H > (int64_t)1 << 31) return FW_ERR_SHAPE;
+    if (shape->B * shape->H > (int64_t)INT32_MAX) return FW_ERR_SHAPE;
+    if (dtype != FW_F32 && dtype != FW_BF16) return FW_ERR_DTYPE;
+    if (mode != FW_FALCON1 && mode != FW_LINATTN) return FW_ERR_MODE;
+    if (phi != FW_PHI_IDENTITY && phi != FW_PHI_ELU1) return FW_ERR_MODE;
+    if (mode == FW_FALCON1 && !(std::isfinite(eps) && eps >= 0.f)) return FW_ERR_ARG;
+    return FW_OK;
+}
+
+}  // namespace
+}  // namespace fw
+
+using namespace fw;
+
+extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
+                             const float *lambda, const float *S0, const void *k_init, void *o,
+                             float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
+                             fw_phi phi, float eps, fw_algo algo, cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps);
+    if (st != FW_OK) return st;
+    if (algo != FW_ALGO_AUTO && algo != FW_ALGO_RECURRENT && algo != FW_ALGO_CHUNKED)
+        return FW_ERR_MODE;
+    if (!q || !k || !v || !o || !S_T) return FW_ERR_NULL;
+    if (mode == FW_FALCON1 && (!beta || !lambda)) return FW_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(S_T) ||
+        misaligned(S0) || misaligned(k_init) || (mode == FW_FALCON1 && (misaligned(beta) ||
+                                                                          misaligned(lambda))))
+        return FW_ERR_ALIGN;
+
+    const int64_t nc = shape->B * shape->H;
+    const int d = shape->d_k;
+    const size_t esz = dtype == FW_F32 ? 4 : 2;
+    const size_t nx = (size_t)nc * (size_t)shape->T * d * esz;
+    const size_t ns = (size_t)nc * d * d * sizeof(float);
+    const size_t nbl = (size_t)nc * (size_t)shape->T * sizeof(float);
+    if (overlaps(o, nx, q, nx) || overlaps(o, nx, k, nx) || overlaps(o, nx, v, nx) ||
+        overlaps(o, nx, S0, S0 ? ns : 0) || overlaps(o, nx, S_T, ns))
+        return FW_ERR_ARG;
+    if (mode == FW_FALCON1 && (overlaps(o, nx, beta, nbl) || overlaps(o, nx, lambda, nbl) ||
+                               overlaps(S_T, ns, beta, nbl) || overlaps(S_T, ns, lambda, nbl)))
+        return FW_ERR_ARG;
+    if (overlaps(S_T, ns, q, nx) || overlaps(S_T, ns, k, nx) || overlaps(S_T, ns, v, nx))
+        return FW_ERR_ARG;
+    if (S0 && S0 != S_T && overlaps(S_T, ns, S0, ns)) return FW_ERR_ARG;
+
+    PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.S0 = S0;
+    a.k_init = (mode == FW_FALCON1) ? k_init : nullptr;
+    a.o = o; a.S_T = S_T; a.n_chains = nc; a.T = shape->T; a.d = d;
+    a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps;
+    a.wait_limit = g_wait_limit.load();
+
+    const bool chunk_ok = chunked_supported(a);
+    if (algo == FW_ALGO_CHUNKED && !chunk_ok) return FW_ERR_UNSUPPORTED;
+
+    st = device_setup(&a.err);
+    if (st != FW_OK) return st;
+
+    cudaError_t e;
+    if (algo == FW_ALGO_RECURRENT || !chunk_ok) e = launch_recurrent(a, stream);
+    else e = launch_chunked(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FW_OK;
+}
+
+extern "C" int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
+                          const float *lambda, const float *S0, void *o, float *S_T,
+                          const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi,
+                          float eps, cudaStream_t stream) {
+    return fw_prefill_ex(q, k, v, beta, lambda, S0, nullptr, o, S_T, shape, dtype, mode, phi,
+                         eps, FW_ALGO_AUTO, stream);
+}
+
+extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
+                       const float *lambda, float *S, void *o, const fw_shape *shape,
+                       fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+                       cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps);
+    if (st != FW_OK) return st;
+    if (shape->T != 1) return FW_ERR_SHAPE;
+    if (!q || !k_prev || !v || !S || !o) return FW_ERR_NULL;
+    if (mode == FW_FALCON1 && (!beta || !lambda)) return FW_ERR_NULL;
+    if (misaligned(q) || misaligned(k_prev) || misaligned(v) || misaligned(S) || misaligned(o) ||
+        (mode == FW_FALCON1 && (misaligned(beta) || misaligned(lambda))))
+        return FW_ERR_ALIGN;
+    const int64_t ns = shape->B * shape->H;
+    const int d = shape->d_k;
+    const size_t esz = dtype == FW_F32 ? 4 : 2;
+    const size_t nx = (size_t)ns * d * esz;
+    const size_t nst = (size_t)ns * d * d * sizeof(float);
+    if (overlaps(o, nx, q, nx) || overlaps(o, nx, k_prev, nx) || overlaps(o, nx, v, nx) ||
+        overlaps(o, nx, S, nst) || overlaps(S, nst, q, nx) || overlaps(S, nst, k_prev, nx) ||
+        overlaps(S, nst, v, nx))
+        return FW_ERR_ARG;
+    if (mode == FW_FALCON1 && (overlaps(S, nst, beta, ns * 4) || overlaps(S, nst, lambda, ns * 4) ||
+                               overlaps(o, nx, beta, ns * 4) || overlaps(o, nx, lambda, ns * 4)))
+        return FW_ERR_ARG;
+
+    int *err = nullptr;
+    st = device_setup(&err);
+    if (st != FW_OK) return st;
+
+    StepArgs a;
+    a.q = q; a.k = k_prev; a.v = v; a.beta = beta; a.lam = lambda; a.S = S; a.o = o;
+    a.n_states = ns; a.d = d; a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps;
+    cudaError_t e = launch_decode(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FW_OK;
+}
+
+extern "C" int fw_check(cudaStream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int *err = nullptr;
+    int st = device_setup(&err);
+    if (st != FW_OK) return st;
+    int h = 0;
+    if ((e = cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    if (h != kDevErrNone) {
+        const int zero = 0;
+        if ((e = cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+            return cuda_fail(e);
+        return FW_ERR_TIMEOUT;
+    }
+    return FW_OK;
+}
+
+extern "C" const char *fw_status_string(int status) {
+    switch (status) {
+    case FW_OK: return "FW_OK";
+    case FW_ERR_NULL: return "FW_ERR_NULL: a required pointer is NULL";
+    case FW_ERR_SHAPE: return "FW_ERR_SHAPE: unsupported shape";
+    case FW_ERR_DTYPE: return "FW_ERR_DTYPE: unknown dtype";
+    case FW_ERR_ALIGN: return "FW_ERR_ALIGN: pointer not 16-byte aligned";
+    case FW_ERR_MODE: return "FW_ERR_MODE: unknown mode, feature map or algorithm";
+    case FW_ERR_CUDA: return "FW_ERR_CUDA: a CUDA call failed";
+    case FW_ERR_TIMEOUT: return "FW_ERR_TIMEOUT: a bounded device wait ran out";
+    case FW_ERR_UNSUPPORTED: return "FW_ERR_UNSUPPORTED: the chunked kernel does not take this call";
+    case FW_ERR_ARG: return "FW_ERR_ARG: invalid eps or overlapping buffers";
+    case FW_ERR_DEVICE: return "FW_ERR_DEVICE: the current device is not sm_103";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int fw_version(void) { return FW_VERSION; }
+
+extern "C" int fw_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" void fw_set_wait_limit(long long polls) {
+    g_wait_limit.store(polls < 1 ? (1LL << 26) : polls);
+}

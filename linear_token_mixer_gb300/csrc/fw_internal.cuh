@@ -1,0 +1,70 @@
+// fw_internal.cuh -- declarations shared by the translation units of libfw.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fw.h"
+
+namespace fw {
+
+// Device error word values (written by kernels, read by fw_check).
+enum : int { kDevErrNone = 0, kDevErrTimeout = 1 };
+
+// Arguments of one prefill call, already validated.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *beta, *lam, *S0;
+    const void *k_init;
+    void *o;
+    float *S_T;
+    int64_t n_chains;  // B * H
+    int64_t T;
+    int d;             // d_k == d_v
+    fw_dtype dtype;
+    fw_mode mode;
+    fw_phi phi;
+    float eps;
+    int *err;          // device error word
+    long long wait_limit;
+};
+
+struct StepArgs {
+    const void *q, *k, *v;
+    const float *beta, *lam;
+    float *S;
+    void *o;
+    int64_t n_states;
+    int d;
+    fw_dtype dtype;
+    fw_mode mode;
+    fw_phi phi;
+    float eps;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_recurrent(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const StepArgs &a, cudaStream_t s);
+// Chunked tensor-core prefill.  supported() tells whether it takes the call.
+bool chunked_supported(const PrefillArgs &a);
+cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s);
+
+// ---- small device helpers ------------------------------------------------
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// phi(z) = elu(z) + 1 = z + 1 (z > 0), exp(z) (z <= 0); identity otherwise.
+__device__ __forceinline__ float apply_phi(int phi, float z) {
+    if (phi == FW_PHI_ELU1) return z > 0.f ? z + 1.f : expf(z);
+    return z;
+}
+
+}  // namespace fw

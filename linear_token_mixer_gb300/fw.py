@@ -1,0 +1,132 @@
+"""Thin ctypes binding of libfw.so (include/fw.h) over torch CUDA tensors.
+
+Argument marshalling only: every step of the recurrence runs in the library's
+CUDA kernels.  There is no CPU path; if libfw.so is missing or fails to load,
+every call raises.  torch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfw.so")
+
+FW_F32, FW_BF16 = 0, 1
+MODES = {"falcon1": 0, "linattn": 1}
+PHIS = {"identity": 0, "elu1": 1}
+ALGOS = {"auto": 0, "recurrent": 1, "chunked": 2}
+DTYPES = {torch.float32: FW_F32, torch.bfloat16: FW_BF16}
+
+FW_OK = 0
+STATUS = {0: "FW_OK", -1: "FW_ERR_NULL", -2: "FW_ERR_SHAPE", -3: "FW_ERR_DTYPE",
+          -4: "FW_ERR_ALIGN", -5: "FW_ERR_MODE", -6: "FW_ERR_CUDA", -7: "FW_ERR_TIMEOUT",
+          -8: "FW_ERR_UNSUPPORTED", -9: "FW_ERR_ARG", -10: "FW_ERR_DEVICE"}
+
+
+class FwError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().fw_status_string(status).decode()
+        if status == -6:
+            msg += " (cudaError %d)" % lib().fw_last_cuda_error()
+        super().__init__("%s: %s" % (where, msg))
+
+
+class fw_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
+
+
+EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_check", "fw_status_string",
+           "fw_version", "fw_last_cuda_error", "fw_set_wait_limit")
+
+_lib = None
+
+
+def lib():
+    """Load libfw.so (building it first is the caller's job: see build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfw.so is not built (run linear_token_mixer_gb300/build.py); "
+                               "there is no fallback path")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        SP = ctypes.POINTER(fw_shape)
+        L.fw_prefill.argtypes = [P, P, P, P, P, P, P, P, SP, I, I, I, F, P]
+        L.fw_prefill_ex.argtypes = [P, P, P, P, P, P, P, P, P, SP, I, I, I, F, I, P]
+        L.fw_step.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, P]
+        L.fw_check.argtypes = [P]
+        L.fw_status_string.argtypes = [I]
+        L.fw_status_string.restype = ctypes.c_char_p
+        L.fw_version.argtypes = []
+        L.fw_last_cuda_error.argtypes = []
+        L.fw_set_wait_limit.argtypes = [ctypes.c_longlong]
+        L.fw_set_wait_limit.restype = None
+        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_check, L.fw_version,
+                  L.fw_last_cuda_error):
+            f.restype = I
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("fw: tensors must live on a CUDA device (no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError("fw: tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def prefill(q, k, v, beta=None, lam=None, S0=None, *, mode="falcon1", phi="identity",
+            eps=1e-6, k_init=None, algo="auto", o=None, S_T=None, stream=None):
+    """Run the recurrence over q, k, v [B, H, T, d] (fp32 or bf16).
+
+    Returns (o [B,H,T,d] in q's dtype, S_T [B,H,d,d] fp32).  beta, lam
+    [B,H,T] fp32 are required in falcon1 mode.  S0 [B,H,d,d] fp32 or None."""
+    B, H, T, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if S_T is None:
+        S_T = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    shp = fw_shape(B, H, T, d, v.shape[-1])
+    st = lib().fw_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+                             _ptr(k_init), _ptr(o), _ptr(S_T), ctypes.byref(shp),
+                             DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi], float(eps),
+                             ALGOS[algo], _stream(stream))
+    if st != FW_OK:
+        raise FwError(st, "fw_prefill")
+    return o, S_T
+
+
+def step(q, k_prev, v, beta, lam, S, *, mode="falcon1", phi="identity", eps=1e-6, o=None,
+         stream=None):
+    """One decode step for q, k_prev, v [B, H, d]; S [B, H, d, d] fp32 is
+    updated in place.  Returns o [B, H, d] in q's dtype."""
+    B, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    shp = fw_shape(B, H, 1, d, v.shape[-1])
+    st = lib().fw_step(_ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S), _ptr(o),
+                       ctypes.byref(shp), DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi],
+                       float(eps), _stream(stream))
+    if st != FW_OK:
+        raise FwError(st, "fw_step")
+    return o
+
+
+def check(stream=None):
+    """Synchronise the stream and raise if a bounded device wait ran out."""
+    st = lib().fw_check(_stream(stream))
+    if st != FW_OK:
+        raise FwError(st, "fw_check")

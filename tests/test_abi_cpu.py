@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every function include/fw.h declares, and argument validation rejects
+bad calls before touching any device.
+
+The validation tests pass small fake addresses; they are skipped when a GPU
+is visible so that no fake pointer could ever reach a launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from linear_token_mixer_gb300 import build as B
+from linear_token_mixer_gb300 import fw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return fw.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fw.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fw_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(fw.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.fw_version() == 100
+    for code, name in fw.STATUS.items():
+        assert L.fw_status_string(code).decode().startswith(name)
+    assert L.fw_status_string(12345) == b"unknown status"
+
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="fake-pointer validation checks run only without a GPU")
+
+A = 0x10000        # fake, 16-byte aligned addresses: validation never dereferences
+P = [A + 0x100000 * i for i in range(12)]
+
+
+def call_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init=None, o=P[5],
+                 S_T=P[6], shape=(1, 1, 8, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6,
+                 algo=0):
+    shp = fw.fw_shape(*shape) if shape is not None else None
+    return L.fw_prefill_ex(q, k, v, beta, lam, S0, k_init, o, S_T,
+                           ctypes.byref(shp) if shp is not None else None,
+                           dtype, mode, phi, eps, algo, None)
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(shape=None), -1), (dict(q=None), -1), (dict(o=None), -1), (dict(S_T=None), -1),
+    (dict(beta=None), -1), (dict(lam=None), -1),
+    (dict(shape=(0, 1, 8, 64, 64)), -2), (dict(shape=(1, 0, 8, 64, 64)), -2),
+    (dict(shape=(1, 1, 0, 64, 64)), -2), (dict(shape=(1, 1, 8, 96, 96)), -2),
+    (dict(shape=(1, 1, 8, 64, 128)), -2), (dict(shape=(1, 1, 8, 32, 32)), -2),
+    (dict(dtype=7), -3), (dict(mode=3), -5), (dict(phi=9), -5), (dict(algo=5), -5),
+    (dict(q=P[0] + 8), -4), (dict(o=P[5] + 2), -4), (dict(S0=P[7] + 4), -4),
+    (dict(k_init=P[8] + 2), -4), (dict(beta=P[3] + 4), -4),
+    (dict(eps=-1.0), -9), (dict(eps=float("nan")), -9), (dict(o=P[0]), -9),
+    (dict(S_T=P[1]), -9), (dict(S0=P[6] + 16), -9),
+])
+def test_prefill_validation(L, kw, code):
+    assert call_prefill(L, **kw) == code
+
+
+@no_gpu
+def test_linattn_needs_no_gates(L):
+    # beta/lambda may be NULL in linear-attention mode: validation passes and the
+    # call fails only at the device query (there is no GPU here).
+    assert call_prefill(L, beta=None, lam=None, mode=1, dtype=7) == -3
+    assert call_prefill(L, beta=None, lam=None, mode=1) in (-6, -10)
+
+
+@no_gpu
+def test_chunked_unsupported_shapes(L):
+    # fp32 or d = 64 calls are not taken by the chunked kernel.
+    assert call_prefill(L, dtype=0, shape=(1, 1, 8, 128, 128), algo=2) == -8
+    assert call_prefill(L, dtype=1, shape=(1, 1, 8, 64, 64), algo=2) == -8
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(shape=(1, 1, 2, 64, 64)), -2), (dict(q=None), -1), (dict(S=None), -1),
+    (dict(beta=None), -1), (dict(S=P[6] + 4), -4), (dict(o=P[0]), -9), (dict(dtype=5), -3),
+])
+def test_step_validation(L, kw, code):
+    args = dict(q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S=P[6], o=P[5],
+                shape=(2, 2, 1, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6)
+    args.update(kw)
+    shp = fw.fw_shape(*args["shape"])
+    st = L.fw_step(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S"],
+                   args["o"], ctypes.byref(shp), args["dtype"], args["mode"], args["phi"],
+                   args["eps"], None)
+    assert st == code
+
+
+@no_gpu
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    st = call_prefill(L)
+    assert st in (-6, -10)
+    if st == -6:
+        assert L.fw_last_cuda_error() != 0
+
+
+def test_binding_refuses_cpu_tensors(L):
+    x = torch.zeros(1, 1, 4, 64)
+    with pytest.raises(ValueError):
+        fw.prefill(x, x, x, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4))
