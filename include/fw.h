@@ -157,9 +157,16 @@ int fw_version(void);
 /* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
 int fw_last_cuda_error(void);
 
-/* Testing hook: iteration limit of every bounded device wait (default 2^26
- * polls, about a second).  Values < 1 restore the default. */
-void fw_set_wait_limit(long long polls);
+/* Wall-time limit of every bounded device wait, in microseconds (default
+ * 2,000,000).  Values < 1 restore the default.  Applies to later calls. */
+void fw_set_wait_limit_us(long long us);
+
+/* Testing hook for the timeout path: while `on` is non-zero, chunked-kernel
+ * launches first wait on a barrier that nothing arrives on, so the wait runs
+ * out after the wait limit; the kernel then records FW_ERR_TIMEOUT (read by
+ * fw_check), drains its copies in flight, frees its tensor memory and exits.
+ * No GPU fault is involved. */
+void fw_debug_force_timeout(int on);
 
 #ifdef __cplusplus
 }

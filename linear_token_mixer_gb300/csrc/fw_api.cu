@@ -13,7 +13,9 @@ namespace {
 __device__ int g_dev_error;
 
 thread_local int g_last_cuda_error = 0;
-std::atomic<long long> g_wait_limit{1LL << 26};
+constexpr long long kDefaultWaitUs = 2000000;  // 2 s
+std::atomic<long long> g_wait_us{kDefaultWaitUs};
+std::atomic<int> g_force_timeout{0};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -118,7 +120,8 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     a.k_init = (mode == FW_FALCON1) ? k_init : nullptr;
     a.o = o; a.S_T = S_T; a.n_chains = nc; a.T = shape->T; a.d = d;
     a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps;
-    a.wait_limit = g_wait_limit.load();
+    a.wait_ns = g_wait_us.load() * 1000LL;
+    a.force_timeout = g_force_timeout.load();
 
     const bool chunk_ok = chunked_supported(a);
     if (algo == FW_ALGO_CHUNKED && !chunk_ok) return FW_ERR_UNSUPPORTED;
@@ -217,6 +220,8 @@ extern "C" int fw_version(void) { return FW_VERSION; }
 
 extern "C" int fw_last_cuda_error(void) { return g_last_cuda_error; }
 
-extern "C" void fw_set_wait_limit(long long polls) {
-    g_wait_limit.store(polls < 1 ? (1LL << 26) : polls);
+extern "C" void fw_set_wait_limit_us(long long us) {
+    g_wait_us.store(us < 1 ? kDefaultWaitUs : us);
 }
+
+extern "C" void fw_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }

@@ -1,8 +1,768 @@
-// fw_chunked.cu -- chunked tensor-core prefill (placeholder until the tcgen05
-// kernel lands: it declines every call, so the recurrent kernel serves all).
+// fw_chunked.cu -- chunked tensor-core prefill for bf16 inputs, d_k = d_v = 128.
+//
+// Follows the three stages the "Fast Weight Attention for Continual Learning"
+// paper reading gives for Falcon-1 in §4.4 (WY representation of the chunk's
+// rank-one edits: intra-chunk triangular solve, short inter-chunk recurrence
+// on a fixed-size state, parallel output materialisation).  The equations are
+// our own derivation of that structure.  For one chunk of C = 64 tokens
+// (chunk-local indices t, s), starting state S0 and
+//   gamma_t = 1 - eta_t lambda_t,  D[t,s] = prod_{i=s+1..t} gamma_i,
+//   G_t = prod_{i<=t} gamma_i,     Gm_t = G_{t-1},
+//   L[t,s] = D[t-1,s] eta_s (x_t.x_s)  (s < t),   T = (I + L)^{-1},
+//   W = T diag(Gm) X,  U = T Y,  R = U - W S0      (the true residuals r_t),
+//   P[t,s] = D[t,s] eta_s (q_t.x_s)    (s <= t),
+//   O = diag(G) Q S0 + P R,
+//   S_C = G_{C-1} S0 + X^T diag(D[C-1,s] eta_s) R.
+// D is built from direct running products, never by dividing prefix
+// products: gamma may be zero or negative.  Linear attention is the same
+// skeleton with x = phi(k_t), q := phi(q_t), eta = gamma = 1 and R = V.
+//
+// Mapping (one CTA per chain, 4 math warps + 1 TMA warp):
+//   * TMA brings the chunk's X (keys shifted by one token for Falcon-1; the
+//     row before the sequence reads as zero), Q and V tiles (64 x 128 bf16
+//     each, 128-byte swizzle) into a double-buffered stage.
+//   * Every product is one tcgen05 MMA batch with M = 128 (the transposed
+//     forms W^T, U^T, R^T, O^T keep d on the M side), bf16 operands in
+//     shared memory, fp32 accumulators in tensor memory:
+//       G = [X;Q] X^T, W^T = X^T (T diag Gm)^T, U^T = Y^T T^T,
+//       R^T = U^T - S^T W^T, O1^T = S^T Q^T, O2^T = R^T P^T,
+//       S += X^T (diag(w) R)   (S accumulates in place in tensor memory).
+//   * The fp32 state lives in tensor memory across chunks (pre-scaled by the
+//     chunk's total decay before the accumulate); its bf16 copy in shared
+//     memory is the MMA operand.  T comes from a blocked SIMT solve in fp32.
+//   * Every wait is bounded; on expiry the kernel records an error, drains
+//     its copies and MMAs in flight, frees tensor memory and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "fw_internal.cuh"
+#include "fw_sm100.cuh"
 
 namespace fw {
-bool chunked_supported(const PrefillArgs &) { return false; }
-cudaError_t launch_chunked(const PrefillArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+using namespace sm100;
+
+constexpr int C = 64;        // chunk length
+constexpr int D = 128;       // d_k = d_v
+constexpr int NMATH = 128;   // math threads (warps 0..3), one per TMEM lane
+constexpr int NTHREADS = NMATH + 32;
+constexpr int LDF = 68;      // fp32 row stride of the solver's L / T buffers
+constexpr int LDM = 36;      // fp32 row stride of the solver's product scratch
+
+constexpr uint32_t KB = 1024;
+// one input stage: X0 Q0 X1 Q1 Y0 Y1, each 64 rows x 128 B (64 columns of d)
+constexpr uint32_t STAGE = 48 * KB;
+constexpr uint32_t ST_X0 = 0, ST_Q0 = 8 * KB, ST_X1 = 16 * KB, ST_Q1 = 24 * KB;
+constexpr uint32_t ST_Y0 = 32 * KB, ST_Y1 = 40 * KB;
+constexpr uint32_t OFF_TB = 2 * STAGE;          // T, bf16, K-major (rows t)
+constexpr uint32_t OFF_TPB = OFF_TB + 8 * KB;   // T diag(Gm), bf16
+constexpr uint32_t OFF_PB = OFF_TPB + 8 * KB;   // P, bf16, K-major (rows t)
+constexpr uint32_t OFF_WTB = OFF_PB + 8 * KB;   // -W^T, bf16, rows i (MN-major B)
+constexpr uint32_t OFF_RA = OFF_WTB + 16 * KB;  // R^T, bf16, rows j (K-major A)
+constexpr uint32_t OFF_RB = OFF_RA + 16 * KB;   // (diag(w) R)^T, bf16, rows j (K-major B)
+constexpr uint32_t OFF_SB = OFF_RB + 16 * KB;   // S, bf16, rows i, two 64-column blocks
+constexpr uint32_t OFF_VEC = OFF_SB + 32 * KB;
+// the solver's fp32 scratch reuses [OFF_WTB, OFF_SB): it is dead before -W^T is written
+constexpr uint32_t OFF_LF = OFF_WTB;
+constexpr uint32_t OFF_TF = OFF_LF + C * LDF * 4;
+constexpr uint32_t OFF_MS = OFF_TF + C * LDF * 4;
+static_assert(OFF_MS + 32 * LDM * 4 <= OFF_SB, "solver scratch overflows its alias");
+constexpr uint32_t V_ETA = OFF_VEC, V_GAM = V_ETA + 256, V_G = V_GAM + 256, V_GM = V_G + 256;
+constexpr uint32_t V_WC = V_GM + 256, V_MISC = V_WC + 256;
+constexpr uint32_t OFF_BAR = V_MISC + 64;
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 64;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;   // slack for 1024-byte alignment
+static_assert(SMEM_ALLOC <= 227 * KB, "shared memory budget");
+
+// tensor-memory columns (128 lanes x 32 bit each)
+constexpr uint32_t COL_A = 0;     // G, then W^T
+constexpr uint32_t COL_B = 64;    // U^T, then R^T
+constexpr uint32_t COL_O1 = 128;  // (Q S0)^T
+constexpr uint32_t COL_O2 = 192;  // (P R)^T
+constexpr uint32_t COL_S = 256;   // state, 128 columns
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+__device__ __forceinline__ void st_row8_bf16(uint32_t addr, const float *v) {
+    st_shared_v4(addr, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                 pack_bf16(v[6], v[7]));
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+               const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t chain = blockIdx.x;
+    const int64_t T = a.T;
+    const int nchunks = (int)((T + C - 1) / C);
+    const bool falcon = (a.mode == FW_FALCON1);
+    const bool elu = (a.phi == FW_PHI_ELU1);
+    const uint64_t limit = (uint64_t)a.wait_ns;
+
+    float *s_eta = reinterpret_cast<float *>(sm + V_ETA);
+    float *s_gam = reinterpret_cast<float *>(sm + V_GAM);
+    float *s_g = reinterpret_cast<float *>(sm + V_G);
+    float *s_gm = reinterpret_cast<float *>(sm + V_GM);
+    float *s_wc = reinterpret_cast<float *>(sm + V_WC);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + V_MISC);
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(sm + V_MISC + 4);
+    volatile float *s_gC = reinterpret_cast<volatile float *>(sm + V_MISC + 8);
+    const uint32_t bar_full0 = sb + OFF_BAR, bar_full1 = sb + OFF_BAR + 8;
+    const uint32_t bar_empty0 = sb + OFF_BAR + 16, bar_empty1 = sb + OFF_BAR + 24;
+    const uint32_t bar_mma = sb + OFF_BAR + 32, bar_never = sb + OFF_BAR + 40;
+
+    if (tid == 0) {
+        mbar_init(bar_full0, 1);
+        mbar_init(bar_full1, 1);
+        mbar_init(bar_empty0, 1);
+        mbar_init(bar_empty1, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_never, 1);
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(sb + V_MISC + 4, TMEM_COLS);
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued0 = 0, issued1 = 0;
+            bool ok = true;
+            const int shift = falcon ? 1 : 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1;
+                const uint32_t full = s ? bar_full1 : bar_full0;
+                if (c >= 2 && !mbar_wait(s ? bar_empty1 : bar_empty0, ((c >> 1) - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                if (*s_abort) break;
+                const uint32_t st = sb + s * STAGE;
+                const int y = c * C;
+                mbar_expect_tx(full, STAGE);
+                tma_load_3d(st + ST_X0, &tmk, 0, y - shift, (int)chain, full);
+                tma_load_3d(st + ST_X1, &tmk, 64, y - shift, (int)chain, full);
+                tma_load_3d(st + ST_Q0, &tmq, 0, y, (int)chain, full);
+                tma_load_3d(st + ST_Q1, &tmq, 64, y, (int)chain, full);
+                tma_load_3d(st + ST_Y0, &tmv, 0, y, (int)chain, full);
+                tma_load_3d(st + ST_Y1, &tmv, 64, y, (int)chain, full);
+                if (s) ++issued1; else ++issued0;
+            }
+            // never leave a copy in flight into this CTA's shared memory
+            bool drained = true;
+            if (issued0) drained &= mbar_wait(bar_full0, (issued0 - 1) & 1, kDrainNs);
+            if (issued1) drained &= mbar_wait(bar_full1, (issued1 - 1) & 1, kDrainNs);
+            if (!ok || !drained) atomicExch(a.err, kDevErrTimeout);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ math warps
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        uint32_t mma_phase = 0;
+        bool mma_pending = false;
+        bool fail = false;
+        float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
+        float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
+        float *Ms = reinterpret_cast<float *>(sm + OFF_MS);
+
+        // collective bounded wait: true when every math thread saw the phase
+        auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+            const bool ok = mbar_wait(bar, parity, limit);
+            return !bar_or(1, NMATH, !ok);
+        };
+        auto wait_mma = [&]() -> bool {
+            if (!wait_all(bar_mma, mma_phase)) return false;
+            mma_phase ^= 1u;
+            mma_pending = false;
+            tc_fence_after();
+            return true;
+        };
+        auto sync_math = [&]() { bar_sync(1, NMATH); };
+
+        // feature map on the freshly loaded tiles, k_init patch
+        auto prep = [&](int cc) {
+            const uint32_t st = sb + (uint32_t)(cc & 1) * STAGE;
+            bool wrote = false;
+            if (elu) {
+                const int t = tid >> 1, b = tid & 1;
+                const int64_t srcx = (int64_t)cc * C + t - (falcon ? 1 : 0);
+                const int64_t srcq = (int64_t)cc * C + t;
+                const uint32_t roff = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
+                for (int which = 0; which < (falcon ? 1 : 2); ++which) {
+                    const int64_t src = which == 0 ? srcx : srcq;
+                    if (src < 0 || src >= T) continue;
+                    const uint32_t row = st + (which == 0 ? (b ? ST_X1 : ST_X0) : (b ? ST_Q1 : ST_Q0)) + roff;
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const uint4 u = ld_shared_v4(row + c16 * 16);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 p = unpack_bf16(w[e]);
+                            f[2 * e] = apply_phi(FW_PHI_ELU1, p.x);
+                            f[2 * e + 1] = apply_phi(FW_PHI_ELU1, p.y);
+                        }
+                        st_row8_bf16(row + c16 * 16, f);
+                    }
+                }
+                wrote = true;
+            }
+            if (falcon && cc == 0 && a.k_init) {
+                if (tid < 16) {
+                    const int b = tid >> 3, c16 = tid & 7;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(a.k_init) + chain * D + b * 64 + c16 * 8);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 p = unpack_bf16(w[e]);
+                        f[2 * e] = apply_phi(a.phi, p.x);
+                        f[2 * e + 1] = apply_phi(a.phi, p.y);
+                    }
+                    st_row8_bf16(st + (b ? ST_X1 : ST_X0) + (uint32_t)c16 * 16u, f);
+                }
+                wrote = true;
+            }
+            if (wrote) fence_proxy_async();
+            sync_math();
+        };
+
+        // per-token step sizes and decay products of chunk cc
+        auto gates = [&](int cc) {
+            if (!falcon) return;
+            if (tid < C) {
+                const int t = tid;
+                const int64_t tok = (int64_t)cc * C + t;
+                const uint32_t st = sb + (uint32_t)(cc & 1) * STAGE;
+                float n = 0.f;
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const uint32_t row = st + (b ? ST_X1 : ST_X0) + (uint32_t)(t >> 3) * 1024u +
+                                         (uint32_t)(t & 7) * 128u;
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const uint4 u = ld_shared_v4(row + c16 * 16);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 p = unpack_bf16(w[e]);
+                            n = fmaf(p.x, p.x, n);
+                            n = fmaf(p.y, p.y, n);
+                        }
+                    }
+                }
+                float eta = 0.f, gam = 1.f;
+                if (tok < T) {
+                    const float lam = a.lam[chain * T + tok];
+                    const bool pair = (tok > 0) || (a.k_init != nullptr);
+                    eta = pair ? a.beta[chain * T + tok] / (n + lam + a.eps) : 0.f;
+                    gam = 1.f - eta * lam;
+                }
+                s_eta[t] = eta;
+                s_gam[t] = gam;
+            }
+            sync_math();
+            if (warp == 0) {
+                // inclusive prefix products G_t and exclusive suffix products
+                float g0 = s_gam[lane], g1 = s_gam[lane + 32];
+                float h0 = g0, h1 = g1;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
+                    const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
+                    const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
+                    const float d1 = __shfl_down_sync(0xffffffffu, h1, off);
+                    if (lane >= off) { g0 *= u0; g1 *= u1; }
+                    if (lane + off < 32) { h0 *= d0; h1 *= d1; }
+                }
+                const float tot0 = __shfl_sync(0xffffffffu, g0, 31);  // prod gamma_0..31
+                const float tot1 = __shfl_sync(0xffffffffu, h1, 0);   // prod gamma_32..63
+                g1 *= tot0;
+                h0 *= tot1;
+                float e0 = __shfl_up_sync(0xffffffffu, g0, 1);
+                float e1 = __shfl_up_sync(0xffffffffu, g1, 1);
+                if (lane == 0) { e0 = 1.f; e1 = tot0; }
+                float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
+                float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
+                if (lane == 31) { x0 = tot1; x1 = 1.f; }
+                s_g[lane] = g0;
+                s_g[lane + 32] = g1;
+                s_gm[lane] = e0;
+                s_gm[lane + 32] = e1;
+                s_wc[lane] = x0 * s_eta[lane];
+                s_wc[lane + 32] = x1 * s_eta[lane + 32];
+                if (lane == 31) *s_gC = g1;
+            }
+            sync_math();
+        };
+
+        if (a.force_timeout) fail = !wait_all(bar_never, 0);
+        if (!fail) fail = !wait_all(bar_full0, 0);
+        if (!fail) {
+            if (!falcon && tid < C) {
+                s_g[tid] = 1.f;
+                s_wc[tid] = 1.f;
+            }
+            if (!falcon && tid == 0) *s_gC = 1.f;
+            prep(0);
+            gates(0);
+            // initial state: TMEM <- G_{C-1} S0, bf16 copy for the MMAs
+            const float gC0 = *s_gC;
+            const int i = tid;
+#pragma unroll 1
+            for (int q = 0; q < 8; ++q) {
+                float v[16];
+                if (a.S0) {
+                    const float4 *src = reinterpret_cast<const float4 *>(a.S0 + (chain * D + i) * D + 16 * q);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 f = src[e];
+                        v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = 0.f;
+                }
+                const uint32_t blk = sb + OFF_SB + (uint32_t)(q >> 2) * 16384u;
+                const uint32_t c16 = (uint32_t)((16 * q) & 63) >> 3;
+                st_row8_bf16(blk + sw128(i, c16), v);
+                st_row8_bf16(blk + sw128(i, c16 + 1), v + 8);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] *= gC0;
+                tmem_st16(tmem + lane_base + COL_S + 16 * q, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            fence_proxy_async();
+            sync_math();
+        }
+
+#pragma unroll 1
+        for (int c = 0; c < nchunks && !fail; ++c) {
+            const int s = c & 1;
+            const uint32_t st = sb + (uint32_t)s * STAGE;
+            const int64_t tok0 = (int64_t)c * C;
+
+            // (1) G = [X; Q] X^T  (rows 0..63: X X^T, rows 64..127: Q X^T)
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                    mma_bf16(tmem + COL_A, sdesc_sw128(st + ST_X0 + off, 16, 1024),
+                             sdesc_sw128(st + ST_X0 + off, 16, 1024), id, kk > 0);
+                }
+                mma_commit(bar_mma);
+            }
+            mma_pending = true;
+            if (!wait_mma()) { fail = true; break; }
+
+            // (2) L rows (fp32, for the solver) and P rows (bf16 MMA operand)
+            {
+                float g[64];
+                tmem_ld32(tmem + lane_base + COL_A, g);
+                tmem_ld32(tmem + lane_base + COL_A + 32, g + 32);
+                if (falcon && tid < C) {
+                    const int t = tid;
+                    float dz = 1.f;
+#pragma unroll
+                    for (int s2 = C - 1; s2 >= 0; --s2) {
+                        const bool act = s2 < t;
+                        g[s2] = act ? dz * s_eta[s2] * g[s2] : 0.f;
+                        if (act) dz *= s_gam[s2];
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        *reinterpret_cast<float4 *>(Lf + t * LDF + 4 * q) =
+                            make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                } else if (tid >= C) {
+                    const int t = tid - C;
+                    float dz = 1.f;
+#pragma unroll
+                    for (int s2 = C - 1; s2 >= 0; --s2) {
+                        const bool act = s2 <= t;
+                        g[s2] = act ? (falcon ? dz * s_eta[s2] * g[s2] : g[s2]) : 0.f;
+                        if (act && falcon) dz *= s_gam[s2];
+                    }
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16)
+                        st_row8_bf16(sb + OFF_PB + sw128(t, c16), g + 8 * c16);
+                }
+                tc_fence_before();
+                fence_proxy_async();
+                sync_math();
+            }
+
+            if (falcon) {
+                // (3) T = (I + L)^{-1}: 16x16 diagonal blocks, then two block merges
+                {
+                    const int kk = lane & 15;
+                    const int base = 16 * warp;
+                    float tc[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                        for (int s2 = 0; s2 < t; ++s2) {
+                            const float l = Lf[(base + t) * LDF + base + s2];
+                            if (s2 & 1) acc1 = fmaf(l, tc[s2], acc1);
+                            else acc0 = fmaf(l, tc[s2], acc0);
+                        }
+                        tc[t] = (t == kk) ? 1.f : ((t > kk) ? -(acc0 + acc1) : 0.f);
+                    }
+                    if (lane < 16) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            Tf[(base + t) * LDF + base + kk] = tc[t];
+                            if ((warp & 1) == 0) Tf[(base + t) * LDF + base + 16 + kk] = 0.f;
+                        }
+                    }
+                }
+                sync_math();
+                {   // T_{b+1,b} = -T_{b+1,b+1} L_{b+1,b} T_{b,b} for the pairs (1,0), (3,2)
+                    const int p = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
+                    const int rb = 16 + 32 * p, cb = 32 * p;
+                    float m[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int s2 = 0; s2 < 16; ++s2) {
+                        const float l = Lf[(rb + r) * LDF + cb + s2];
+                        const float4 tv = *reinterpret_cast<const float4 *>(Tf + (cb + s2) * LDF + cb + 4 * cg);
+                        m[0] = fmaf(l, tv.x, m[0]); m[1] = fmaf(l, tv.y, m[1]);
+                        m[2] = fmaf(l, tv.z, m[2]); m[3] = fmaf(l, tv.w, m[3]);
+                    }
+                    *reinterpret_cast<float4 *>(Ms + (p * 16 + r) * LDM + 4 * cg) =
+                        make_float4(m[0], m[1], m[2], m[3]);
+                    sync_math();
+                    float u[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int s2 = 0; s2 < 16; ++s2) {
+                        const float tl = Tf[(rb + r) * LDF + rb + s2];
+                        const float4 mv = *reinterpret_cast<const float4 *>(Ms + (p * 16 + s2) * LDM + 4 * cg);
+                        u[0] = fmaf(tl, mv.x, u[0]); u[1] = fmaf(tl, mv.y, u[1]);
+                        u[2] = fmaf(tl, mv.z, u[2]); u[3] = fmaf(tl, mv.w, u[3]);
+                    }
+                    *reinterpret_cast<float4 *>(Tf + (rb + r) * LDF + cb + 4 * cg) =
+                        make_float4(-u[0], -u[1], -u[2], -u[3]);
+                }
+                sync_math();
+                {   // T[32:64, 0:32] = -T[32:64,32:64] L[32:64, 0:32] T[0:32, 0:32]
+                    const int r = tid >> 2, cg = tid & 3;
+                    float m[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m[e] = 0.f;
+#pragma unroll 8
+                    for (int s2 = 0; s2 < 32; ++s2) {
+                        const float l = Lf[(32 + r) * LDF + s2];
+                        const float4 a0 = *reinterpret_cast<const float4 *>(Tf + s2 * LDF + 8 * cg);
+                        const float4 a1 = *reinterpret_cast<const float4 *>(Tf + s2 * LDF + 8 * cg + 4);
+                        m[0] = fmaf(l, a0.x, m[0]); m[1] = fmaf(l, a0.y, m[1]);
+                        m[2] = fmaf(l, a0.z, m[2]); m[3] = fmaf(l, a0.w, m[3]);
+                        m[4] = fmaf(l, a1.x, m[4]); m[5] = fmaf(l, a1.y, m[5]);
+                        m[6] = fmaf(l, a1.z, m[6]); m[7] = fmaf(l, a1.w, m[7]);
+                    }
+                    *reinterpret_cast<float4 *>(Ms + r * LDM + 8 * cg) = make_float4(m[0], m[1], m[2], m[3]);
+                    *reinterpret_cast<float4 *>(Ms + r * LDM + 8 * cg + 4) = make_float4(m[4], m[5], m[6], m[7]);
+                    sync_math();
+                    float u[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) u[e] = 0.f;
+#pragma unroll 8
+                    for (int s2 = 0; s2 < 32; ++s2) {
+                        const float tl = Tf[(32 + r) * LDF + 32 + s2];
+                        const float4 b0 = *reinterpret_cast<const float4 *>(Ms + s2 * LDM + 8 * cg);
+                        const float4 b1 = *reinterpret_cast<const float4 *>(Ms + s2 * LDM + 8 * cg + 4);
+                        u[0] = fmaf(tl, b0.x, u[0]); u[1] = fmaf(tl, b0.y, u[1]);
+                        u[2] = fmaf(tl, b0.z, u[2]); u[3] = fmaf(tl, b0.w, u[3]);
+                        u[4] = fmaf(tl, b1.x, u[4]); u[5] = fmaf(tl, b1.y, u[5]);
+                        u[6] = fmaf(tl, b1.z, u[6]); u[7] = fmaf(tl, b1.w, u[7]);
+                    }
+                    *reinterpret_cast<float4 *>(Tf + (32 + r) * LDF + 8 * cg) = make_float4(-u[0], -u[1], -u[2], -u[3]);
+                    *reinterpret_cast<float4 *>(Tf + (32 + r) * LDF + 8 * cg + 4) = make_float4(-u[4], -u[5], -u[6], -u[7]);
+                }
+                sync_math();
+                {   // bf16 T and T diag(Gm), lower triangle, K-major rows t
+                    const int t = tid >> 1, h = tid & 1;
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const int c16 = 4 * h + m4;
+                        float v[8], vp[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int col = 8 * c16 + e;
+                            v[e] = (col <= t) ? Tf[t * LDF + col] : 0.f;
+                            vp[e] = v[e] * s_gm[col];
+                        }
+                        st_row8_bf16(sb + OFF_TB + sw128(t, c16), v);
+                        st_row8_bf16(sb + OFF_TPB + sw128(t, c16), vp);
+                    }
+                }
+                fence_proxy_async();
+                sync_math();
+
+                // (4) W^T = X^T (T diag Gm)^T -> COL_A,  U^T = Y^T T^T -> COL_B
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t id = idesc_bf16(128, 64, true, false);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_A, sdesc_sw128(st + ST_X0 + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(sb + OFF_TPB + kk * 32, 16, 1024), id, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_B, sdesc_sw128(st + ST_Y0 + kk * 2048, 8192, 1024),
+                                 sdesc_sw128(sb + OFF_TB + kk * 32, 16, 1024), id, kk > 0);
+                    mma_commit(bar_mma);
+                }
+                mma_pending = true;
+                if (!wait_mma()) { fail = true; break; }
+
+                // (5) -W^T -> bf16 rows i (MN-major B operand)
+                {
+                    float w[64];
+                    tmem_ld32(tmem + lane_base + COL_A, w);
+                    tmem_ld32(tmem + lane_base + COL_A + 32, w + 32);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) w[e] = -w[e];
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16)
+                        st_row8_bf16(sb + OFF_WTB + sw128(tid, c16), w + 8 * c16);
+                    tc_fence_before();
+                    fence_proxy_async();
+                    sync_math();
+                }
+
+                // (6) R^T = U^T - S^T W^T (accumulate into COL_B), O1^T = S^T Q^T
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t idr = idesc_bf16(128, 64, true, true);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + COL_B, sdesc_sw128(sb + OFF_SB + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(sb + OFF_WTB + kk * 2048, 8192, 1024), idr, 1);
+                    const uint32_t ido = idesc_bf16(128, 64, true, false);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                        mma_bf16(tmem + COL_O1, sdesc_sw128(sb + OFF_SB + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(st + ST_Q0 + off, 16, 1024), ido, kk > 0);
+                    }
+                    mma_commit(bar_mma);
+                }
+                mma_pending = true;
+                if (!wait_mma()) { fail = true; break; }
+
+                // (7) R^T -> bf16 rows j (A operand) and scaled copy (B operand)
+                {
+                    float r[64];
+                    tmem_ld32(tmem + lane_base + COL_B, r);
+                    tmem_ld32(tmem + lane_base + COL_B + 32, r + 32);
+#pragma unroll
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        float w8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w8[e] = r[8 * c16 + e] * s_wc[8 * c16 + e];
+                        st_row8_bf16(sb + OFF_RA + sw128(tid, c16), r + 8 * c16);
+                        st_row8_bf16(sb + OFF_RB + sw128(tid, c16), w8);
+                    }
+                    tc_fence_before();
+                    fence_proxy_async();
+                    sync_math();
+                }
+
+                // (8) O2^T = R^T P^T,  S += X^T (diag(w) R)
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t ido = idesc_bf16(128, 64, false, false);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_O2, sdesc_sw128(sb + OFF_RA + kk * 32, 16, 1024),
+                                 sdesc_sw128(sb + OFF_PB + kk * 32, 16, 1024), ido, kk > 0);
+                    const uint32_t ids = idesc_bf16(128, 128, true, false);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_S, sdesc_sw128(st + ST_X0 + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(sb + OFF_RB + kk * 32, 16, 1024), ids, 1);
+                    mma_commit(bar_mma);
+                }
+                mma_pending = true;
+                if (!wait_mma()) { fail = true; break; }
+            } else {
+                // linear attention: O1^T = S^T Q^T, O2^T = V^T P^T, S += X^T V
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t ido = idesc_bf16(128, 64, true, false);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                        mma_bf16(tmem + COL_O1, sdesc_sw128(sb + OFF_SB + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(st + ST_Q0 + off, 16, 1024), ido, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_O2, sdesc_sw128(st + ST_Y0 + kk * 2048, 8192, 1024),
+                                 sdesc_sw128(sb + OFF_PB + kk * 32, 16, 1024), ido, kk > 0);
+                    const uint32_t ids = idesc_bf16(128, 128, true, true);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_S, sdesc_sw128(st + ST_X0 + kk * 2048, 16384, 1024),
+                                 sdesc_sw128(st + ST_Y0 + kk * 2048, 8192, 1024), ids, 1);
+                    mma_commit(bar_mma);
+                }
+                mma_pending = true;
+                if (!wait_mma()) { fail = true; break; }
+            }
+
+            // (9) o_t = G_t (S0^T q_t) + (P R)_t, column j = tid
+            {
+                __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(a.o) + (chain * T + tok0) * D + tid;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float o1[32], o2[32];
+                    tmem_ld32(tmem + lane_base + COL_O1 + 32 * h, o1);
+                    tmem_ld32(tmem + lane_base + COL_O2 + 32 * h, o2);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int t = 32 * h + e;
+                        if (tok0 + t < T) og[(int64_t)t * D] = __float2bfloat16_rn(fmaf(s_g[t], o1[e], o2[e]));
+                    }
+                }
+            }
+
+            // (10) the stage's tiles are no longer needed
+            tc_fence_before();
+            sync_math();
+            if (tid == 0) mbar_arrive(s ? bar_empty1 : bar_empty0);
+
+            // (11) gates of the next chunk (needs its key tile)
+            float gC_next = 1.f;
+            const bool last = (c + 1 == nchunks);
+            if (!last) {
+                const int s1 = (c + 1) & 1;
+                if (!wait_all(s1 ? bar_full1 : bar_full0, (uint32_t)((c + 1) >> 1) & 1u)) {
+                    fail = true;
+                    break;
+                }
+                prep(c + 1);
+                gates(c + 1);
+                gC_next = *s_gC;
+            }
+
+            // (12) state: bf16 copy for the next chunk's MMAs, pre-scale by its decay
+            {
+                const int i = tid;
+#pragma unroll 1
+                for (int q = 0; q < 8; ++q) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + COL_S + 16 * q, v);
+                    if (last) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + i) * D + 16 * q);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                    } else {
+                        const uint32_t blk = sb + OFF_SB + (uint32_t)(q >> 2) * 16384u;
+                        const uint32_t c16 = (uint32_t)((16 * q) & 63) >> 3;
+                        st_row8_bf16(blk + sw128(i, c16), v);
+                        st_row8_bf16(blk + sw128(i, c16 + 1), v + 8);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] *= gC_next;
+                        tmem_st16(tmem + lane_base + COL_S + 16 * q, v);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                fence_proxy_async();
+                sync_math();
+            }
+        }
+
+        if (fail) {
+            if (tid == 0) {
+                *s_abort = 1;
+                atomicExch(a.err, kDevErrTimeout);
+                // an MMA batch may still be running: let it finish before TMEM is freed
+                if (mma_pending) mbar_wait(bar_mma, mma_phase, kDrainNs);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [n_chains][T][128] bf16 viewed as a 3-D tensor (d, T, chain); 64 x 64 boxes.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)nc};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Falcon-1 with phi = elu+1 is declined: phi(k) is close to 1 + k for small
+// keys, and rounding it to a bf16 MMA operand erases most of the key's varying
+// part, which the residual write depends on (the per-token kernel keeps it in
+// fp32).  Linear attention accumulates phi(k) additively and keeps bf16
+// operand accuracy.
+bool chunked_supported(const PrefillArgs &a) {
+    if (a.mode == FW_FALCON1 && a.phi == FW_PHI_ELU1) return false;
+    return a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
+           a.n_chains <= (int64_t)INT32_MAX;
+}
+
+cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
+        !make_map(&tv, a.v, a.T, a.n_chains))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    chunked_kernel<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, a);
+    return cudaGetLastError();
+}
+
 }  // namespace fw

@@ -27,7 +27,8 @@ struct PrefillArgs {
     fw_phi phi;
     float eps;
     int *err;          // device error word
-    long long wait_limit;
+    long long wait_ns; // limit of every bounded device wait, nanoseconds
+    int force_timeout; // testing hook: wait on a barrier nothing arrives on
 };
 
 struct StepArgs {

@@ -41,7 +41,7 @@ class fw_shape(ctypes.Structure):
 
 
 EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_check", "fw_status_string",
-           "fw_version", "fw_last_cuda_error", "fw_set_wait_limit")
+           "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us", "fw_debug_force_timeout")
 
 _lib = None
 
@@ -64,8 +64,10 @@ def lib():
         L.fw_status_string.restype = ctypes.c_char_p
         L.fw_version.argtypes = []
         L.fw_last_cuda_error.argtypes = []
-        L.fw_set_wait_limit.argtypes = [ctypes.c_longlong]
-        L.fw_set_wait_limit.restype = None
+        L.fw_set_wait_limit_us.argtypes = [ctypes.c_longlong]
+        L.fw_set_wait_limit_us.restype = None
+        L.fw_debug_force_timeout.argtypes = [I]
+        L.fw_debug_force_timeout.restype = None
         for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_check, L.fw_version,
                   L.fw_last_cuda_error):
             f.restype = I

@@ -92,6 +92,8 @@ def test_chunked_unsupported_shapes(L):
     # fp32 or d = 64 calls are not taken by the chunked kernel.
     assert call_prefill(L, dtype=0, shape=(1, 1, 8, 128, 128), algo=2) == -8
     assert call_prefill(L, dtype=1, shape=(1, 1, 8, 64, 64), algo=2) == -8
+    # Falcon-1 with phi = elu+1 stays on the per-token kernel.
+    assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), phi=1, algo=2) == -8
 
 
 @no_gpu

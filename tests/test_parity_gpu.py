@@ -183,3 +183,93 @@ def test_bf16_workloads_full_size_sampled(name, chains):
     S_s = S.reshape(-1, d, d)[torch.as_tensor(chains, device=DEV)].cpu().unsqueeze(0)
     eo, es = rel_l2(to64(o_s), o_ref), rel_l2(to64(S_s), S_ref)
     assert eo <= 2e-2 and es <= 2e-2, (eo, es)
+
+
+# ---------------------------------------------------------------- chunked tensor-core kernel
+
+@pytest.mark.parametrize("mode,phi", [("falcon1", "identity"), ("linattn", "elu1"),
+                                      ("linattn", "identity")])
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 130, 257])
+def test_chunked_small(mode, phi, T):
+    w, x = _small(mode, torch.bfloat16, 128, T, s0=(T % 2 == 0), phi=phi, seed=T)
+    _check_prefill(w, x, "chunked")
+
+
+def test_chunked_declines_falcon1_elu1():
+    """Falcon-1 with phi = elu+1 is not taken by the chunked kernel (bf16
+    rounding of phi(k) ~ 1 + k loses the key's varying part); the default
+    path serves it with the per-token fp32 kernel within the bf16 gate."""
+    w, x = _small("falcon1", torch.bfloat16, 128, 63, phi="elu1")
+    g = _gpu(x)
+    with pytest.raises(fw.FwError) as ei:
+        fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], phi="elu1",
+                   algo="chunked")
+    assert ei.value.status == -8
+    _check_prefill(w, x, "auto")
+
+
+@pytest.mark.parametrize("T", [5, 64, 200])
+def test_chunked_k_init(T):
+    w, x = _small("falcon1", torch.bfloat16, 128, T)
+    kin = torch.randn(2, 3, 128).to(torch.bfloat16)
+    _check_prefill(w, x, "chunked", k_init=kin)
+
+
+def test_chunked_nonpositive_decay_and_zero_steps():
+    """Tokens with gamma <= 0 (tiny keys, large lambda), beta = 0 tokens and
+    zero keys: the chunk form uses no division by decay products."""
+    w, x = _small("falcon1", torch.bfloat16, 128, 190)
+    k = x["k"].float()
+    k[:, :, 10] *= 1e-3
+    k[:, :, 70] *= 1e-3
+    k[:, :, 100] = 0.0
+    x["k"] = k.to(torch.bfloat16)
+    x["lam"][:, :, 11] = 0.5
+    x["lam"][:, :, 71] = 0.5
+    x["beta"][:, :, 11] = 1.9
+    x["beta"][:, :, 71] = 1.9
+    x["beta"][:, :, 40:44] = 0.0
+    kf = x["k"].double()
+    n = (kf[:, :, 10] ** 2).sum(-1)
+    eta = x["beta"][:, :, 11].double() / (n + 0.5 + 1e-6)
+    assert (1 - eta * 0.5).max() < 0.0
+    _check_prefill(w, x, "chunked")
+
+
+@pytest.mark.parametrize("mode", ["falcon1", "linattn"])
+def test_chunked_matches_recurrent_kernel(mode):
+    """The two CUDA kernels agree with each other (and the oracle) on a
+    mid-size case spanning many chunks."""
+    w, x = _small(mode, torch.bfloat16, 128, 1000, B=2, H=4)
+    g = _gpu(x)
+    outs = {}
+    for algo in ("chunked", "recurrent"):
+        outs[algo] = fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"],
+                                mode=w.mode, phi=w.phi, eps=w.eps, algo=algo)
+    fw.check()
+    o_ref, S_ref = oracle_prefill(w.mode, w.phi, w.eps, x)
+    for algo, (o, S) in outs.items():
+        assert rel_l2(to64(o), o_ref) <= 2e-2, algo
+        assert rel_l2(to64(S), S_ref) <= 2e-2, algo
+    assert rel_l2(to64(outs["chunked"][1]), to64(outs["recurrent"][1])) <= 2e-2
+
+
+def test_chunked_timeout_path_reports_and_recovers():
+    """A bounded wait on a barrier nothing arrives on runs out: the kernel
+    reports FW_ERR_TIMEOUT through fw_check, frees its resources and the
+    context stays usable for the next call."""
+    L = fw.lib()
+    w, x = _small("falcon1", torch.bfloat16, 128, 300)
+    g = _gpu(x)
+    L.fw_set_wait_limit_us(2000)
+    L.fw_debug_force_timeout(1)
+    try:
+        fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], algo="chunked")
+        with pytest.raises(fw.FwError) as ei:
+            fw.check()
+        assert ei.value.status == -7
+    finally:
+        L.fw_debug_force_timeout(0)
+        L.fw_set_wait_limit_us(0)
+    fw.check()  # error word was cleared
+    _check_prefill(w, x, "chunked")
