@@ -49,15 +49,19 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra=(), out: str = LIB,
+          build_dir: str = BUILD_DIR) -> str:
+    """Compile every csrc/*.cu and link `out` (default: the in-tree libfw.so).
+    `extra` adds nvcc flags (e.g. a -D switch for an instrumented variant,
+    written to another `out` and `build_dir`)."""
+    if not force and out == LIB and up_to_date():
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -71,13 +75,13 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(one, srcs))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = out + ".tmp.%d" % os.getpid()
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
