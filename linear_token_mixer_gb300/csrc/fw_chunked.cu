@@ -27,8 +27,9 @@
 //   warp 2      state-path MMA issuer: R^T = U^T - S^T W^T, O1^T = S^T Q^T,
 //               O2^T = R^T P^T, S += X^T (diag(w) R).
 //   warp 3      tensor-memory allocation.
-//   warps 4-7   key group: feature map, gates and decay products, L and P from
-//               G, the triangular solve, -W^T staging.
+//   warps 4-7,  key group (two warps per tensor-memory lane quarter, each
+//   12-15       owning half the columns): feature map, gates and decay products,
+//               L and P from G, the triangular solve, -W^T staging.
 //   warps 8-11  state group: R staging, state carry (fp32 in tensor memory,
 //               bf16 copy in shared memory as the MMA operand), outputs
 //               o_t = G_t O1_t + O2_t.
@@ -53,11 +54,12 @@ using namespace sm100;
 
 constexpr int C = 64;        // chunk length
 constexpr int D = 128;       // d_k = d_v
-constexpr int NTHREADS = 384;
-constexpr int KG_W0 = 4;     // first warp of the key group
+constexpr int NTHREADS = 512;
+constexpr int KG_W0 = 4;     // first warp of the key group (lane quarters 0..3, column half 0)
 constexpr int SG_W0 = 8;     // first warp of the state group
-constexpr int BAR_KG = 1, BAR_SG = 2;
-constexpr int GROUP = 128;
+constexpr int KG2_W0 = 12;   // key group, column half 1
+constexpr int BAR_KG = 1, BAR_SG = 2;   // named barriers of the two groups
+constexpr int GROUP = 128, KGROUP = 256;
 
 constexpr uint32_t KB = 1024;
 // shared memory (offsets from a 1024-aligned base)
@@ -74,10 +76,11 @@ constexpr uint32_t OFF_RA = 128 * KB;   // R^T, bf16, rows j (K-major A operand)
 constexpr uint32_t OFF_RB = 144 * KB;   // (diag(w) R)^T, bf16, rows j (K-major B operand)
 constexpr uint32_t OFF_SB = 160 * KB;   // S, bf16, rows i, two 64-column blocks (16 KB each)
 constexpr uint32_t OFF_TF = 192 * KB;   // T, fp32 64x64, swizzled
-constexpr uint32_t OFF_MS = 208 * KB;   // solver scratch: 4 x 2 KB per-warp 16x16 pairs, or 32x32
-constexpr uint32_t OFF_VEC = 216 * KB;  // two gate blocks of 1536 B
-constexpr uint32_t VEC_BYTES = 1536;
-constexpr uint32_t V_ETA = 0, V_GAM = 256, V_G = 512, V_GM = 768, V_WC = 1024, V_GC = 1280;
+constexpr uint32_t OFF_MS = 208 * KB;   // solver scratch: 4 warps x 3 fragment-ordered 16x16, or 32x32
+constexpr uint32_t OFF_VEC = 220 * KB;  // two gate blocks
+constexpr uint32_t VEC_BYTES = 1792;
+constexpr uint32_t V_ETA = 0, V_GAM = 256, V_G = 512, V_GM = 768, V_WC = 1024, V_Q32 = 1280,
+                   V_GC = 1536;
 constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
 constexpr uint32_t OFF_SGV = OFF_MISC + 64;    // G_t of the chunk the state group is on
@@ -129,14 +132,15 @@ __device__ __forceinline__ void unpack8(const uint4 u, float *f) {
     }
 }
 
-// Bounded wait for the single-thread roles (producer, MMA issuers): polls
-// without parking, so a hand-off is seen as soon as it lands.
+// Bounded wait for the single-thread roles (producer, MMA issuers): parked like
+// the group waits (a spinning warp would steal issue slots from the math warps
+// that share its scheduler).
 __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, uint64_t limit,
                                           volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > limit) return false;
     }
@@ -156,22 +160,33 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t
 }
 
 // tf32 fragments of a 16x8 A tile / 8x8 B tile of a swizzled fp32 matrix.
+// (fp32 bits go in as is: the tf32 MMA reads the top 19 bits of each operand)
 __device__ __forceinline__ void frag_a64(const float *M, int r0, int k0, int lane, uint32_t (&a)[4]) {
     const int g = lane >> 2, t = lane & 3;
-    a[0] = f2tf32(M[f64i(r0 + g, k0 + t)]);
-    a[1] = f2tf32(M[f64i(r0 + g + 8, k0 + t)]);
-    a[2] = f2tf32(M[f64i(r0 + g, k0 + t + 4)]);
-    a[3] = f2tf32(M[f64i(r0 + g + 8, k0 + t + 4)]);
+    a[0] = __float_as_uint(M[f64i(r0 + g, k0 + t)]);
+    a[1] = __float_as_uint(M[f64i(r0 + g + 8, k0 + t)]);
+    a[2] = __float_as_uint(M[f64i(r0 + g, k0 + t + 4)]);
+    a[3] = __float_as_uint(M[f64i(r0 + g + 8, k0 + t + 4)]);
 }
 __device__ __forceinline__ void frag_b64(const float *M, int k0, int n0, int lane, uint32_t (&b)[2]) {
     const int g = lane >> 2, t = lane & 3;
-    b[0] = f2tf32(M[f64i(k0 + t, n0 + g)]);
-    b[1] = f2tf32(M[f64i(k0 + t + 4, n0 + g)]);
+    b[0] = __float_as_uint(M[f64i(k0 + t, n0 + g)]);
+    b[1] = __float_as_uint(M[f64i(k0 + t + 4, n0 + g)]);
 }
 __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lane, uint32_t (&b)[2]) {
     const int g = lane >> 2, t = lane & 3;
-    b[0] = f2tf32(M[f32i(k0 + t, n0 + g)]);
-    b[1] = f2tf32(M[f32i(k0 + t + 4, n0 + g)]);
+    b[0] = __float_as_uint(M[f32i(k0 + t, n0 + g)]);
+    b[1] = __float_as_uint(M[f32i(k0 + t + 4, n0 + g)]);
+}
+
+// 16x16 fp32 scratch in fragment order: "A order" holds each lane's m16n8k8 A
+// fragment of k-step ks as one float4, "B order" each lane's B fragment of
+// (ks, nt) as one float2, so an operand fetch is a single vector load.
+__device__ __forceinline__ int a_ord(int r, int c) {
+    return (((c >> 3) * 32 + (r & 7) * 4 + (c & 3)) << 2) + (r >> 3) + 2 * ((c & 7) >> 2);
+}
+__device__ __forceinline__ int b_ord(int r, int c) {
+    return ((((r >> 3) * 2 + (c >> 3)) * 32 + (c & 7) * 4 + (r & 3)) << 1) + ((r & 7) >> 2);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -295,12 +310,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const uint64_t dtp = sdesc_sw128(sb + OFF_TPB, 16, 1024);
                     const uint64_t dy = sdesc_sw128(sb + OFF_Y0, 8192, 1024);
                     const uint64_t dt = sdesc_sw128(sb + OFF_TB, 16, 1024);
+                    // two independent accumulator chains, interleaved
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 4; ++kk) {
                         mma_bf16(tmem + COL_W, dx + kk * 128, dtp + kk * 2, id, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
                         mma_bf16(tmem + COL_R0 + 64 * b, dy + kk * 128, dt + kk * 2, id, kk > 0);
+                    }
                     mma_commit(bar(B_WUDONE));
                     mma_commit(bar(B_YFREE));
                     TRACE(c, 16);
@@ -336,12 +351,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const uint32_t id_mm = idesc_bf16(128, 64, true, true);
                     const uint64_t dw = sdesc_sw128(sb + OFF_WTB, 8192, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < 8; ++kk) {
                         mma_bf16(tmem + COL_R0 + 64 * b, ds + kk * 128, dw + kk * 128, id_mm, 1);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
                         mma_bf16(tmem + COL_O1, ds + kk * 128,
                                  dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
+                    }
                     mma_commit(bar(B_RDONE));
                     TRACE(c, 17);
                     if (!wait_fast(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
@@ -350,27 +364,25 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const uint32_t id_kk = idesc_bf16(128, 64, false, false);
                     const uint64_t dra = sdesc_sw128(sb + OFF_RA, 16, 1024);
                     const uint64_t drb = sdesc_sw128(sb + OFF_RB, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_O2, dra + kk * 2, dp + kk * 2, id_kk, kk > 0);
                     const uint32_t id_s = idesc_bf16(128, 128, true, false);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 4; ++kk) {
                         mma_bf16(tmem + COL_S, dx + kk * 128, drb + kk * 2, id_s, 1);
+                        mma_bf16(tmem + COL_O2, dra + kk * 2, dp + kk * 2, id_kk, kk > 0);
+                    }
                 } else {
                     const uint64_t dv = sdesc_sw128(sb + (b ? OFF_Y1 : OFF_Y0), 8192, 1024);
                     // O1^T = S^T Q^T, O2^T = V^T P^T;  S += X^T V
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + COL_O1, ds + kk * 128,
-                                 dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_O2, dv + kk * 128, dp + kk * 2, id_mk, kk > 0);
                     const uint32_t id_s = idesc_bf16(128, 128, true, true);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_S, dx + kk * 128, dv + kk * 128, id_s, 1);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        mma_bf16(tmem + COL_O1, ds + kk * 128,
+                                 dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
+                        if (kk < 4) {
+                            mma_bf16(tmem + COL_S, dx + kk * 128, dv + kk * 128, id_s, 1);
+                            mma_bf16(tmem + COL_O2, dv + kk * 128, dp + kk * 2, id_mk, kk > 0);
+                        }
+                    }
                 }
                 mma_commit(bar(B_SDONE));
                 mma_commit(bar(B_PFREE0 + b));
@@ -382,40 +394,45 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             mbar_wait(bar(B_SDRAIN), 0, kDrainNs);
         }
         __syncwarp();
-    } else if (warp >= KG_W0 && warp < SG_W0) {
+    } else if ((warp >= KG_W0 && warp < SG_W0) || warp >= KG2_W0) {
         // ================================================================ key group
-        const int kt = tid - KG_W0 * 32;           // == TMEM lane of this thread
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        // 8 warps: two per TMEM lane quarter.  Thread (kt, h) owns row kt of the
+        // 128-lane tiles and the column half [32h, 32h + 32).
+        const int h = (warp >= KG2_W0) ? 1 : 0;
+        const int kt = (warp & 3) * 32 + lane;     // TMEM lane of this thread
+        const int kidx = h * 128 + kt;             // 0..255 within the group
+        const int kw = warp & 3;                   // lane quarter
+        const uint32_t lane_base = (uint32_t)(kw * 32) << 16;
         float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Ms = reinterpret_cast<float *>(sm + OFF_MS);
-        const int kw = warp - KG_W0;
         auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool ok = wait_bar(bb, parity, limit, s_abort);
-            return !bar_or(BAR_KG, GROUP, !ok);
+            return !bar_or(BAR_KG, KGROUP, !ok);
         };
-        auto gsync = [&]() { bar_sync(BAR_KG, GROUP); };
+        auto gsync = [&]() { bar_sync(BAR_KG, KGROUP); };
 
-        if (!falcon && kt < C) {
+        if (!falcon && kidx < C) {
             for (int b = 0; b < 2; ++b) {
                 float *v = vec(b);
-                v[V_ETA / 4 + kt] = 1.f;
-                v[V_GAM / 4 + kt] = 1.f;
-                v[V_G / 4 + kt] = 1.f;
-                v[V_GM / 4 + kt] = 1.f;
-                v[V_WC / 4 + kt] = 1.f;
-                if (kt == 0) v[V_GC / 4] = 1.f;
+                v[V_ETA / 4 + kidx] = 1.f;
+                v[V_GAM / 4 + kidx] = 1.f;
+                v[V_G / 4 + kidx] = 1.f;
+                v[V_GM / 4 + kidx] = 1.f;
+                v[V_WC / 4 + kidx] = 1.f;
+                v[V_Q32 / 4 + kidx] = 1.f;
+                if (kidx == 0) v[V_GC / 4] = 1.f;
             }
         }
 
         bool ok = true;
         // testing hook: a wait on a barrier nothing arrives on runs out
         if (a.force_timeout && !gwait(bar(B_NEVER), 0)) ok = false;
-        // beta, lambda of the next chunk are loaded one chunk ahead (thread t < C)
+        // beta, lambda of the next chunk are loaded one chunk ahead (kidx < C)
         float nb = 0.f, nl = 0.f;
         auto load_gates = [&](int cc) {
-            const int64_t tok = (int64_t)cc * C + kt;
-            if (falcon && kt < C && cc < nch && tok < T) {
+            const int64_t tok = (int64_t)cc * C + kidx;
+            if (falcon && kidx < C && cc < nch && tok < T) {
                 nb = a.beta[chain * T + tok];
                 nl = a.lam[chain * T + tok];
             }
@@ -427,32 +444,36 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const uint32_t st = xq(b);
             float *vb = vec(b);
             if (!gwait(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u)) { ok = false; break; }
-            if (kt == 0) TRACE(c, 0);
+            if (kidx == 0) TRACE(c, 0);
 
-            // ---- feature map on the loaded tiles, k_init patch
+            // ---- feature map on the loaded tiles (row t, a quarter of its 16-byte
+            //      chunks per thread), k_init patch
             {
                 bool wrote = false;
                 if (elu) {
-                    const int t = kt >> 1, hb = kt & 1;
+                    const int t = kidx >> 2, qq = kidx & 3;
                     const uint32_t roff = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
                     for (int which = 0; which < (falcon ? 1 : 2); ++which) {
                         const int64_t src = (int64_t)c * C + t - ((which == 0 && falcon) ? 1 : 0);
                         if (src < 0 || src >= T) continue;
-                        const uint32_t row = st + (which == 0 ? (hb ? XQ_X1 : XQ_X0) : (hb ? XQ_Q1 : XQ_Q0)) + roff;
 #pragma unroll
-                        for (int c16 = 0; c16 < 8; ++c16) {
+                        for (int m = 0; m < 4; ++m) {
+                            const int cidx = 4 * qq + m;   // 0..15: block (cidx >> 3), chunk (cidx & 7)
+                            const uint32_t row = st + (which == 0 ? ((cidx >> 3) ? XQ_X1 : XQ_X0)
+                                                                  : ((cidx >> 3) ? XQ_Q1 : XQ_Q0)) + roff;
+                            const uint32_t ad = row + (uint32_t)(cidx & 7) * 16u;
                             float f[8];
-                            unpack8(ld_shared_v4(row + c16 * 16), f);
+                            unpack8(ld_shared_v4(ad), f);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) f[e] = f[e] > 0.f ? f[e] + 1.f : __expf(f[e]);
-                            st_row8_bf16(row + c16 * 16, f);
+                            st_row8_bf16(ad, f);
                         }
                     }
                     wrote = true;
                 }
                 if (falcon && c == 0 && a.k_init) {
-                    if (kt < 16) {
-                        const int hb = kt >> 3, c16 = kt & 7;
+                    if (kidx < 16) {
+                        const int hb = kidx >> 3, c16 = kidx & 7;
                         const uint4 u = *reinterpret_cast<const uint4 *>(
                             static_cast<const __nv_bfloat16 *>(a.k_init) + chain * D + hb * 64 + c16 * 8);
                         float f[8];
@@ -466,26 +487,32 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (wrote) fence_proxy_async();
             }
             gsync();   // mapped tiles (and the k_init row) complete: the Gram MMA may start
-            if (kt == 0) mbar_arrive(bar(B_GGO));
+            if (kidx == 0) mbar_arrive(bar(B_GGO));
 
             if (!gwait(bar(B_GDONE), (uint32_t)c & 1u)) { ok = false; break; }
-            if (kt == 0) TRACE(c, 2);
+            if (kidx == 0) TRACE(c, 2);
             tc_fence_after();
             if (c >= 2 && !gwait(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u)) { ok = false; break; }
-            float g[64];   // row kt of G = [X;Q] X^T
-            tmem_ld32(tmem + lane_base + COL_G, g);
-            tmem_ld32(tmem + lane_base + COL_G + 32, g + 32);
+            float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
+            tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
+            if (kidx == 0) TRACE(c, 20);
 
             // ---- step sizes and decay products of chunk c; |x_t|^2 is G[t,t]
             if (falcon) {
-                if (kt < C) {
-                    const int t = kt;
-                    const int64_t tok = (int64_t)c * C + t;
-                    const float bt = nb, lt = nl;
-                    load_gates(c + 1);
+                if (kt < C && (kt >> 5) == h) {   // the thread whose half holds the diagonal
                     float n = 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < C; ++s2) n = (s2 == t) ? g[s2] : n;
+                    for (int s2 = 0; s2 < 32; ++s2) n = (s2 == lane) ? g[s2] : n;
+                    vb[V_ETA / 4 + kt] = n;   // |x_t|^2; the thread holding beta_t turns it into eta_t
+                }
+                gsync();
+                if (kidx == 0) TRACE(c, 21);
+                if (kidx < C) {
+                    const int t = kidx;
+                    const int64_t tok = (int64_t)c * C + t;
+                    const float n = vb[V_ETA / 4 + t];
+                    const float bt = nb, lt = nl;
+                    load_gates(c + 1);
                     float eta = 0.f, gam = 1.f;
                     if (tok < T) {
                         const bool pair = (tok > 0) || (a.k_init != nullptr);
@@ -496,208 +523,236 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     vb[V_GAM / 4 + t] = gam;
                 }
                 gsync();
-                if (kw == 0) {
+                if (kidx == 0) TRACE(c, 22);
+                if (kidx < 32) {
+                    // warp of kidx 0..31: prefix products G_t, Gm_t, Q32_t = prod_{32..t}
                     float g0 = vb[V_GAM / 4 + lane], g1 = vb[V_GAM / 4 + lane + 32];
-                    float h0 = g0, h1 = g1;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
                         const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
-                        const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
-                        const float d1 = __shfl_down_sync(0xffffffffu, h1, off);
                         if (lane >= off) { g0 *= u0; g1 *= u1; }
-                        if (lane + off < 32) { h0 *= d0; h1 *= d1; }
                     }
                     const float tot0 = __shfl_sync(0xffffffffu, g0, 31);
-                    const float tot1 = __shfl_sync(0xffffffffu, h1, 0);
+                    vb[V_Q32 / 4 + lane + 32] = g1;   // prod_{i=32}^{t} gamma_i
                     g1 *= tot0;
-                    h0 *= tot1;
                     float e0 = __shfl_up_sync(0xffffffffu, g0, 1);
                     float e1 = __shfl_up_sync(0xffffffffu, g1, 1);
                     if (lane == 0) { e0 = 1.f; e1 = tot0; }
-                    float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
-                    float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
-                    if (lane == 31) { x0 = tot1; x1 = 1.f; }
                     vb[V_G / 4 + lane] = g0;
                     vb[V_G / 4 + lane + 32] = g1;
                     vb[V_GM / 4 + lane] = e0;
                     vb[V_GM / 4 + lane + 32] = e1;
+                    if (lane == 31) vb[V_GC / 4] = g1;
+                } else if (kidx >= 128 && kidx < 160) {
+                    // a warp of the other half: suffix products -> w_s = D[C-1,s] eta_s
+                    float h0 = vb[V_GAM / 4 + lane], h1 = vb[V_GAM / 4 + lane + 32];
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
+                        const float d1 = __shfl_down_sync(0xffffffffu, h1, off);
+                        if (lane + off < 32) { h0 *= d0; h1 *= d1; }
+                    }
+                    const float tot1 = __shfl_sync(0xffffffffu, h1, 0);
+                    h0 *= tot1;
+                    float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
+                    float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
+                    if (lane == 31) { x0 = tot1; x1 = 1.f; }
                     vb[V_WC / 4 + lane] = x0 * vb[V_ETA / 4 + lane];
                     vb[V_WC / 4 + lane + 32] = x1 * vb[V_ETA / 4 + lane + 32];
-                    if (lane == 31) vb[V_GC / 4] = g1;
                 }
                 gsync();
             }
-            if (kt == 0) {
+            if (kidx == 0) {
                 TRACE(c, 1);
                 mbar_arrive(bar(B_GV0 + b));
             }
 
-            // ---- L and P from G = [X;Q] X^T
+            // ---- L and P from G, columns 32h..32h+31 of row kt.  A half's running
+            //      product starts from prod_{i=32}^{u} gamma_i when its row reaches
+            //      past column 31 (division-free).
             {
-                const float4 *eta4 = reinterpret_cast<const float4 *>(vb + V_ETA / 4);
-                const float4 *gam4 = reinterpret_cast<const float4 *>(vb + V_GAM / 4);
-                if (kt < C) {
-                    if (falcon) {   // L[t,s] = D[t-1,s] eta_s A[t,s], s < t
-                        const int t = kt;
-                        float dz = 1.f;
-#pragma unroll
-                        for (int q = 15; q >= 0; --q) {
-                            const float4 e4 = eta4[q], y4 = gam4[q];
-                            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
-                            const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
-#pragma unroll
-                            for (int e = 3; e >= 0; --e) {
-                                const int s2 = 4 * q + e;
-                                const bool act = s2 < t;
-                                g[s2] = act ? dz * ev[e] * g[s2] : 0.f;
-                                if (act) dz *= yv[e];
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            *reinterpret_cast<float4 *>(Lf + t * 64 + ((q ^ (t & 15)) << 2)) =
-                                make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
-                    }
-                } else {   // P[t,s] = D[t,s] eta_s (q_t.x_s), s <= t
-                    const int t = kt - C;
+                const float4 *eta4 = reinterpret_cast<const float4 *>(vb + V_ETA / 4) + 8 * h;
+                const float4 *gam4 = reinterpret_cast<const float4 *>(vb + V_GAM / 4) + 8 * h;
+                const bool lrow = kt < C;
+                if (lrow && !falcon) {
+                    // linear attention needs no L
+                } else {
+                    const int t = lrow ? kt : kt - C;
+                    const int top = lrow ? t - 1 : t;        // last active column
                     float dz = 1.f;
+                    if (h == 0 && top >= 32) dz = vb[V_Q32 / 4 + top];
 #pragma unroll
-                    for (int q = 15; q >= 0; --q) {
+                    for (int q = 7; q >= 0; --q) {
                         const float4 e4 = eta4[q], y4 = gam4[q];
                         const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
                         const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
                         for (int e = 3; e >= 0; --e) {
-                            const int s2 = 4 * q + e;
-                            const bool act = s2 <= t;
+                            const int s2 = 4 * q + e;              // local column
+                            const bool act = (32 * h + s2) <= top;
                             g[s2] = act ? dz * ev[e] * g[s2] : 0.f;
                             if (act) dz *= yv[e];
                         }
                     }
-                    const uint32_t pb = sb + (b ? OFF_PB1 : OFF_PB0);
+                    if (lrow) {
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) st_row8_bf16(pb + sw128(t, c16), g + 8 * c16);
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4 *>(Lf + t * 64 + (((8 * h + q) ^ (t & 15)) << 2)) =
+                                make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                    } else {
+                        const uint32_t pb = sb + (b ? OFF_PB1 : OFF_PB0);
+#pragma unroll
+                        for (int c16 = 0; c16 < 4; ++c16)
+                            st_row8_bf16(pb + sw128(t, 4 * h + c16), g + 8 * c16);
+                    }
                 }
             }
             tc_fence_before();
             fence_proxy_async();
             gsync();
-            if (kt == 0) TRACE(c, 3);
+            if (kidx == 0) TRACE(c, 3);
             if (!falcon) {
-                if (kt == 0) mbar_arrive(bar(B_WRDY));
+                if (kidx == 0) mbar_arrive(bar(B_WRDY));
                 continue;
             }
 
-            if (kt == 0) TRACE(c, 4);
-            // ---- T = (I + L)^{-1} on warp-level tf32 MMAs.  Outputs: fp32 T blocks
-            //      needed by later merges (Tf), and the bf16 operands T and
-            //      -T diag(Gm) (K-major rows t) written straight from the fragments.
-            // bf16 T and -T diag(Gm) live where L does: their writes wait until the
-            // last read of L (the second merge level), so fragments are kept here.
+            if (kidx == 0) TRACE(c, 4);
+            // ---- T = (I + L)^{-1} on warp-level tf32 MMAs.  bf16 T and -T diag(Gm)
+            //      live where L does: their writes wait until the last read of L
+            //      (the second merge level), so fragments are kept in registers.
             const int gq = lane >> 2, tq = lane & 3;
             const float *gmv = vb + V_GM / 4;
-            auto put_t = [&](int r, int c, float v0, float v1) {   // bf16 pair (r, c..c+1)
-                const uint32_t off = sw128((uint32_t)r, (uint32_t)c >> 3) + ((uint32_t)(c & 7) << 1);
+            auto put_t = [&](int r, int cc, float v0, float v1) {   // bf16 pair (r, cc..cc+1)
+                const uint32_t off = sw128((uint32_t)r, (uint32_t)cc >> 3) + ((uint32_t)(cc & 7) << 1);
                 st_shared_u32(sb + OFF_TB + off, pack_bf16(v0, v1));
-                st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[c], -v1 * gmv[c + 1]));
+                st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[cc], -v1 * gmv[cc + 1]));
             };
-            float tdiag[2][4];   // this warp's diagonal block of T (C fragment)
-            float tpair[4];      // this warp's tile of T_{10} / T_{32}
-            {
+            float tpair[4];      // phase-1 tile (warps of half 0)
+            float t2b[4];        // phase-2 tile
+            float tdiag[2][4];   // diagonal block kw of T (C fragments, warps of half 0)
+            if (h == 0) {
+                // diagonal block kw: (I + L)^{-1} = (I - L)(I + L^2)(I + L^4)(I + L^8),
+                // four 16x16x16 products on the warp's tf32 MMAs
                 const int g = gq, t4 = tq;
-                // diagonal block kw: (I + L)^{-1} = (I - L)(I + L^2)(I + L^4)(I + L^8)
                 const int base = 16 * kw;
-                float *SA = Ms + kw * 512;        // 16x16 fp32 scratch pair of this warp
-                float *SB2 = SA + 256;
-                auto sidx = [&](int r, int c) { return r * 16 + ((((c >> 2) ^ (r & 3)) << 2) | (c & 3)); };
-                // C fragment (two 8-column tiles) <-> 16x16 scratch
-                auto store_c = [&](float *M, const float (&d)[2][4]) {
+                float *sa0 = Ms + kw * 768;   // A order
+                float *sa1 = sa0 + 256;       // A order
+                float *sb0 = sa0 + 512;       // B order
+                // fragments of L (kept in registers) and of I - L
+                uint32_t la[2][4], lb[2][2][2], ia[2][4];
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        M[sidx(g, 8 * nt + 2 * t4)] = d[nt][0];
-                        M[sidx(g, 8 * nt + 2 * t4 + 1)] = d[nt][1];
-                        M[sidx(g + 8, 8 * nt + 2 * t4)] = d[nt][2];
-                        M[sidx(g + 8, 8 * nt + 2 * t4 + 1)] = d[nt][3];
-                    }
-                };
-                // d = Aop(16x16) * Bop(16x16); operands fetched by the given functions
-                auto prod = [&](float (&d)[2][4], auto geta, auto getb) {
+                for (int ks = 0; ks < 2; ++ks) {
+                    frag_a64(Lf, base, base + 8 * ks, lane, la[ks]);
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
+                    for (int nt = 0; nt < 2; ++nt) frag_b64(Lf, base + 8 * ks, base + 8 * nt, lane, lb[ks][nt]);
+                    const int r0 = g, r1 = g + 8, c0 = 8 * ks + t4, c1 = c0 + 4;
+                    ia[ks][0] = __float_as_uint((r0 == c0 ? 1.f : 0.f) - __uint_as_float(la[ks][0]));
+                    ia[ks][1] = __float_as_uint((r1 == c0 ? 1.f : 0.f) - __uint_as_float(la[ks][1]));
+                    ia[ks][2] = __float_as_uint((r0 == c1 ? 1.f : 0.f) - __uint_as_float(la[ks][2]));
+                    ia[ks][3] = __float_as_uint((r1 == c1 ? 1.f : 0.f) - __uint_as_float(la[ks][3]));
+                }
+                auto mm = [&](float (&d)[2][4], auto fa, auto fb) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+                    for (int nt = 0; nt < 2; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
 #pragma unroll
                     for (int ks = 0; ks < 2; ++ks) {
-                        uint32_t fa[4];
-                        fa[0] = f2tf32(geta(g, 8 * ks + t4));
-                        fa[1] = f2tf32(geta(g + 8, 8 * ks + t4));
-                        fa[2] = f2tf32(geta(g, 8 * ks + t4 + 4));
-                        fa[3] = f2tf32(geta(g + 8, 8 * ks + t4 + 4));
+                        uint32_t a4[4];
+                        fa(ks, a4);
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t fb[2];
-                            fb[0] = f2tf32(getb(8 * ks + t4, 8 * nt + g));
-                            fb[1] = f2tf32(getb(8 * ks + t4 + 4, 8 * nt + g));
-                            mma_tf32_16x8x8(d[nt], fa, fb);
+                            uint32_t b2[2];
+                            fb(ks, nt, b2);
+                            mma_tf32_16x8x8(d[nt], a4, b2);
                         }
                     }
                 };
-                auto Lget = [&](int r, int c) { return Lf[f64i(base + r, base + c)]; };
-                auto ImL = [&](int r, int c) { return (r == c ? 1.f : 0.f) - Lf[f64i(base + r, base + c)]; };
-                auto SAget = [&](int r, int c) { return SA[sidx(r, c)]; };
-                auto SBget = [&](int r, int c) { return SB2[sidx(r, c)]; };
-                float d[2][4], p[2][4];
-                prod(d, Lget, Lget);                    // L^2
-                store_c(SA, d);
-                __syncwarp();
-                prod(p, ImL, SAget);                    // (I - L) L^2
-                // A2 = (I - L) + (I - L) L^2
+                auto from_a = [&](const float *M) {
+                    return [M, lane](int ks, uint32_t (&a4)[4]) {
+                        const float4 v = *reinterpret_cast<const float4 *>(M + ((ks * 32 + lane) << 2));
+                        a4[0] = __float_as_uint(v.x); a4[1] = __float_as_uint(v.y);
+                        a4[2] = __float_as_uint(v.z); a4[3] = __float_as_uint(v.w);
+                    };
+                };
+                auto from_b = [&](const float *M) {
+                    return [M, lane](int ks, int nt, uint32_t (&b2)[2]) {
+                        const float2 v = *reinterpret_cast<const float2 *>(M + (((ks * 2 + nt) * 32 + lane) << 1));
+                        b2[0] = __float_as_uint(v.x); b2[1] = __float_as_uint(v.y);
+                    };
+                };
+                auto put = [&](float *M, bool aord, const float (&d)[2][4]) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int c0 = 8 * nt + 2 * t4;
-                    p[nt][0] += ImL(g, c0);     p[nt][1] += ImL(g, c0 + 1);
-                    p[nt][2] += ImL(g + 8, c0); p[nt][3] += ImL(g + 8, c0 + 1);
-                }
-                store_c(SB2, p);
-                prod(d, SAget, SAget);                  // L^4
-                __syncwarp();
-                store_c(SA, d);
-                __syncwarp();
-                prod(d, SBget, SAget);                  // A2 L^4
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p[nt][e] += d[nt][e];   // A3
-                prod(d, SAget, SAget);                  // L^8
-                __syncwarp();
-                store_c(SB2, p);
-                store_c(SA, d);
-                __syncwarp();
-                prod(d, SBget, SAget);                  // A3 L^8
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int c0 = 8 * nt + 2 * t4;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        d[nt][e] += p[nt][e];   // T_kk
-                        tdiag[nt][e] = d[nt][e];
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int c0 = 8 * nt + 2 * t4;
+                        if (aord) {
+                            M[a_ord(g, c0)] = d[nt][0];     M[a_ord(g, c0 + 1)] = d[nt][1];
+                            M[a_ord(g + 8, c0)] = d[nt][2]; M[a_ord(g + 8, c0 + 1)] = d[nt][3];
+                        } else {
+                            M[b_ord(g, c0)] = d[nt][0];     M[b_ord(g, c0 + 1)] = d[nt][1];
+                            M[b_ord(g + 8, c0)] = d[nt][2]; M[b_ord(g + 8, c0 + 1)] = d[nt][3];
+                        }
                     }
-                    Tf[f64i(base + g, base + c0)] = d[nt][0];
-                    Tf[f64i(base + g, base + c0 + 1)] = d[nt][1];
-                    Tf[f64i(base + g + 8, base + c0)] = d[nt][2];
-                    Tf[f64i(base + g + 8, base + c0 + 1)] = d[nt][3];
-                    if ((kw & 1) == 0) {   // zero fp32 block above, inside the 32-block
-                        Tf[f64i(base + g, base + 16 + c0)] = 0.f;
-                        Tf[f64i(base + g, base + 16 + c0 + 1)] = 0.f;
-                        Tf[f64i(base + g + 8, base + 16 + c0)] = 0.f;
-                        Tf[f64i(base + g + 8, base + 16 + c0 + 1)] = 0.f;
+                };
+                auto regA = [&](const uint32_t (&f)[2][4]) {
+                    return [&f](int ks, uint32_t (&a4)[4]) {
+                        a4[0] = f[ks][0]; a4[1] = f[ks][1]; a4[2] = f[ks][2]; a4[3] = f[ks][3];
+                    };
+                };
+                auto regB = [&](int ks, int nt, uint32_t (&b2)[2]) { b2[0] = lb[ks][nt][0]; b2[1] = lb[ks][nt][1]; };
+                float d[2][4], p[2][4];
+                mm(d, regA(la), regB);                  // L^2
+                put(sa0, true, d);
+                put(sb0, false, d);
+                __syncwarp();
+                mm(p, regA(ia), from_b(sb0));           // (I - L) L^2
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {        // A2 = (I - L) + (I - L) L^2
+                    const int c0 = 8 * nt + 2 * t4;
+                    p[nt][0] += (g == c0 ? 1.f : 0.f) - Lf[f64i(base + g, base + c0)];
+                    p[nt][1] += (g == c0 + 1 ? 1.f : 0.f) - Lf[f64i(base + g, base + c0 + 1)];
+                    p[nt][2] += (g + 8 == c0 ? 1.f : 0.f) - Lf[f64i(base + g + 8, base + c0)];
+                    p[nt][3] += (g + 8 == c0 + 1 ? 1.f : 0.f) - Lf[f64i(base + g + 8, base + c0 + 1)];
+                }
+                put(sa1, true, p);
+                mm(d, from_a(sa0), from_b(sb0));        // L^4
+                __syncwarp();
+                put(sa0, true, d);
+                put(sb0, false, d);
+                __syncwarp();
+                {
+                    float q[2][4];
+                    mm(q, from_a(sa1), from_b(sb0));    // A2 L^4
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) p[nt][e] += q[nt][e];   // A3
+                }
+                mm(d, from_a(sa0), from_b(sb0));        // L^8
+                __syncwarp();
+                put(sa1, true, p);
+                put(sb0, false, d);
+                __syncwarp();
+                mm(d, from_a(sa1), from_b(sb0));        // A3 L^8
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int c0 = base + 8 * nt + 2 * t4;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) tdiag[nt][e] = d[nt][e] + p[nt][e];   // T_kk
+                    Tf[f64i(base + g, c0)] = tdiag[nt][0];
+                    Tf[f64i(base + g, c0 + 1)] = tdiag[nt][1];
+                    Tf[f64i(base + g + 8, c0)] = tdiag[nt][2];
+                    Tf[f64i(base + g + 8, c0 + 1)] = tdiag[nt][3];
+                    if ((kw & 1) == 0) {   // zero the fp32 block above, inside the 32-block
+                        Tf[f64i(base + g, c0 + 16)] = 0.f;
+                        Tf[f64i(base + g, c0 + 17)] = 0.f;
+                        Tf[f64i(base + g + 8, c0 + 16)] = 0.f;
+                        Tf[f64i(base + g + 8, c0 + 17)] = 0.f;
                     }
                 }
             }
             gsync();
-            if (kt == 0) TRACE(c, 5);
-            {   // pairs (1,0) and (3,2): warp kw -> pair p, 8-column tile nt
+            if (kidx == 0) TRACE(c, 5);
+            if (h == 0) {   // pairs (1,0) and (3,2): warp kw -> pair p, 8-column tile nt
                 const int p = kw >> 1, nt = kw & 1;
                 const int rb = 16 + 32 * p, cb = 32 * p;
                 const int g = gq, t4 = tq;
@@ -720,8 +775,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 for (int ks = 0; ks < 2; ++ks) {
                     uint32_t fa[4], fb[2];
                     frag_a64(Tf, rb, rb + 8 * ks, lane, fa);
-                    fb[0] = f2tf32(Mw[(8 * ks + t4) * 8 + g]);
-                    fb[1] = f2tf32(Mw[(8 * ks + t4 + 4) * 8 + g]);
+                    fb[0] = __float_as_uint(Mw[(8 * ks + t4) * 8 + g]);
+                    fb[1] = __float_as_uint(Mw[(8 * ks + t4 + 4) * 8 + g]);
                     mma_tf32_16x8x8(u, fa, fb);
                 }
                 const int c0 = cb + 8 * nt + 2 * t4;
@@ -733,106 +788,88 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 for (int e = 0; e < 4; ++e) tpair[e] = -u[e];
             }
             gsync();
+            // second level: 32x32 tiles, one 16x8 tile per warp: row tile rt, column tile ct
+            const int rt = kw >> 1, ct = 2 * (kw & 1) + h;
             {   // M2 = L[32:64, 0:32] T[0:32, 0:32]
-                const int rt = kw >> 1, ch = kw & 1;   // 16-row tile, 16-column half
-                const int g = lane >> 2, t4 = lane & 3;
-                float m[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const int g = gq, t4 = tq;
+                float m[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t fa[4];
+                    uint32_t fa[4], fb[2];
                     frag_a64(Lf, 32 + 16 * rt, 8 * ks, lane, fa);
-#pragma unroll
-                    for (int n2 = 0; n2 < 2; ++n2) {
-                        uint32_t fb[2];
-                        frag_b64(Tf, 8 * ks, 16 * ch + 8 * n2, lane, fb);
-                        mma_tf32_16x8x8(m[n2], fa, fb);
-                    }
+                    frag_b64(Tf, 8 * ks, 8 * ct, lane, fb);
+                    mma_tf32_16x8x8(m, fa, fb);
                 }
-#pragma unroll
-                for (int n2 = 0; n2 < 2; ++n2) {
-                    const int c0 = 16 * ch + 8 * n2 + 2 * t4;
-                    Ms[f32i(16 * rt + g, c0)] = m[n2][0];
-                    Ms[f32i(16 * rt + g, c0 + 1)] = m[n2][1];
-                    Ms[f32i(16 * rt + g + 8, c0)] = m[n2][2];
-                    Ms[f32i(16 * rt + g + 8, c0 + 1)] = m[n2][3];
-                }
+                const int c0 = 8 * ct + 2 * t4;
+                Ms[f32i(16 * rt + g, c0)] = m[0];
+                Ms[f32i(16 * rt + g, c0 + 1)] = m[1];
+                Ms[f32i(16 * rt + g + 8, c0)] = m[2];
+                Ms[f32i(16 * rt + g + 8, c0 + 1)] = m[3];
             }
             gsync();
-            {   // L is dead: write the bf16 blocks computed so far, zero the upper ones
+            {   // T[32:64, 0:32] = -T[32:64, 32:64] M2
                 const int g = gq, t4 = tq;
-                const int base = 16 * kw;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int c0 = base + 8 * nt + 2 * t4;
-                    put_t(base + g, c0, tdiag[nt][0], tdiag[nt][1]);
-                    put_t(base + g + 8, c0, tdiag[nt][2], tdiag[nt][3]);
-                }
-                const int p = kw >> 1, nt = kw & 1;
-                const int rb = 16 + 32 * p, c0 = 32 * p + 8 * nt + 2 * t4;
-                put_t(rb + g, c0, tpair[0], tpair[1]);
-                put_t(rb + g + 8, c0, tpair[2], tpair[3]);
-                for (int cb = kw + 1; cb < 4; ++cb) {
-                    const int r = base + (lane >> 1), c = 16 * cb + 8 * (lane & 1);
-                    st_shared_v4(sb + OFF_TB + sw128((uint32_t)r, (uint32_t)c >> 3), 0u, 0u, 0u, 0u);
-                    st_shared_v4(sb + OFF_TPB + sw128((uint32_t)r, (uint32_t)c >> 3), 0u, 0u, 0u, 0u);
-                }
-            }
-            {   // T[32:64, 0:32] = -T[32:64, 32:64] M2  (bf16 operands only)
-                const int rt = kw >> 1, ch = kw & 1;
-                const int g = gq, t4 = tq;
-                float u[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t fa[4];
+                    uint32_t fa[4], fb[2];
                     frag_a64(Tf, 32 + 16 * rt, 32 + 8 * ks, lane, fa);
-#pragma unroll
-                    for (int n2 = 0; n2 < 2; ++n2) {
-                        uint32_t fb[2];
-                        frag_b32(Ms, 8 * ks, 16 * ch + 8 * n2, lane, fb);
-                        mma_tf32_16x8x8(u[n2], fa, fb);
-                    }
+                    frag_b32(Ms, 8 * ks, 8 * ct, lane, fb);
+                    mma_tf32_16x8x8(u, fa, fb);
                 }
 #pragma unroll
-                for (int n2 = 0; n2 < 2; ++n2) {
-                    const int c0 = 16 * ch + 8 * n2 + 2 * t4;
-                    const int r0 = 32 + 16 * rt + g;
+                for (int e = 0; e < 4; ++e) t2b[e] = -u[e];
+            }
+            {   // L is dead: write every bf16 block, zero the upper ones
+                const int g = gq, t4 = tq;
+                const int base = 16 * kw;
+                if (h == 0) {
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = r0 + 8 * hh;
-                        const float v0 = -u[n2][2 * hh], v1 = -u[n2][2 * hh + 1];
-                        const uint32_t off = sw128((uint32_t)r, (uint32_t)c0 >> 3) + ((uint32_t)(c0 & 7) << 1);
-                        st_shared_u32(sb + OFF_TB + off, pack_bf16(v0, v1));
-                        st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[c0], -v1 * gmv[c0 + 1]));
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int cd = base + 8 * nt + 2 * t4;
+                        put_t(base + g, cd, tdiag[nt][0], tdiag[nt][1]);
+                        put_t(base + g + 8, cd, tdiag[nt][2], tdiag[nt][3]);
                     }
+                    const int p = kw >> 1, nt = kw & 1;
+                    const int rb = 16 + 32 * p, c1 = 32 * p + 8 * nt + 2 * t4;
+                    put_t(rb + g, c1, tpair[0], tpair[1]);
+                    put_t(rb + g + 8, c1, tpair[2], tpair[3]);
+                }
+                const int r2 = 32 + 16 * rt + g, c2 = 8 * ct + 2 * t4;
+                put_t(r2, c2, t2b[0], t2b[1]);
+                put_t(r2 + 8, c2, t2b[2], t2b[3]);
+                // upper blocks of row block kw: the two warps of the quarter split them
+                for (int cb = kw + 1; cb < 4; ++cb) {
+                    if (((cb - kw - 1) & 1) != h) continue;
+                    const int r = base + (lane >> 1), cc = 16 * cb + 8 * (lane & 1);
+                    st_shared_v4(sb + OFF_TB + sw128((uint32_t)r, (uint32_t)cc >> 3), 0u, 0u, 0u, 0u);
+                    st_shared_v4(sb + OFF_TPB + sw128((uint32_t)r, (uint32_t)cc >> 3), 0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async();
             gsync();
-            if (kt == 0) { TRACE(c, 6); mbar_arrive(bar(B_TRDY)); }
+            if (kidx == 0) { TRACE(c, 6); mbar_arrive(bar(B_TRDY)); }
 
             // ---- -W^T -> bf16 rows i, once W^T(c) is done and R(c-1) has read the old one
             if (!gwait(bar(B_WUDONE), (uint32_t)c & 1u)) { ok = false; break; }
-            if (kt == 0) TRACE(c, 7);
+            if (kidx == 0) TRACE(c, 7);
             tc_fence_after();
             if (c >= 1 && !gwait(bar(B_RDONE), (uint32_t)(c - 1) & 1u)) { ok = false; break; }
-            if (kt == 0) TRACE(c, 8);
+            if (kidx == 0) TRACE(c, 8);
             {
                 float w[32];
+                tmem_ld32(tmem + lane_base + COL_W + 32 * h, w);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(tmem + lane_base + COL_W + 32 * h, w);
-#pragma unroll
-                    for (int c16 = 0; c16 < 4; ++c16)
-                        st_row8_bf16(sb + OFF_WTB + sw128(kt, 4 * h + c16), w + 8 * c16);
-                }
+                for (int c16 = 0; c16 < 4; ++c16)
+                    st_row8_bf16(sb + OFF_WTB + sw128(kt, 4 * h + c16), w + 8 * c16);
             }
             tc_fence_before();
             fence_proxy_async();
             gsync();
-            if (kt == 0) { TRACE(c, 9); mbar_arrive(bar(B_WRDY)); }
+            if (kidx == 0) { TRACE(c, 9); mbar_arrive(bar(B_WRDY)); }
         }
-        if (!ok && kt == 0) fail_now();
-    } else if (warp >= SG_W0) {
+        if (!ok && kidx == 0) fail_now();
+    } else if (warp >= SG_W0 && warp < KG2_W0) {
         // ================================================================ state group
         const int srow = tid - SG_W0 * 32;         // == TMEM lane of this thread
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -932,6 +969,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int q = 0; q < 8; ++q) {
                 float v[16];
                 tmem_ld16(tmem + lane_base + COL_S + 16 * q, v);
+                if (srow == 0 && q == 0) TRACE(c, 23);
                 if (last) {
                     float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + srow) * D + 16 * q);
 #pragma unroll
@@ -947,7 +985,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     tmem_st16(tmem + lane_base + COL_S + 16 * q, v);
                 }
             }
+            if (srow == 0) TRACE(c, 24);
             tmem_st_wait();
+            if (srow == 0) TRACE(c, 25);
             tc_fence_before();
             fence_proxy_async();
             gsync();
@@ -969,16 +1009,20 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     float o1[32], o2[32];
                     tmem_ld32(tmem + lane_base + COL_O1 + 32 * h, o1);
                     tmem_ld32(tmem + lane_base + COL_O2 + 32 * h, o2);
+                    if (srow == 0) TRACE(c, 26 + 2 * h);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const int t = 32 * h + e;
-                        const float v0 = falcon ? fmaf(gv[t], o1[e], o2[e]) : o1[e] + o2[e];
-                        const float v1 = falcon ? fmaf(gv[t + 1], o1[e + 1], o2[e + 1]) : o1[e + 1] + o2[e + 1];
+                        const float2 g2 = falcon ? *reinterpret_cast<const float2 *>(gv + t)
+                                                 : make_float2(1.f, 1.f);
+                        const float v0 = fmaf(g2.x, o1[e], o2[e]);
+                        const float v1 = fmaf(g2.y, o1[e + 1], o2[e + 1]);
                         const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
                         const int tt = odd ? t + 1 : t;
                         const uint32_t w = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
                         if (tt < nvalid) og[(int64_t)tt * (D / 2)] = w;
                     }
+                    if (srow == 0) TRACE(c, 27 + 2 * h);
                 }
             }
             tc_fence_before();
