@@ -283,7 +283,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int c = 0; c < nch && ok; ++c) {
                 const int b = c & 1;
                 const uint32_t st = xq(b);
-                if (!wait_fast(bar(B_GGO), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                if (!wait_fast(bar(B_GGO), (uint32_t)c & 1u, limit, s_abort) ||
+                    !wait_fast(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 {   // G = [X; Q] X^T  (rows 0..63: X X^T, rows 64..127: Q X^T)
                     const uint32_t id = idesc_bf16(128, 64, false, false);
@@ -438,14 +442,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
         };
         load_gates(0);
-#pragma unroll 1
-        for (int c = 0; c < nch && ok; ++c) {
-            const int b = c & 1;
-            const uint32_t st = xq(b);
-            float *vb = vec(b);
-            if (!gwait(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u)) { ok = false; break; }
-            if (kidx == 0) TRACE(c, 0);
 
+        // feature map on the loaded tiles of chunk cc and the k_init patch, then
+        // release the Gram MMA of chunk cc
+        auto prep_go = [&](int cc) -> bool {
+            const uint32_t st_ = xq(cc & 1);
+            if (!gwait(bar(B_FULL0 + (cc & 1)), (uint32_t)(cc >> 1) & 1u)) return false;
             // ---- feature map on the loaded tiles (row t, a quarter of its 16-byte
             //      chunks per thread), k_init patch
             {
@@ -454,12 +456,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const int t = kidx >> 2, qq = kidx & 3;
                     const uint32_t roff = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
                     for (int which = 0; which < (falcon ? 1 : 2); ++which) {
-                        const int64_t src = (int64_t)c * C + t - ((which == 0 && falcon) ? 1 : 0);
+                        const int64_t src = (int64_t)cc * C + t - ((which == 0 && falcon) ? 1 : 0);
                         if (src < 0 || src >= T) continue;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int cidx = 4 * qq + m;   // 0..15: block (cidx >> 3), chunk (cidx & 7)
-                            const uint32_t row = st + (which == 0 ? ((cidx >> 3) ? XQ_X1 : XQ_X0)
+                            const uint32_t row = st_ + (which == 0 ? ((cidx >> 3) ? XQ_X1 : XQ_X0)
                                                                   : ((cidx >> 3) ? XQ_Q1 : XQ_Q0)) + roff;
                             const uint32_t ad = row + (uint32_t)(cidx & 7) * 16u;
                             float f[8];
@@ -471,7 +473,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     }
                     wrote = true;
                 }
-                if (falcon && c == 0 && a.k_init) {
+                if (falcon && cc == 0 && a.k_init) {
                     if (kidx < 16) {
                         const int hb = kidx >> 3, c16 = kidx & 7;
                         const uint4 u = *reinterpret_cast<const uint4 *>(
@@ -480,7 +482,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         unpack8(u, f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] = apply_phi(a.phi, f[e]);
-                        st_row8_bf16(st + (hb ? XQ_X1 : XQ_X0) + (uint32_t)c16 * 16u, f);
+                        st_row8_bf16(st_ + (hb ? XQ_X1 : XQ_X0) + (uint32_t)c16 * 16u, f);
                     }
                     wrote = true;
                 }
@@ -488,45 +490,49 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             gsync();   // mapped tiles (and the k_init row) complete: the Gram MMA may start
             if (kidx == 0) mbar_arrive(bar(B_GGO));
-
-            if (!gwait(bar(B_GDONE), (uint32_t)c & 1u)) { ok = false; break; }
-            if (kidx == 0) TRACE(c, 2);
+            return true;
+        };
+        // gates of chunk cc: waits for its Gram MMA, reads |x_t|^2 off the diagonal,
+        // publishes eta, gamma and the decay products in gate block cc & 1.
+        // (Block cc & 1 was last read by the state group for chunk cc - 2, which is
+        // finished: the Gram MMA of chunk cc ran on a tile whose stage the state
+        // MMAs of chunk cc - 2 released.)
+        auto gates = [&](int cc) -> bool {
+            float *vg = vec(cc & 1);
+            if (!gwait(bar(B_GDONE), (uint32_t)cc & 1u)) return false;
             tc_fence_after();
-            if (c >= 2 && !gwait(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u)) { ok = false; break; }
-            float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
-            tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
-            if (kidx == 0) TRACE(c, 20);
-
             // ---- step sizes and decay products of chunk c; |x_t|^2 is G[t,t]
             if (falcon) {
-                if (kt < C && (kt >> 5) == h) {   // the thread whose half holds the diagonal
+                if (kt < C && (kt >> 5) == h) {   // the warp whose half holds the diagonal
+                    float gd[32];
+                    tmem_ld32(tmem + lane_base + COL_G + 32 * h, gd);
                     float n = 0.f;
 #pragma unroll
-                    for (int s2 = 0; s2 < 32; ++s2) n = (s2 == lane) ? g[s2] : n;
-                    vb[V_ETA / 4 + kt] = n;   // |x_t|^2; the thread holding beta_t turns it into eta_t
+                    for (int s2 = 0; s2 < 32; ++s2) n = (s2 == lane) ? gd[s2] : n;
+                    vg[V_ETA / 4 + kt] = n;   // |x_t|^2; the thread holding beta_t turns it into eta_t
                 }
                 gsync();
-                if (kidx == 0) TRACE(c, 21);
+                if (kidx == 0) TRACE(cc, 21);
                 if (kidx < C) {
                     const int t = kidx;
-                    const int64_t tok = (int64_t)c * C + t;
-                    const float n = vb[V_ETA / 4 + t];
+                    const int64_t tok = (int64_t)cc * C + t;
+                    const float n = vg[V_ETA / 4 + t];
                     const float bt = nb, lt = nl;
-                    load_gates(c + 1);
+                    load_gates(cc + 1);
                     float eta = 0.f, gam = 1.f;
                     if (tok < T) {
                         const bool pair = (tok > 0) || (a.k_init != nullptr);
                         eta = pair ? bt / (n + lt + a.eps) : 0.f;
                         gam = 1.f - eta * lt;
                     }
-                    vb[V_ETA / 4 + t] = eta;
-                    vb[V_GAM / 4 + t] = gam;
+                    vg[V_ETA / 4 + t] = eta;
+                    vg[V_GAM / 4 + t] = gam;
                 }
                 gsync();
-                if (kidx == 0) TRACE(c, 22);
+                if (kidx == 0) TRACE(cc, 22);
                 if (kidx < 32) {
                     // warp of kidx 0..31: prefix products G_t, Gm_t, Q32_t = prod_{32..t}
-                    float g0 = vb[V_GAM / 4 + lane], g1 = vb[V_GAM / 4 + lane + 32];
+                    float g0 = vg[V_GAM / 4 + lane], g1 = vg[V_GAM / 4 + lane + 32];
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
@@ -534,19 +540,19 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         if (lane >= off) { g0 *= u0; g1 *= u1; }
                     }
                     const float tot0 = __shfl_sync(0xffffffffu, g0, 31);
-                    vb[V_Q32 / 4 + lane + 32] = g1;   // prod_{i=32}^{t} gamma_i
+                    vg[V_Q32 / 4 + lane + 32] = g1;   // prod_{i=32}^{t} gamma_i
                     g1 *= tot0;
                     float e0 = __shfl_up_sync(0xffffffffu, g0, 1);
                     float e1 = __shfl_up_sync(0xffffffffu, g1, 1);
                     if (lane == 0) { e0 = 1.f; e1 = tot0; }
-                    vb[V_G / 4 + lane] = g0;
-                    vb[V_G / 4 + lane + 32] = g1;
-                    vb[V_GM / 4 + lane] = e0;
-                    vb[V_GM / 4 + lane + 32] = e1;
-                    if (lane == 31) vb[V_GC / 4] = g1;
+                    vg[V_G / 4 + lane] = g0;
+                    vg[V_G / 4 + lane + 32] = g1;
+                    vg[V_GM / 4 + lane] = e0;
+                    vg[V_GM / 4 + lane + 32] = e1;
+                    if (lane == 31) vg[V_GC / 4] = g1;
                 } else if (kidx >= 128 && kidx < 160) {
                     // a warp of the other half: suffix products -> w_s = D[C-1,s] eta_s
-                    float h0 = vb[V_GAM / 4 + lane], h1 = vb[V_GAM / 4 + lane + 32];
+                    float h0 = vg[V_GAM / 4 + lane], h1 = vg[V_GAM / 4 + lane + 32];
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
@@ -558,15 +564,31 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
                     float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
                     if (lane == 31) { x0 = tot1; x1 = 1.f; }
-                    vb[V_WC / 4 + lane] = x0 * vb[V_ETA / 4 + lane];
-                    vb[V_WC / 4 + lane + 32] = x1 * vb[V_ETA / 4 + lane + 32];
+                    vg[V_WC / 4 + lane] = x0 * vg[V_ETA / 4 + lane];
+                    vg[V_WC / 4 + lane + 32] = x1 * vg[V_ETA / 4 + lane + 32];
                 }
                 gsync();
             }
             if (kidx == 0) {
-                TRACE(c, 1);
-                mbar_arrive(bar(B_GV0 + b));
+                TRACE(cc, 1);
+                mbar_arrive(bar(B_GV0 + (cc & 1)));
             }
+            return true;
+        };
+        // Without a feature-map pass on the tiles (phi = identity), the Gram MMA of
+        // chunk c+1 is released as soon as the Gram of chunk c has been read, so it
+        // runs while chunk c's solve and W/U products do.
+        const bool early = !elu;
+        if (ok) ok = prep_go(0) && gates(0);
+#pragma unroll 1
+        for (int c = 0; c < nch && ok; ++c) {
+            const int b = c & 1;
+            float *vb = vec(b);
+            if (c > 0 && !early && !(prep_go(c) && gates(c))) { ok = false; break; }
+            if (kidx == 0) TRACE(c, 2);
+            if (c >= 2 && !gwait(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u)) { ok = false; break; }
+            float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
+            tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
 
             // ---- L and P from G, columns 32h..32h+31 of row kt.  A half's running
             //      product starts from prod_{i=32}^{u} gamma_i when its row reaches
@@ -612,8 +634,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             fence_proxy_async();
             gsync();
             if (kidx == 0) TRACE(c, 3);
+            const bool more = (c + 1 < nch);
+            if (early && more && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
             if (!falcon) {
                 if (kidx == 0) mbar_arrive(bar(B_WRDY));
+                if (early && more && !gates(c + 1)) { ok = false; break; }
                 continue;
             }
 
@@ -867,6 +892,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             fence_proxy_async();
             gsync();
             if (kidx == 0) { TRACE(c, 9); mbar_arrive(bar(B_WRDY)); }
+            // the next chunk's Gram MMA has been running since L/P: take its gates now
+            if (early && more && !gates(c + 1)) { ok = false; break; }
         }
         if (!ok && kidx == 0) fail_now();
     } else if (warp >= SG_W0 && warp < KG2_W0) {
