@@ -398,6 +398,136 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             mbar_wait(bar(B_SDRAIN), 0, kDrainNs);
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ================================================================ gates
+        // Step sizes and decay products of chunk cc, published in gate block cc & 1
+        // as soon as the chunk's keys land: |x_t|^2 straight from the staged X tile,
+        // eta_t = beta_t / (|x_t|^2 + lambda_t + eps), gamma_t = 1 - eta_t lambda_t,
+        // then the in-chunk prefix and suffix products (division-free).
+        // Lane l holds tokens l and l + 32 of the chunk.
+        // (Block cc & 1 was last read for chunk cc - 2 by the key group (L, P, the
+        // solve) and the state group (the R epilogue), all of which precede the S
+        // MMAs of chunk cc - 2, whose completion released the stage chunk cc's
+        // keys were loaded into.)
+        bool ok = true;
+        if (!falcon) {   // linear attention: eta = 1, no decay
+            for (int b = 0; b < 2; ++b) {
+                float *v = vec(b);
+                for (int t = lane; t < C; t += 32) {
+                    v[V_ETA / 4 + t] = 1.f;
+                    v[V_GAM / 4 + t] = 1.f;
+                    v[V_G / 4 + t] = 1.f;
+                    v[V_GM / 4 + t] = 1.f;
+                    v[V_WC / 4 + t] = 1.f;
+                    v[V_Q32 / 4 + t] = 1.f;
+                }
+                if (lane == 0) v[V_GC / 4] = 1.f;
+            }
+        }
+        // beta, lambda of tokens lane and lane + 32, loaded one chunk ahead
+        float nb[2] = {0.f, 0.f}, nl[2] = {0.f, 0.f};
+        auto load_bl = [&](int cc) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int64_t tok = (int64_t)cc * C + lane + 32 * u;
+                if (falcon && cc < nch && tok < T) {
+                    nb[u] = a.beta[chain * T + tok];
+                    nl[u] = a.lam[chain * T + tok];
+                }
+            }
+        };
+        load_bl(0);
+#pragma unroll 1
+        for (int cc = 0; cc < nch && ok; ++cc) {
+            const int b = cc & 1;
+            float *vg = vec(b);
+            bool w = wait_bar(bar(B_FULL0 + b), (uint32_t)(cc >> 1) & 1u, limit, s_abort);
+            // chunk 0's first key row is patched with phi(k_init) before the Gram is released
+            if (falcon && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            if (falcon) {
+                const uint32_t xs = xq(b);
+                float n[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = lane + 32 * u;
+                    // the whole 128-byte row of each half, chunks in a lane-rotated
+                    // order (the squared norm does not depend on the swizzle)
+                    const uint32_t row = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int hx = 0; hx < 2; ++hx) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            float f[8];
+                            unpack8(ld_shared_v4(xs + (hx ? XQ_X1 : XQ_X0) + row +
+                                                 (uint32_t)((k + lane) & 7) * 16u), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
+                        }
+                    }
+                    n[u] = acc;
+                }
+                float eta[2], gam[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int64_t tok = (int64_t)cc * C + lane + 32 * u;
+                    eta[u] = 0.f;
+                    gam[u] = 1.f;
+                    if (tok < T) {
+                        const bool pair = (tok > 0) || (a.k_init != nullptr);
+                        eta[u] = pair ? nb[u] / (n[u] + nl[u] + a.eps) : 0.f;
+                        gam[u] = 1.f - eta[u] * nl[u];
+                    }
+                }
+                load_bl(cc + 1);
+                // prefix products G_t, Gm_t = G_{t-1}, Q32_t = prod_{32..t} gamma_i
+                float g0 = gam[0], g1 = gam[1];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
+                    const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
+                    if (lane >= off) { g0 *= u0; g1 *= u1; }
+                }
+                const float tot0 = __shfl_sync(0xffffffffu, g0, 31);
+                const float q32 = g1;
+                g1 *= tot0;
+                float e0 = __shfl_up_sync(0xffffffffu, g0, 1);
+                float e1 = __shfl_up_sync(0xffffffffu, g1, 1);
+                if (lane == 0) { e0 = 1.f; e1 = tot0; }
+                // suffix products -> w_s = D[C-1,s] eta_s = eta_s prod_{s<i<C} gamma_i
+                float h0 = gam[0], h1 = gam[1];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
+                    const float d1 = __shfl_down_sync(0xffffffffu, h1, off);
+                    if (lane + off < 32) { h0 *= d0; h1 *= d1; }
+                }
+                const float tot1 = __shfl_sync(0xffffffffu, h1, 0);
+                h0 *= tot1;
+                float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
+                float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
+                if (lane == 31) { x0 = tot1; x1 = 1.f; }
+                vg[V_ETA / 4 + lane] = eta[0];
+                vg[V_ETA / 4 + lane + 32] = eta[1];
+                vg[V_GAM / 4 + lane] = gam[0];
+                vg[V_GAM / 4 + lane + 32] = gam[1];
+                vg[V_G / 4 + lane] = g0;
+                vg[V_G / 4 + lane + 32] = g1;
+                vg[V_GM / 4 + lane] = e0;
+                vg[V_GM / 4 + lane + 32] = e1;
+                vg[V_Q32 / 4 + lane + 32] = q32;
+                vg[V_WC / 4 + lane] = x0 * eta[0];
+                vg[V_WC / 4 + lane + 32] = x1 * eta[1];
+                if (lane == 31) vg[V_GC / 4] = g1;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                TRACE(cc, 1);
+                mbar_arrive(bar(B_GV0 + b));
+            }
+        }
+        if (!ok && lane == 0) fail_now();
     } else if ((warp >= KG_W0 && warp < SG_W0) || warp >= KG2_W0) {
         // ================================================================ key group
         // 8 warps: two per TMEM lane quarter.  Thread (kt, h) owns row kt of the
@@ -416,32 +546,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         };
         auto gsync = [&]() { bar_sync(BAR_KG, KGROUP); };
 
-        if (!falcon && kidx < C) {
-            for (int b = 0; b < 2; ++b) {
-                float *v = vec(b);
-                v[V_ETA / 4 + kidx] = 1.f;
-                v[V_GAM / 4 + kidx] = 1.f;
-                v[V_G / 4 + kidx] = 1.f;
-                v[V_GM / 4 + kidx] = 1.f;
-                v[V_WC / 4 + kidx] = 1.f;
-                v[V_Q32 / 4 + kidx] = 1.f;
-                if (kidx == 0) v[V_GC / 4] = 1.f;
-            }
-        }
-
         bool ok = true;
         // testing hook: a wait on a barrier nothing arrives on runs out
         if (a.force_timeout && !gwait(bar(B_NEVER), 0)) ok = false;
-        // beta, lambda of the next chunk are loaded one chunk ahead (kidx < C)
-        float nb = 0.f, nl = 0.f;
-        auto load_gates = [&](int cc) {
-            const int64_t tok = (int64_t)cc * C + kidx;
-            if (falcon && kidx < C && cc < nch && tok < T) {
-                nb = a.beta[chain * T + tok];
-                nl = a.lam[chain * T + tok];
-            }
-        };
-        load_gates(0);
 
         // feature map on the loaded tiles of chunk cc and the k_init patch, then
         // release the Gram MMA of chunk cc
@@ -492,101 +599,24 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (kidx == 0) mbar_arrive(bar(B_GGO));
             return true;
         };
-        // gates of chunk cc: waits for its Gram MMA, reads |x_t|^2 off the diagonal,
-        // publishes eta, gamma and the decay products in gate block cc & 1.
-        // (Block cc & 1 was last read by the state group for chunk cc - 2, which is
-        // finished: the Gram MMA of chunk cc ran on a tile whose stage the state
-        // MMAs of chunk cc - 2 released.)
-        auto gates = [&](int cc) -> bool {
-            float *vg = vec(cc & 1);
-            if (!gwait(bar(B_GDONE), (uint32_t)cc & 1u)) return false;
-            tc_fence_after();
-            // ---- step sizes and decay products of chunk c; |x_t|^2 is G[t,t]
-            if (falcon) {
-                if (kt < C && (kt >> 5) == h) {   // the warp whose half holds the diagonal
-                    float gd[32];
-                    tmem_ld32(tmem + lane_base + COL_G + 32 * h, gd);
-                    float n = 0.f;
-#pragma unroll
-                    for (int s2 = 0; s2 < 32; ++s2) n = (s2 == lane) ? gd[s2] : n;
-                    vg[V_ETA / 4 + kt] = n;   // |x_t|^2; the thread holding beta_t turns it into eta_t
-                }
-                gsync();
-                if (kidx == 0) TRACE(cc, 21);
-                if (kidx < C) {
-                    const int t = kidx;
-                    const int64_t tok = (int64_t)cc * C + t;
-                    const float n = vg[V_ETA / 4 + t];
-                    const float bt = nb, lt = nl;
-                    load_gates(cc + 1);
-                    float eta = 0.f, gam = 1.f;
-                    if (tok < T) {
-                        const bool pair = (tok > 0) || (a.k_init != nullptr);
-                        eta = pair ? bt / (n + lt + a.eps) : 0.f;
-                        gam = 1.f - eta * lt;
-                    }
-                    vg[V_ETA / 4 + t] = eta;
-                    vg[V_GAM / 4 + t] = gam;
-                }
-                gsync();
-                if (kidx == 0) TRACE(cc, 22);
-                if (kidx < 32) {
-                    // warp of kidx 0..31: prefix products G_t, Gm_t, Q32_t = prod_{32..t}
-                    float g0 = vg[V_GAM / 4 + lane], g1 = vg[V_GAM / 4 + lane + 32];
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float u0 = __shfl_up_sync(0xffffffffu, g0, off);
-                        const float u1 = __shfl_up_sync(0xffffffffu, g1, off);
-                        if (lane >= off) { g0 *= u0; g1 *= u1; }
-                    }
-                    const float tot0 = __shfl_sync(0xffffffffu, g0, 31);
-                    vg[V_Q32 / 4 + lane + 32] = g1;   // prod_{i=32}^{t} gamma_i
-                    g1 *= tot0;
-                    float e0 = __shfl_up_sync(0xffffffffu, g0, 1);
-                    float e1 = __shfl_up_sync(0xffffffffu, g1, 1);
-                    if (lane == 0) { e0 = 1.f; e1 = tot0; }
-                    vg[V_G / 4 + lane] = g0;
-                    vg[V_G / 4 + lane + 32] = g1;
-                    vg[V_GM / 4 + lane] = e0;
-                    vg[V_GM / 4 + lane + 32] = e1;
-                    if (lane == 31) vg[V_GC / 4] = g1;
-                } else if (kidx >= 128 && kidx < 160) {
-                    // a warp of the other half: suffix products -> w_s = D[C-1,s] eta_s
-                    float h0 = vg[V_GAM / 4 + lane], h1 = vg[V_GAM / 4 + lane + 32];
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float d0 = __shfl_down_sync(0xffffffffu, h0, off);
-                        const float d1 = __shfl_down_sync(0xffffffffu, h1, off);
-                        if (lane + off < 32) { h0 *= d0; h1 *= d1; }
-                    }
-                    const float tot1 = __shfl_sync(0xffffffffu, h1, 0);
-                    h0 *= tot1;
-                    float x0 = __shfl_down_sync(0xffffffffu, h0, 1);
-                    float x1 = __shfl_down_sync(0xffffffffu, h1, 1);
-                    if (lane == 31) { x0 = tot1; x1 = 1.f; }
-                    vg[V_WC / 4 + lane] = x0 * vg[V_ETA / 4 + lane];
-                    vg[V_WC / 4 + lane + 32] = x1 * vg[V_ETA / 4 + lane + 32];
-                }
-                gsync();
-            }
-            if (kidx == 0) {
-                TRACE(cc, 1);
-                mbar_arrive(bar(B_GV0 + (cc & 1)));
-            }
-            return true;
-        };
         // Without a feature-map pass on the tiles (phi = identity), the Gram MMA of
         // chunk c+1 is released as soon as the Gram of chunk c has been read, so it
         // runs while chunk c's solve and W/U products do.
         const bool early = !elu;
-        if (ok) ok = prep_go(0) && gates(0);
+        if (ok) ok = prep_go(0);
 #pragma unroll 1
         for (int c = 0; c < nch && ok; ++c) {
             const int b = c & 1;
             float *vb = vec(b);
-            if (c > 0 && !early && !(prep_go(c) && gates(c))) { ok = false; break; }
+            if (c > 0 && !early && !prep_go(c)) { ok = false; break; }
             if (kidx == 0) TRACE(c, 2);
-            if (c >= 2 && !gwait(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u)) { ok = false; break; }
+            {   // P buffer b free (chunk c-2's O2 done), Gram of chunk c done, gates of chunk c
+                bool w = c < 2 || wait_bar(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort);
+                w = w && wait_bar(bar(B_GDONE), (uint32_t)c & 1u, limit, s_abort);
+                w = w && wait_bar(bar(B_GV0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort);
+                if (bar_or(BAR_KG, KGROUP, !w)) { ok = false; break; }
+            }
+            tc_fence_after();
             float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
             tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
 
@@ -638,7 +668,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (early && more && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
             if (!falcon) {
                 if (kidx == 0) mbar_arrive(bar(B_WRDY));
-                if (early && more && !gates(c + 1)) { ok = false; break; }
                 continue;
             }
 
@@ -892,8 +921,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             fence_proxy_async();
             gsync();
             if (kidx == 0) { TRACE(c, 9); mbar_arrive(bar(B_WRDY)); }
-            // the next chunk's Gram MMA has been running since L/P: take its gates now
-            if (early && more && !gates(c + 1)) { ok = false; break; }
         }
         if (!ok && kidx == 0) fail_now();
     } else if (warp >= SG_W0 && warp < KG2_W0) {
@@ -954,7 +981,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (srow == 0) TRACE(c, 10);
                 tc_fence_after();
                 const float *wc = vec(b) + V_WC / 4;
-                if (srow < C)   // the key group may recycle this gate block once S(c) is done
+                if (srow < C)   // the gate warp may recycle this gate block once S(c) is done
                     reinterpret_cast<float *>(sm + OFF_SGV)[srow] = vec(b)[V_G / 4 + srow];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
