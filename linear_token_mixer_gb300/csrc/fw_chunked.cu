@@ -179,16 +179,6 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
     b[1] = __float_as_uint(M[f32i(k0 + t + 4, n0 + g)]);
 }
 
-// 16x16 fp32 scratch in fragment order: "A order" holds each lane's m16n8k8 A
-// fragment of k-step ks as one float4, "B order" each lane's B fragment of
-// (ks, nt) as one float2, so an operand fetch is a single vector load.
-__device__ __forceinline__ int a_ord(int r, int c) {
-    return (((c >> 3) * 32 + (r & 7) * 4 + (c & 3)) << 2) + (r >> 3) + 2 * ((c & 7) >> 2);
-}
-__device__ __forceinline__ int b_ord(int r, int c) {
-    return ((((r >> 3) * 2 + (c >> 3)) * 32 + (c & 7) * 4 + (r & 3)) << 1) + ((r & 7) >> 2);
-}
-
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
@@ -280,29 +270,55 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // ================================================================ key-path MMAs
         if (lane == 0) {
             bool ok = true;
+            // G = [X; Q] X^T of chunk cc (rows 0..63: X X^T, rows 64..127: Q X^T)
+            auto issue_g = [&](int cc) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+                const uint64_t dx = sdesc_sw128(xq(cc & 1) + XQ_X0, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                    mma_bf16(tmem + COL_G, dx + off, dx + off, id, kk > 0);
+                }
+                mma_commit(bar(B_GDONE));
+                TRACE(cc, 15);
+            };
+            // chunk cc's Gram may go: its tile has landed and the Gram region is free
+            auto g_ready = [&](int cc) -> bool {
+                return mbar_test(bar(B_GGO), (uint32_t)cc & 1u) &&
+                       mbar_test(bar(B_FULL0 + (cc & 1)), (uint32_t)(cc >> 1) & 1u);
+            };
+            // With phi = identity the Gram of chunk c+1 is released once chunk c's has
+            // been read; it is issued as soon as it can go, ahead of chunk c's W/U
+            // when those are not ready yet.
+            const bool early = !elu;
+            int gnext = 0;   // first chunk whose Gram has not been issued
             for (int c = 0; c < nch && ok; ++c) {
                 const int b = c & 1;
                 const uint32_t st = xq(b);
-                if (!wait_fast(bar(B_GGO), (uint32_t)c & 1u, limit, s_abort) ||
-                    !wait_fast(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                {   // G = [X; Q] X^T  (rows 0..63: X X^T, rows 64..127: Q X^T)
-                    const uint32_t id = idesc_bf16(128, 64, false, false);
-                    const uint64_t dx = sdesc_sw128(st + XQ_X0, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
-                        mma_bf16(tmem + COL_G, dx + off, dx + off, id, kk > 0);
+                if (gnext == c) {
+                    if (!wait_fast(bar(B_GGO), (uint32_t)c & 1u, limit, s_abort) ||
+                        !wait_fast(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(bar(B_GDONE));
-                    TRACE(c, 15);
+                    issue_g(c);
+                    ++gnext;
                 }
                 if (!falcon) continue;
-                if (!wait_fast(bar(B_TRDY), (uint32_t)c & 1u, limit, s_abort) ||
-                    !wait_fast(bar(B_FULLY), (uint32_t)c & 1u, limit, s_abort) ||
+                {   // T of chunk c; meanwhile the next Gram, once it can go
+                    const uint64_t t0 = globaltimer();
+                    for (;;) {
+                        if (early && gnext == c + 1 && gnext < nch && g_ready(gnext)) {
+                            issue_g(gnext);
+                            ++gnext;
+                        }
+                        if (mbar_try_wait_sleep(bar(B_TRDY), (uint32_t)c & 1u, 200u)) break;
+                        if (*s_abort || globaltimer() - t0 > limit) { ok = false; break; }
+                    }
+                    if (!ok) break;
+                }
+                if (!wait_fast(bar(B_FULLY), (uint32_t)c & 1u, limit, s_abort) ||
                     (c >= 2 && !wait_fast(bar(B_RFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort))) {
                     ok = false;
                     break;
@@ -337,9 +353,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int c = 0; c < nch && ok; ++c) {
                 const int b = c & 1;
                 const uint32_t st = xq(b);
+                // Falcon-1: R first (it needs only W and S); O1 once the output
+                // accumulators of chunk c-1 have been read
                 if (!wait_fast(bar(B_WRDY), (uint32_t)c & 1u, limit, s_abort) ||
                     !wait_fast(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort) ||
-                    (c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort))) {
+                    (!falcon && c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort))) {
                     ok = false;
                     break;
                 }
@@ -351,16 +369,19 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const uint64_t dp = sdesc_sw128(pb, 16, 1024);
                 const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);
                 if (falcon) {
-                    // R^T += S^T (-W^T);  O1^T = S^T Q^T
+                    // R^T += S^T (-W^T), then O1^T = S^T Q^T
                     const uint32_t id_mm = idesc_bf16(128, 64, true, true);
                     const uint64_t dw = sdesc_sw128(sb + OFF_WTB, 8192, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    for (int kk = 0; kk < 8; ++kk)
                         mma_bf16(tmem + COL_R0 + 64 * b, ds + kk * 128, dw + kk * 128, id_mm, 1);
+                    mma_commit(bar(B_RDONE));
+                    if (c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
                         mma_bf16(tmem + COL_O1, ds + kk * 128,
                                  dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
-                    }
-                    mma_commit(bar(B_RDONE));
                     TRACE(c, 17);
                     if (!wait_fast(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
                     tc_fence_after();
@@ -445,29 +466,49 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             // chunk 0's first key row is patched with phi(k_init) before the Gram is released
             if (falcon && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            if (lane == 0) TRACE(cc, 21);
             if (falcon) {
                 const uint32_t xs = xq(b);
+                // |x_t|^2: the diagonal of each 16x16 block X_blk X_blk^T, on the warp's
+                // bf16 MMAs (fp32 accumulate).  One ldmatrix.x4 gives the A fragment of
+                // a 16-wide k step; its row-0..7 / row-8..15 halves are the B fragments
+                // of the two 8-column tiles.
                 float n[2];
+                {
+                    const int g = lane >> 2;
+                    const int mrow = ((lane >> 3) & 1) * 8 + (lane & 7);   // row within the block
+                    const int mchk = lane >> 4;                              // 16-byte chunk within the k step
+                    float dg0[4], dg1[4];   // diagonal values held by lanes with t4 == g / 2
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = lane + 32 * u;
-                    // the whole 128-byte row of each half, chunks in a lane-rotated
-                    // order (the squared norm does not depend on the swizzle)
-                    const uint32_t row = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
-                    float acc = 0.f;
+                    for (int blk = 0; blk < 4; ++blk) {
+                        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                        const uint32_t r = (uint32_t)(16 * blk + mrow);
 #pragma unroll
-                    for (int hx = 0; hx < 2; ++hx) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            float f[8];
-                            unpack8(ld_shared_v4(xs + (hx ? XQ_X1 : XQ_X0) + row +
-                                                 (uint32_t)((k + lane) & 7) * 16u), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            uint32_t f[4];
+                            ldmatrix_x4(xs + ((ks >> 2) ? XQ_X1 : XQ_X0) +
+                                            sw128(r, (uint32_t)(2 * (ks & 3) + mchk)), f);
+                            mma_bf16_16x8x16(d0, f[0], f[1], f[2], f[3], f[0], f[2]);
+                            mma_bf16_16x8x16(d1, f[0], f[1], f[2], f[3], f[1], f[3]);
                         }
+                        dg0[blk] = (g & 1) ? d0[1] : d0[0];   // (g, g) of rows 0..7
+                        dg1[blk] = (g & 1) ? d1[3] : d1[2];   // (8+g, 8+g) of rows 8..15
                     }
-                    n[u] = acc;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int rr = lane & 15, blk0 = 2 * u + (lane >> 4);
+                        const int src = 4 * (rr & 7) + ((rr & 7) >> 1);
+                        float v = 0.f;
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk) {
+                            const float a0 = __shfl_sync(0xffffffffu, dg0[blk], src);
+                            const float a1 = __shfl_sync(0xffffffffu, dg1[blk], src);
+                            if (blk == blk0) v = (rr < 8) ? a0 : a1;
+                        }
+                        n[u] = v;
+                    }
                 }
+                if (lane == 0) TRACE(cc, 22);
                 float eta[2], gam[2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -540,6 +581,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Ms = reinterpret_cast<float *>(sm + OFF_MS);
+        // the blocks of T above its diagonal 16x16 blocks are zero and stay so
+        for (int i = kidx; i < 64 * 64; i += KGROUP) {
+            const int r = i >> 6, cc = i & 63;
+            if ((cc >> 4) > (r >> 4)) Tf[f64i(r, cc)] = 0.f;
+        }
         auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool ok = wait_bar(bb, parity, limit, s_abort);
             return !bar_or(BAR_KG, KGROUP, !ok);
@@ -672,140 +718,36 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
 
             if (kidx == 0) TRACE(c, 4);
-            // ---- T = (I + L)^{-1} on warp-level tf32 MMAs.  bf16 T and -T diag(Gm)
-            //      live where L does: their writes wait until the last read of L
-            //      (the second merge level), so fragments are kept in registers.
-            const int gq = lane >> 2, tq = lane & 3;
-            const float *gmv = vb + V_GM / 4;
-            auto put_t = [&](int r, int cc, float v0, float v1) {   // bf16 pair (r, cc..cc+1)
-                const uint32_t off = sw128((uint32_t)r, (uint32_t)cc >> 3) + ((uint32_t)(cc & 7) << 1);
-                st_shared_u32(sb + OFF_TB + off, pack_bf16(v0, v1));
-                st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[cc], -v1 * gmv[cc + 1]));
-            };
-            float tpair[4];      // phase-1 tile (warps of half 0)
-            float t2b[4];        // phase-2 tile
-            float tdiag[2][4];   // diagonal block kw of T (C fragments, warps of half 0)
-            if (h == 0) {
-                // diagonal block kw: (I + L)^{-1} = (I - L)(I + L^2)(I + L^4)(I + L^8),
-                // four 16x16x16 products on the warp's tf32 MMAs
-                const int g = gq, t4 = tq;
-                const int base = 16 * kw;
-                float *sa0 = Ms + kw * 768;   // A order
-                float *sa1 = sa0 + 256;       // A order
-                float *sb0 = sa0 + 512;       // B order
-                // fragments of L (kept in registers) and of I - L
-                uint32_t la[2][4], lb[2][2][2], ia[2][4];
+            // ---- T = (I + L)^{-1} on the CUDA cores in fp32 (the warp-level tensor
+            //      MMAs would queue behind the chunk MMAs on the shared tensor pipe).
+            //      Blocks of 16: forward substitution on the diagonal blocks, then
+            //      T21 = -T22 L21 T11 at 16 -> 32 and 32 -> 64.  Tf's blocks above the
+            //      diagonal blocks stay zero, so every product runs over whole blocks.
+            if (h == 0 && lane < 16) {
+                // diagonal block kw, column j: T[r][j] = [r == j] - sum_{s<r} L[r][s] T[s][j]
+                const int j = lane, B0 = 16 * kw;
+                float tc[16];
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    frag_a64(Lf, base, base + 8 * ks, lane, la[ks]);
+                for (int r = 0; r < 16; ++r) {
+                    float acc = (r == j) ? 1.f : 0.f;
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) frag_b64(Lf, base + 8 * ks, base + 8 * nt, lane, lb[ks][nt]);
-                    const int r0 = g, r1 = g + 8, c0 = 8 * ks + t4, c1 = c0 + 4;
-                    ia[ks][0] = __float_as_uint((r0 == c0 ? 1.f : 0.f) - __uint_as_float(la[ks][0]));
-                    ia[ks][1] = __float_as_uint((r1 == c0 ? 1.f : 0.f) - __uint_as_float(la[ks][1]));
-                    ia[ks][2] = __float_as_uint((r0 == c1 ? 1.f : 0.f) - __uint_as_float(la[ks][2]));
-                    ia[ks][3] = __float_as_uint((r1 == c1 ? 1.f : 0.f) - __uint_as_float(la[ks][3]));
-                }
-                auto mm = [&](float (&d)[2][4], auto fa, auto fb) {
+                    for (int s4 = 0; 4 * s4 < r; ++s4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(
+                            Lf + (B0 + r) * 64 + ((((B0 >> 2) + s4) ^ r) << 2));
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
-#pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        uint32_t a4[4];
-                        fa(ks, a4);
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt) {
-                            uint32_t b2[2];
-                            fb(ks, nt, b2);
-                            mma_tf32_16x8x8(d[nt], a4, b2);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * s4 + e < r) acc = fmaf(-lv[e], tc[4 * s4 + e], acc);
                     }
-                };
-                auto from_a = [&](const float *M) {
-                    return [M, lane](int ks, uint32_t (&a4)[4]) {
-                        const float4 v = *reinterpret_cast<const float4 *>(M + ((ks * 32 + lane) << 2));
-                        a4[0] = __float_as_uint(v.x); a4[1] = __float_as_uint(v.y);
-                        a4[2] = __float_as_uint(v.z); a4[3] = __float_as_uint(v.w);
-                    };
-                };
-                auto from_b = [&](const float *M) {
-                    return [M, lane](int ks, int nt, uint32_t (&b2)[2]) {
-                        const float2 v = *reinterpret_cast<const float2 *>(M + (((ks * 2 + nt) * 32 + lane) << 1));
-                        b2[0] = __float_as_uint(v.x); b2[1] = __float_as_uint(v.y);
-                    };
-                };
-                auto put = [&](float *M, bool aord, const float (&d)[2][4]) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int c0 = 8 * nt + 2 * t4;
-                        if (aord) {
-                            M[a_ord(g, c0)] = d[nt][0];     M[a_ord(g, c0 + 1)] = d[nt][1];
-                            M[a_ord(g + 8, c0)] = d[nt][2]; M[a_ord(g + 8, c0 + 1)] = d[nt][3];
-                        } else {
-                            M[b_ord(g, c0)] = d[nt][0];     M[b_ord(g, c0 + 1)] = d[nt][1];
-                            M[b_ord(g + 8, c0)] = d[nt][2]; M[b_ord(g + 8, c0 + 1)] = d[nt][3];
-                        }
-                    }
-                };
-                auto regA = [&](const uint32_t (&f)[2][4]) {
-                    return [&f](int ks, uint32_t (&a4)[4]) {
-                        a4[0] = f[ks][0]; a4[1] = f[ks][1]; a4[2] = f[ks][2]; a4[3] = f[ks][3];
-                    };
-                };
-                auto regB = [&](int ks, int nt, uint32_t (&b2)[2]) { b2[0] = lb[ks][nt][0]; b2[1] = lb[ks][nt][1]; };
-                float d[2][4], p[2][4];
-                mm(d, regA(la), regB);                  // L^2
-                put(sa0, true, d);
-                put(sb0, false, d);
-                __syncwarp();
-                mm(p, regA(ia), from_b(sb0));           // (I - L) L^2
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {        // A2 = (I - L) + (I - L) L^2
-                    const int c0 = 8 * nt + 2 * t4;
-                    p[nt][0] += (g == c0 ? 1.f : 0.f) - Lf[f64i(base + g, base + c0)];
-                    p[nt][1] += (g == c0 + 1 ? 1.f : 0.f) - Lf[f64i(base + g, base + c0 + 1)];
-                    p[nt][2] += (g + 8 == c0 ? 1.f : 0.f) - Lf[f64i(base + g + 8, base + c0)];
-                    p[nt][3] += (g + 8 == c0 + 1 ? 1.f : 0.f) - Lf[f64i(base + g + 8, base + c0 + 1)];
+                    tc[r] = acc;
                 }
-                put(sa1, true, p);
-                mm(d, from_a(sa0), from_b(sb0));        // L^4
-                __syncwarp();
-                put(sa0, true, d);
-                put(sb0, false, d);
-                __syncwarp();
-                {
-                    float q[2][4];
-                    mm(q, from_a(sa1), from_b(sb0));    // A2 L^4
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) p[nt][e] += q[nt][e];   // A3
-                }
-                mm(d, from_a(sa0), from_b(sb0));        // L^8
-                __syncwarp();
-                put(sa1, true, p);
-                put(sb0, false, d);
-                __syncwarp();
-                mm(d, from_a(sa1), from_b(sb0));        // A3 L^8
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int c0 = base + 8 * nt + 2 * t4;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) tdiag[nt][e] = d[nt][e] + p[nt][e];   // T_kk
-                    Tf[f64i(base + g, c0)] = tdiag[nt][0];
-                    Tf[f64i(base + g, c0 + 1)] = tdiag[nt][1];
-                    Tf[f64i(base + g + 8, c0)] = tdiag[nt][2];
-                    Tf[f64i(base + g + 8, c0 + 1)] = tdiag[nt][3];
-                    if ((kw & 1) == 0) {   // zero the fp32 block above, inside the 32-block
-                        Tf[f64i(base + g, c0 + 16)] = 0.f;
-                        Tf[f64i(base + g, c0 + 17)] = 0.f;
-                        Tf[f64i(base + g + 8, c0 + 16)] = 0.f;
-                        Tf[f64i(base + g + 8, c0 + 17)] = 0.f;
-                    }
-                }
+                for (int r = 0; r < 16; ++r) Tf[f64i(B0 + r, B0 + j)] = tc[r];
             }
             gsync();
             if (kidx == 0) TRACE(c, 5);
+            const int gq = lane >> 2, tq = lane & 3;
+            float t2b[4];        // phase-2 tile
             if (h == 0) {   // pairs (1,0) and (3,2): warp kw -> pair p, 8-column tile nt
                 const int p = kw >> 1, nt = kw & 1;
                 const int rb = 16 + 32 * p, cb = 32 * p;
@@ -838,10 +780,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 Tf[f64i(rb + g, c0 + 1)] = -u[1];
                 Tf[f64i(rb + g + 8, c0)] = -u[2];
                 Tf[f64i(rb + g + 8, c0 + 1)] = -u[3];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) tpair[e] = -u[e];
             }
             gsync();
+            if (kidx == 0) TRACE(c, 20);
             // second level: 32x32 tiles, one 16x8 tile per warp: row tile rt, column tile ct
             const int rt = kw >> 1, ct = 2 * (kw & 1) + h;
             {   // M2 = L[32:64, 0:32] T[0:32, 0:32]
@@ -861,8 +802,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 Ms[f32i(16 * rt + g + 8, c0 + 1)] = m[3];
             }
             gsync();
+            if (kidx == 0) TRACE(c, 30);
             {   // T[32:64, 0:32] = -T[32:64, 32:64] M2
-                const int g = gq, t4 = tq;
                 float u[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
@@ -874,30 +815,36 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) t2b[e] = -u[e];
             }
-            {   // L is dead: write every bf16 block, zero the upper ones
+            {   // bf16 T and -T diag(Gm), K-major rows t, where L was (L is dead now)
+                const float *gmv = vb + V_GM / 4;
                 const int g = gq, t4 = tq;
-                const int base = 16 * kw;
-                if (h == 0) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int cd = base + 8 * nt + 2 * t4;
-                        put_t(base + g, cd, tdiag[nt][0], tdiag[nt][1]);
-                        put_t(base + g + 8, cd, tdiag[nt][2], tdiag[nt][3]);
-                    }
-                    const int p = kw >> 1, nt = kw & 1;
-                    const int rb = 16 + 32 * p, c1 = 32 * p + 8 * nt + 2 * t4;
-                    put_t(rb + g, c1, tpair[0], tpair[1]);
-                    put_t(rb + g + 8, c1, tpair[2], tpair[3]);
-                }
                 const int r2 = 32 + 16 * rt + g, c2 = 8 * ct + 2 * t4;
+                auto put_t = [&](int r, int cc, float v0, float v1) {   // bf16 pair (r, cc..cc+1)
+                    const uint32_t off = sw128((uint32_t)r, (uint32_t)cc >> 3) + ((uint32_t)(cc & 7) << 1);
+                    st_shared_u32(sb + OFF_TB + off, pack_bf16(v0, v1));
+                    st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[cc], -v1 * gmv[cc + 1]));
+                };
                 put_t(r2, c2, t2b[0], t2b[1]);
                 put_t(r2 + 8, c2, t2b[2], t2b[3]);
-                // upper blocks of row block kw: the two warps of the quarter split them
-                for (int cb = kw + 1; cb < 4; ++cb) {
-                    if (((cb - kw - 1) & 1) != h) continue;
-                    const int r = base + (lane >> 1), cc = 16 * cb + 8 * (lane & 1);
-                    st_shared_v4(sb + OFF_TB + sw128((uint32_t)r, (uint32_t)cc >> 3), 0u, 0u, 0u, 0u);
-                    st_shared_v4(sb + OFF_TPB + sw128((uint32_t)r, (uint32_t)cc >> 3), 0u, 0u, 0u, 0u);
+                // the rest from Tf: row t, columns 16q..16q+15 (rows 32.., columns ..31 are T21 above)
+                const int t = kidx >> 2, q = kidx & 3;
+                if (t < 32 || q >= 2) {
+                    const float4 *gm4 = reinterpret_cast<const float4 *>(gmv) + 4 * q;
+                    float tv[16], tp[16];
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(Tf + f64i(t, 16 * q + 4 * e4));
+                        const float4 g4 = gm4[e4];
+                        tv[4 * e4] = v4.x; tv[4 * e4 + 1] = v4.y; tv[4 * e4 + 2] = v4.z; tv[4 * e4 + 3] = v4.w;
+                        tp[4 * e4] = -v4.x * g4.x; tp[4 * e4 + 1] = -v4.y * g4.y;
+                        tp[4 * e4 + 2] = -v4.z * g4.z; tp[4 * e4 + 3] = -v4.w * g4.w;
+                    }
+#pragma unroll
+                    for (int h8 = 0; h8 < 2; ++h8) {
+                        const uint32_t off = sw128((uint32_t)t, (uint32_t)(2 * q + h8));
+                        st_row8_bf16(sb + OFF_TB + off, tv + 8 * h8);
+                        st_row8_bf16(sb + OFF_TPB + off, tp + 8 * h8);
+                    }
                 }
             }
             fence_proxy_async();
