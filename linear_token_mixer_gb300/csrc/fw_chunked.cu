@@ -181,7 +181,8 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-               const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
+               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+               const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -215,6 +216,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmo);
     }
     tc_fence_before();
     __syncthreads();
@@ -309,6 +311,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 {   // T of chunk c; meanwhile the next Gram, once it can go
                     const uint64_t t0 = globaltimer();
                     for (;;) {
+                        if (mbar_test(bar(B_TRDY), (uint32_t)c & 1u)) break;   // W/U first
                         if (early && gnext == c + 1 && gnext < nch && g_ready(gnext)) {
                             issue_g(gnext);
                             ++gnext;
@@ -922,7 +925,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const int b = c & 1;
             const int64_t tok0 = (int64_t)c * C;
             if (falcon) {
-                // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand)
+                // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
+                //      the output store of chunk c-1 has read the R^T buffer by then
+                if (srow == 0) bulk_wait_read0();
                 if (!gwait(bar(B_RDONE), (uint32_t)c & 1u) ||
                     !gwait(bar(B_GV0 + b), (uint32_t)(c >> 1) & 1u)) { ok = false; break; }
                 if (srow == 0) TRACE(c, 10);
@@ -930,19 +935,18 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const float *wc = vec(b) + V_WC / 4;
                 if (srow < C)   // the gate warp may recycle this gate block once S(c) is done
                     reinterpret_cast<float *>(sm + OFF_SGV)[srow] = vec(b)[V_G / 4 + srow];
+                {
+                    float r[64];
+                    tmem_ld64(tmem + lane_base + COL_R0 + 64 * b, r);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float r[32];
-                    tmem_ld32(tmem + lane_base + COL_R0 + 64 * b + 32 * h, r);
-#pragma unroll
-                    for (int c16 = 0; c16 < 4; ++c16) {
-                        const float4 w0 = *reinterpret_cast<const float4 *>(wc + 32 * h + 8 * c16);
-                        const float4 w1 = *reinterpret_cast<const float4 *>(wc + 32 * h + 8 * c16 + 4);
+                    for (int c16 = 0; c16 < 8; ++c16) {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(wc + 8 * c16);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(wc + 8 * c16 + 4);
                         const float *rr = r + 8 * c16;
                         const float w8[8] = {rr[0] * w0.x, rr[1] * w0.y, rr[2] * w0.z, rr[3] * w0.w,
                                              rr[4] * w1.x, rr[5] * w1.y, rr[6] * w1.z, rr[7] * w1.w};
-                        st_row8_bf16(sb + OFF_RA + sw128(srow, 4 * h + c16), rr);
-                        st_row8_bf16(sb + OFF_RB + sw128(srow, 4 * h + c16), w8);
+                        st_row8_bf16(sb + OFF_RA + sw128(srow, c16), rr);
+                        st_row8_bf16(sb + OFF_RB + sw128(srow, c16), w8);
                     }
                 }
                 tc_fence_before();
@@ -955,7 +959,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 }
             }
 
-            // ---- state carry
+            // ---- state carry (linear attention: the output store of chunk c-1 has read
+            //      its staging tile before this chunk's is written)
+            if (srow == 0) bulk_wait_read0();
             if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
             if (srow == 0) TRACE(c, 12);
             tc_fence_after();
@@ -967,23 +973,28 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 gC_next = vec(b1)[V_GC / 4];
             }
 #pragma unroll 1
-            for (int q = 0; q < 8; ++q) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + COL_S + 16 * q, v);
-                if (srow == 0 && q == 0) TRACE(c, 23);
-                if (last) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + srow) * D + 16 * q);
+            for (int q4 = 0; q4 < 2; ++q4) {   // 64 columns per TMEM round trip
+                float v[64];
+                tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+                if (srow == 0 && q4 == 0) TRACE(c, 23);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                } else {
-                    const uint32_t blk = sb + OFF_SB + (uint32_t)(q >> 2) * 16384u;
-                    const uint32_t c16 = (uint32_t)((16 * q) & 63) >> 3;
-                    st_row8_bf16(blk + sw128(srow, c16), v);
-                    st_row8_bf16(blk + sw128(srow, c16 + 1), v + 8);
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int q = 4 * q4 + qq;
+                    float *vq = v + 16 * qq;
+                    if (last) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + srow) * D + 16 * q);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] *= gC_next;
-                    tmem_st16(tmem + lane_base + COL_S + 16 * q, v);
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_float4(vq[4 * e], vq[4 * e + 1], vq[4 * e + 2], vq[4 * e + 3]);
+                    } else {
+                        const uint32_t blk = sb + OFF_SB + (uint32_t)q4 * 16384u;
+                        const uint32_t c16 = (uint32_t)(2 * qq);
+                        st_row8_bf16(blk + sw128(srow, c16), vq);
+                        st_row8_bf16(blk + sw128(srow, c16 + 1), vq + 8);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) vq[e] *= gC_next;
+                        tmem_st16(tmem + lane_base + COL_S + 16 * q, vq);
+                    }
                 }
             }
             if (srow == 0) TRACE(c, 24);
@@ -995,42 +1006,43 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (srow == 0) TRACE(c, 13);
             if (!last && srow == 0) mbar_arrive(bar(B_SRDY));
 
-            // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t.  Lanes j and j^1 swap
-            //      halves so each stores a bf16 pair (t, j..j+1): even lanes the
-            //      even tokens, odd lanes the odd ones.
+            // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t, staged as a [t][j] bf16 tile
+            //      in the R^T buffer (free once S(c) and O2(c) are done: s_done),
+            //      then one tensor store (rows past T are not written)
             {
                 const float *gv = reinterpret_cast<const float *>(sm + OFF_SGV);
-                const bool odd = (lane & 1) != 0;
-                const int jj = srow & ~1;
-                uint32_t *og = reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(a.o) +
-                                                           (chain * T + tok0) * D + jj);
-                const int64_t nvalid = T - tok0;
+                __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RA) + srow;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     float o1[32], o2[32];
-                    tmem_ld32(tmem + lane_base + COL_O1 + 32 * h, o1);
-                    tmem_ld32(tmem + lane_base + COL_O2 + 32 * h, o2);
+                    tmem_ld32x2(tmem + lane_base + COL_O1 + 32 * h, tmem + lane_base + COL_O2 + 32 * h, o1, o2);
                     if (srow == 0) TRACE(c, 26 + 2 * h);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int t = 32 * h + e;
-                        const float2 g2 = falcon ? *reinterpret_cast<const float2 *>(gv + t)
-                                                 : make_float2(1.f, 1.f);
-                        const float v0 = fmaf(g2.x, o1[e], o2[e]);
-                        const float v1 = fmaf(g2.y, o1[e + 1], o2[e + 1]);
-                        const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-                        const int tt = odd ? t + 1 : t;
-                        const uint32_t w = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
-                        if (tt < nvalid) og[(int64_t)tt * (D / 2)] = w;
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 g4 = falcon ? *reinterpret_cast<const float4 *>(gv + 32 * h + 4 * e4)
+                                                 : make_float4(1.f, 1.f, 1.f, 1.f);
+                        const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int t = 32 * h + 4 * e4 + e;
+                            ot[t * D] = __float2bfloat16_rn(fmaf(gg[e], o1[4 * e4 + e], o2[4 * e4 + e]));
+                        }
                     }
                     if (srow == 0) TRACE(c, 27 + 2 * h);
                 }
             }
+            fence_proxy_async();
             tc_fence_before();
             gsync();
-            if (srow == 0) { TRACE(c, 14); mbar_arrive(bar(B_OFREE)); }
+            if (srow == 0) {
+                tma_store_3d(&tmo, sb + OFF_RA, 0, (int)tok0, (int)chain);
+                bulk_commit();
+                TRACE(c, 14);
+                mbar_arrive(bar(B_OFREE));
+            }
         }
         if (!ok && srow == 0) fail_now();
+        if (srow == 0) bulk_wait0();   // no output store in flight at exit
     }
 
     // every role meets here; tensor memory is released last
@@ -1056,16 +1068,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [n_chains][T][128] bf16 viewed as a 3-D tensor (d, T, chain); 64 x 64 boxes.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc) {
+// [n_chains][T][128] bf16 viewed as a 3-D tensor (d, T, chain); boxes of box_d x 64:
+// 64 x 64 with the 128-byte swizzle for the tile loads, 128 x 64 plain for the
+// output store.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t box_d = 64,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)nc};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
+    cuuint32_t box[3] = {box_d, (cuuint32_t)C, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1090,14 +1105,15 @@ extern "C" int fw_debug_read_trace(unsigned long long *dst, int n) {
 #endif
 
 cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
-        !make_map(&tv, a.v, a.T, a.n_chains))
+        !make_map(&tv, a.v, a.T, a.n_chains) ||
+        !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    chunked_kernel<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, a);
+    chunked_kernel<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
     return cudaGetLastError();
 }
 
