@@ -379,6 +379,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     for (int kk = 0; kk < 8; ++kk)
                         mma_bf16(tmem + COL_R0 + 64 * b, ds + kk * 128, dw + kk * 128, id_mm, 1);
                     mma_commit(bar(B_RDONE));
+                    TRACE(c, 0);
                     if (c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
@@ -484,18 +485,20 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     float dg0[4], dg1[4];   // diagonal values held by lanes with t4 == g / 2
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk) {
-                        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                        // two accumulators per tile (k halves): dependent chains of 4
+                        float d0[2][4] = {}, d1[2][4] = {};
                         const uint32_t r = (uint32_t)(16 * blk + mrow);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {
                             uint32_t f[4];
                             ldmatrix_x4(xs + ((ks >> 2) ? XQ_X1 : XQ_X0) +
                                             sw128(r, (uint32_t)(2 * (ks & 3) + mchk)), f);
-                            mma_bf16_16x8x16(d0, f[0], f[1], f[2], f[3], f[0], f[2]);
-                            mma_bf16_16x8x16(d1, f[0], f[1], f[2], f[3], f[1], f[3]);
+                            mma_bf16_16x8x16(d0[ks >> 2], f[0], f[1], f[2], f[3], f[0], f[2]);
+                            mma_bf16_16x8x16(d1[ks >> 2], f[0], f[1], f[2], f[3], f[1], f[3]);
                         }
-                        dg0[blk] = (g & 1) ? d0[1] : d0[0];   // (g, g) of rows 0..7
-                        dg1[blk] = (g & 1) ? d1[3] : d1[2];   // (8+g, 8+g) of rows 8..15
+                        // (g, g) of rows 0..7 and (8+g, 8+g) of rows 8..15
+                        dg0[blk] = (g & 1) ? d0[0][1] + d0[1][1] : d0[0][0] + d0[1][0];
+                        dg1[blk] = (g & 1) ? d1[0][3] + d1[1][3] : d1[0][2] + d1[1][2];
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -520,7 +523,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     gam[u] = 1.f;
                     if (tok < T) {
                         const bool pair = (tok > 0) || (a.k_init != nullptr);
-                        eta[u] = pair ? nb[u] / (n[u] + nl[u] + a.eps) : 0.f;
+                        eta[u] = pair ? __fdividef(nb[u], n[u] + nl[u] + a.eps) : 0.f;
                         gam[u] = 1.f - eta[u] * nl[u];
                     }
                 }
@@ -927,7 +930,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (falcon) {
                 // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
                 //      the output store of chunk c-1 has read the R^T buffer by then
-                if (srow == 0) bulk_wait_read0();
+                if (srow == 0) { TRACE(c, 31); bulk_wait_read0(); }
                 if (!gwait(bar(B_RDONE), (uint32_t)c & 1u) ||
                     !gwait(bar(B_GV0 + b), (uint32_t)(c >> 1) & 1u)) { ok = false; break; }
                 if (srow == 0) TRACE(c, 10);
