@@ -62,26 +62,26 @@ constexpr int BAR_KG = 1, BAR_SG = 2;   // named barriers of the two groups
 constexpr int GROUP = 128, KGROUP = 256;
 
 constexpr uint32_t KB = 1024;
+constexpr int NST = 3;       // depth of the key/query tile ring (and of the gate blocks)
 // shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t OFF_XQ0 = 0, OFF_XQ1 = 32 * KB;   // X0 Q0 X1 Q1 (8 KB each)
+constexpr uint32_t OFF_XQ0 = 0;         // NST stages of X0 Q0 X1 Q1 (8 KB each)
 constexpr uint32_t XQ_X0 = 0, XQ_Q0 = 8 * KB, XQ_X1 = 16 * KB, XQ_Q1 = 24 * KB;
-constexpr uint32_t OFF_Y0 = 64 * KB;   // V tile (Falcon-1: the only one; linattn: stage 0)
-constexpr uint32_t OFF_Y1 = 80 * KB;   // linattn: V of stage 1; Falcon-1: L (fp32), then T
+constexpr uint32_t OFF_Y0 = 96 * KB;    // V tile (Falcon-1: the only one; linattn: stage 0)
+constexpr uint32_t OFF_Y1 = 112 * KB;   // linattn: V of stage 1; Falcon-1: L (fp32), then T
 constexpr uint32_t OFF_LF = OFF_Y1;            // L, fp32 64x64, 16-byte-group swizzle
 constexpr uint32_t OFF_TB = OFF_Y1;            // T, bf16, K-major rows t (after L is dead)
 constexpr uint32_t OFF_TPB = OFF_Y1 + 8 * KB;  // T diag(Gm), bf16
-constexpr uint32_t OFF_PB0 = 96 * KB, OFF_PB1 = 104 * KB;   // P, bf16, K-major rows t
-constexpr uint32_t OFF_WTB = 112 * KB;  // -W^T, bf16, rows i (MN-major B operand)
-constexpr uint32_t OFF_RA = 128 * KB;   // R^T, bf16, rows j (K-major A operand)
-constexpr uint32_t OFF_RB = 144 * KB;   // (diag(w) R)^T, bf16, rows j (K-major B operand)
-constexpr uint32_t OFF_SB = 160 * KB;   // S, bf16, rows i, two 64-column blocks (16 KB each)
-constexpr uint32_t OFF_TF = 192 * KB;   // T, fp32 64x64, swizzled
-constexpr uint32_t OFF_MS = 208 * KB;   // solver scratch: 4 warps x 3 fragment-ordered 16x16, or 32x32
-constexpr uint32_t OFF_VEC = 220 * KB;  // two gate blocks
+constexpr uint32_t OFF_PB0 = 128 * KB, OFF_PB1 = 136 * KB;   // P, bf16, K-major rows t
+constexpr uint32_t OFF_WTB = 144 * KB;  // -W^T, bf16, rows i (MN-major B operand)
+constexpr uint32_t OFF_RA = 160 * KB;   // R^T, bf16, rows j (K-major A operand)
+constexpr uint32_t OFF_RB = 176 * KB;   // (diag(w) R)^T, bf16, rows j (K-major A operand)
+constexpr uint32_t OFF_TF = 192 * KB;   // T, fp32 64x64, swizzled (linattn: V of stage 2)
+constexpr uint32_t OFF_MS = 208 * KB;   // solver scratch: 32 x 32 fp32
+constexpr uint32_t OFF_VEC = 212 * KB;  // NST gate blocks
 constexpr uint32_t VEC_BYTES = 1792;
 constexpr uint32_t V_ETA = 0, V_GAM = 256, V_G = 512, V_GM = 768, V_WC = 1024, V_Q32 = 1280,
                    V_GC = 1536;
-constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_BYTES;
+constexpr uint32_t OFF_BAR = OFF_VEC + NST * VEC_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
 constexpr uint32_t OFF_SGV = OFF_MISC + 64;    // G_t of the chunk the state group is on
 constexpr uint32_t SMEM_BYTES = OFF_SGV + 256;
@@ -90,14 +90,16 @@ static_assert(SMEM_ALLOC <= 227 * KB, "shared memory budget");
 
 // mbarriers
 enum {
-    B_FULL0 = 0, B_FULL1, B_EMPTY0, B_EMPTY1, B_FULLY, B_YFREE, B_GGO, B_GDONE, B_TRDY,
-    B_WUDONE, B_WRDY, B_GV0, B_GV1, B_PFREE0, B_PFREE1, B_SRDY, B_RDONE, B_RRDY, B_SDONE,
-    B_OFREE, B_RFREE0, B_RFREE1, B_KDRAIN, B_SDRAIN, B_NEVER, B_COUNT
+    B_FULL0 = 0, B_EMPTY0 = B_FULL0 + NST, B_FULLY = B_EMPTY0 + NST, B_YFREE, B_GGO, B_GDONE,
+    B_TRDY, B_WUDONE, B_WRDY, B_GV0, B_PFREE0 = B_GV0 + NST, B_PFREE1, B_SRDY, B_RDONE, B_RRDY,
+    B_SDONE, B_OFREE, B_RFREE, B_KDRAIN, B_SDRAIN, B_NEVER, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
-// tensor-memory columns (128 lanes x 32 bit)
-constexpr uint32_t COL_G = 0, COL_W = 64, COL_R0 = 128, COL_O1 = 256, COL_O2 = 320, COL_S = 384;
+// tensor-memory columns (128 lanes x 32 bit).  The state is held transposed (lane j),
+// with a bf16 copy (two i per column) that is the A operand of R and O1.
+constexpr uint32_t COL_G = 0, COL_W = 64, COL_R = 128, COL_SB = 192, COL_O1 = 256, COL_O2 = 320,
+                   COL_S = 384;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint64_t kDrainNs = 2000000000ull;
@@ -200,7 +202,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 4);
     auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8u * (uint32_t)i; };
     auto vec = [&](int b) -> float * { return reinterpret_cast<float *>(sm + OFF_VEC + b * VEC_BYTES); };
-    auto xq = [&](int b) -> uint32_t { return sb + (b ? OFF_XQ1 : OFF_XQ0); };
+    auto xq = [&](int st) -> uint32_t { return sb + OFF_XQ0 + (uint32_t)st * 32u * KB; };
+    // linear attention: V of ring stage st (Falcon-1 keeps its single V tile at OFF_Y0)
+    auto yv_of = [&](int st) -> uint32_t { return sb + (st == 0 ? OFF_Y0 : st == 1 ? OFF_Y1 : OFF_TF); };
     auto fail_now = [&]() {
         *s_abort = 1;
         atomicExch(a.err, kDevErrTimeout);
@@ -227,11 +231,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // ================================================================ TMA producer
         if (lane == 0) {
             const int shift = falcon ? 1 : 0;
-            int nxq0 = 0, nxq1 = 0, ny = 0;
+            int nfill[NST] = {}, ny = 0;
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
-                const int b = c & 1;
-                if (c >= 2 && !wait_fast(bar(B_EMPTY0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort)) {
+                const int b = c % NST;
+                if (c >= NST && !wait_fast(bar(B_EMPTY0 + b), (uint32_t)((c / NST) - 1) & 1u, limit, s_abort)) {
                     ok = false;
                     break;
                 }
@@ -244,11 +248,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
                 tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
                 if (!falcon) {
-                    const uint32_t yv = sb + (b ? OFF_Y1 : OFF_Y0);
+                    const uint32_t yv = yv_of(b);
                     tma_load_3d(yv, &tmv, 0, y, (int)chain, full);
                     tma_load_3d(yv + 8 * KB, &tmv, 64, y, (int)chain, full);
                 }
-                if (b) ++nxq1; else ++nxq0;
+                ++nfill[b];
                 TRACE(c, 19);
                 if (falcon) {
                     if (c >= 1 && !wait_fast(bar(B_YFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) {
@@ -263,8 +267,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             if (!ok) fail_now();
             // never leave a copy in flight into this CTA's shared memory
-            if (nxq0) mbar_wait(bar(B_FULL0), (uint32_t)(nxq0 - 1) & 1u, kDrainNs);
-            if (nxq1) mbar_wait(bar(B_FULL1), (uint32_t)(nxq1 - 1) & 1u, kDrainNs);
+            for (int b = 0; b < NST; ++b)
+                if (nfill[b]) mbar_wait(bar(B_FULL0 + b), (uint32_t)(nfill[b] - 1) & 1u, kDrainNs);
             if (ny) mbar_wait(bar(B_FULLY), (uint32_t)(ny - 1) & 1u, kDrainNs);
         }
         __syncwarp();
@@ -276,7 +280,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             auto issue_g = [&](int cc) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, false, false);
-                const uint64_t dx = sdesc_sw128(xq(cc & 1) + XQ_X0, 16, 1024);
+                const uint64_t dx = sdesc_sw128(xq(cc % NST) + XQ_X0, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
@@ -288,7 +292,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             // chunk cc's Gram may go: its tile has landed and the Gram region is free
             auto g_ready = [&](int cc) -> bool {
                 return mbar_test(bar(B_GGO), (uint32_t)cc & 1u) &&
-                       mbar_test(bar(B_FULL0 + (cc & 1)), (uint32_t)(cc >> 1) & 1u);
+                       mbar_test(bar(B_FULL0 + cc % NST), (uint32_t)(cc / NST) & 1u);
             };
             // With phi = identity the Gram of chunk c+1 is released once chunk c's has
             // been read; it is issued as soon as it can go, ahead of chunk c's W/U
@@ -296,11 +300,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const bool early = !elu;
             int gnext = 0;   // first chunk whose Gram has not been issued
             for (int c = 0; c < nch && ok; ++c) {
-                const int b = c & 1;
+                const int b = c % NST;
                 const uint32_t st = xq(b);
                 if (gnext == c) {
                     if (!wait_fast(bar(B_GGO), (uint32_t)c & 1u, limit, s_abort) ||
-                        !wait_fast(bar(B_FULL0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort)) {
+                        !wait_fast(bar(B_FULL0 + b), (uint32_t)(c / NST) & 1u, limit, s_abort)) {
                         ok = false;
                         break;
                     }
@@ -321,8 +325,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     }
                     if (!ok) break;
                 }
+                // U^T goes where R^T of chunk c-1 was: its epilogue has read it
                 if (!wait_fast(bar(B_FULLY), (uint32_t)c & 1u, limit, s_abort) ||
-                    (c >= 2 && !wait_fast(bar(B_RFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort))) {
+                    (c >= 1 && !wait_fast(bar(B_RFREE), (uint32_t)(c - 1) & 1u, limit, s_abort))) {
                     ok = false;
                     break;
                 }
@@ -337,7 +342,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         mma_bf16(tmem + COL_W, dx + kk * 128, dtp + kk * 2, id, kk > 0);
-                        mma_bf16(tmem + COL_R0 + 64 * b, dy + kk * 128, dt + kk * 2, id, kk > 0);
+                        mma_bf16(tmem + COL_R, dy + kk * 128, dt + kk * 2, id, kk > 0);
                     }
                     mma_commit(bar(B_WUDONE));
                     mma_commit(bar(B_YFREE));
@@ -354,7 +359,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         if (lane == 0) {
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
-                const int b = c & 1;
+                const int b = c % NST, pi = c & 1;
                 const uint32_t st = xq(b);
                 // Falcon-1: R first (it needs only W and S); O1 once the output
                 // accumulators of chunk c-1 have been read
@@ -365,56 +370,57 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     break;
                 }
                 tc_fence_after();
-                const uint32_t pb = sb + (b ? OFF_PB1 : OFF_PB0);
-                const uint32_t id_mk = idesc_bf16(128, 64, true, false);
-                const uint64_t ds = sdesc_sw128(sb + OFF_SB, 16384, 1024);
+                const uint32_t pb = sb + (pi ? OFF_PB1 : OFF_PB0);
+                const uint32_t sa = tmem + COL_SB;   // bf16 S^T, A operand: 8 columns per k step
+                const uint32_t id_mk = idesc_bf16(128, 64, false, false);
                 const uint64_t dq = sdesc_sw128(st + XQ_Q0, 16, 1024);
                 const uint64_t dp = sdesc_sw128(pb, 16, 1024);
-                const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);
+                const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);   // X as MN-major B (N = i)
                 if (falcon) {
                     // R^T += S^T (-W^T), then O1^T = S^T Q^T
-                    const uint32_t id_mm = idesc_bf16(128, 64, true, true);
+                    const uint32_t id_mm = idesc_bf16(128, 64, false, true);
                     const uint64_t dw = sdesc_sw128(sb + OFF_WTB, 8192, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + COL_R0 + 64 * b, ds + kk * 128, dw + kk * 128, id_mm, 1);
+                        mma_bf16_ta(tmem + COL_R, sa + 8 * kk, dw + kk * 128, id_mm, 1);
                     mma_commit(bar(B_RDONE));
                     TRACE(c, 0);
                     if (c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + COL_O1, ds + kk * 128,
-                                 dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
+                        mma_bf16_ta(tmem + COL_O1, sa + 8 * kk,
+                                    dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
                     TRACE(c, 17);
                     if (!wait_fast(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
                     tc_fence_after();
-                    // O2^T = R^T P^T;  S += X^T (diag(w) R)
+                    // O2^T = R^T P^T;  S^T += (diag(w) R)^T X
                     const uint32_t id_kk = idesc_bf16(128, 64, false, false);
                     const uint64_t dra = sdesc_sw128(sb + OFF_RA, 16, 1024);
                     const uint64_t drb = sdesc_sw128(sb + OFF_RB, 16, 1024);
-                    const uint32_t id_s = idesc_bf16(128, 128, true, false);
+                    const uint32_t id_s = idesc_bf16(128, 128, false, true);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        mma_bf16(tmem + COL_S, dx + kk * 128, drb + kk * 2, id_s, 1);
+                        mma_bf16(tmem + COL_S, drb + kk * 2, dx + kk * 128, id_s, 1);
                         mma_bf16(tmem + COL_O2, dra + kk * 2, dp + kk * 2, id_kk, kk > 0);
                     }
                 } else {
-                    const uint64_t dv = sdesc_sw128(sb + (b ? OFF_Y1 : OFF_Y0), 8192, 1024);
-                    // O1^T = S^T Q^T, O2^T = V^T P^T;  S += X^T V
+                    const uint64_t dv = sdesc_sw128(yv_of(b), 8192, 1024);
+                    // O1^T = S^T Q^T, O2^T = V^T P^T;  S^T += V^T X
                     const uint32_t id_s = idesc_bf16(128, 128, true, true);
+                    const uint32_t id_v = idesc_bf16(128, 64, true, false);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        mma_bf16(tmem + COL_O1, ds + kk * 128,
-                                 dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
+                        mma_bf16_ta(tmem + COL_O1, sa + 8 * kk,
+                                    dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
                         if (kk < 4) {
-                            mma_bf16(tmem + COL_S, dx + kk * 128, dv + kk * 128, id_s, 1);
-                            mma_bf16(tmem + COL_O2, dv + kk * 128, dp + kk * 2, id_mk, kk > 0);
+                            mma_bf16(tmem + COL_S, dv + kk * 128, dx + kk * 128, id_s, 1);
+                            mma_bf16(tmem + COL_O2, dv + kk * 128, dp + kk * 2, id_v, kk > 0);
                         }
                     }
                 }
                 mma_commit(bar(B_SDONE));
-                mma_commit(bar(B_PFREE0 + b));
+                mma_commit(bar(B_PFREE0 + pi));
                 mma_commit(bar(B_EMPTY0 + b));
                 TRACE(c, 18);
             }
@@ -425,18 +431,18 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         __syncwarp();
     } else if (warp == 3) {
         // ================================================================ gates
-        // Step sizes and decay products of chunk cc, published in gate block cc & 1
+        // Step sizes and decay products of chunk cc, published in gate block cc % NST
         // as soon as the chunk's keys land: |x_t|^2 straight from the staged X tile,
         // eta_t = beta_t / (|x_t|^2 + lambda_t + eps), gamma_t = 1 - eta_t lambda_t,
         // then the in-chunk prefix and suffix products (division-free).
         // Lane l holds tokens l and l + 32 of the chunk.
-        // (Block cc & 1 was last read for chunk cc - 2 by the key group (L, P, the
-        // solve) and the state group (the R epilogue), all of which precede the S
-        // MMAs of chunk cc - 2, whose completion released the stage chunk cc's
-        // keys were loaded into.)
+        // (Block cc % NST was last read for chunk cc - NST by the key group (L, P,
+        // the solve) and the state group (the R epilogue), all of which precede the
+        // S MMAs of chunk cc - NST, whose completion released the ring stage chunk
+        // cc's keys were loaded into.)
         bool ok = true;
         if (!falcon) {   // linear attention: eta = 1, no decay
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < NST; ++b) {
                 float *v = vec(b);
                 for (int t = lane; t < C; t += 32) {
                     v[V_ETA / 4 + t] = 1.f;
@@ -464,9 +470,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         load_bl(0);
 #pragma unroll 1
         for (int cc = 0; cc < nch && ok; ++cc) {
-            const int b = cc & 1;
+            const int b = cc % NST;
             float *vg = vec(b);
-            bool w = wait_bar(bar(B_FULL0 + b), (uint32_t)(cc >> 1) & 1u, limit, s_abort);
+            bool w = wait_bar(bar(B_FULL0 + b), (uint32_t)(cc / NST) & 1u, limit, s_abort);
             // chunk 0's first key row is patched with phi(k_init) before the Gram is released
             if (falcon && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -588,7 +594,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Ms = reinterpret_cast<float *>(sm + OFF_MS);
         // the blocks of T above its diagonal 16x16 blocks are zero and stay so
-        for (int i = kidx; i < 64 * 64; i += KGROUP) {
+        // (linear attention keeps a V tile there instead)
+        for (int i = kidx; falcon && i < 64 * 64; i += KGROUP) {
             const int r = i >> 6, cc = i & 63;
             if ((cc >> 4) > (r >> 4)) Tf[f64i(r, cc)] = 0.f;
         }
@@ -605,8 +612,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // feature map on the loaded tiles of chunk cc and the k_init patch, then
         // release the Gram MMA of chunk cc
         auto prep_go = [&](int cc) -> bool {
-            const uint32_t st_ = xq(cc & 1);
-            if (!gwait(bar(B_FULL0 + (cc & 1)), (uint32_t)(cc >> 1) & 1u)) return false;
+            const uint32_t st_ = xq(cc % NST);
+            if (!gwait(bar(B_FULL0 + cc % NST), (uint32_t)(cc / NST) & 1u)) return false;
             // ---- feature map on the loaded tiles (row t, a quarter of its 16-byte
             //      chunks per thread), k_init patch
             {
@@ -658,14 +665,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         if (ok) ok = prep_go(0);
 #pragma unroll 1
         for (int c = 0; c < nch && ok; ++c) {
-            const int b = c & 1;
-            float *vb = vec(b);
+            const int b = c & 1;             // P buffer
+            float *vb = vec(c % NST);        // gate block
             if (c > 0 && !early && !prep_go(c)) { ok = false; break; }
             if (kidx == 0) TRACE(c, 2);
             {   // P buffer b free (chunk c-2's O2 done), Gram of chunk c done, gates of chunk c
                 bool w = c < 2 || wait_bar(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort);
                 w = w && wait_bar(bar(B_GDONE), (uint32_t)c & 1u, limit, s_abort);
-                w = w && wait_bar(bar(B_GV0 + b), (uint32_t)(c >> 1) & 1u, limit, s_abort);
+                w = w && wait_bar(bar(B_GV0 + c % NST), (uint32_t)(c / NST) & 1u, limit, s_abort);
                 if (bar_or(BAR_KG, KGROUP, !w)) { ok = false; break; }
             }
             tc_fence_after();
@@ -887,7 +894,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         auto gsync = [&]() { bar_sync(BAR_SG, GROUP); };
         bool ok = true;
 
-        // initial state: TMEM <- G_{C-1}(chunk 0) S0, bf16 copy for the MMAs
+        // bf16 copy of 32 state entries (i = i0 .. i0+31 of column j): the A operand
+        // of R and O1 holds two consecutive i per column, the even one low
+        auto put_sb = [&](int i0, const float *v) {
+            float pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(v[2 * e], v[2 * e + 1]));
+            tmem_st16(tmem + lane_base + COL_SB + (uint32_t)(i0 / 2), pk);
+        };
+
+        // initial state, transposed (this thread holds column j = srow of S):
+        // TMEM <- G_{C-1}(chunk 0) S0^T, and the bf16 copy
         float gC0 = 1.f;
         if (falcon) {
             if (!gwait(bar(B_GV0), 0)) ok = false;
@@ -895,44 +912,33 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         }
         if (ok) {
 #pragma unroll 1
-            for (int q = 0; q < 8; ++q) {
-                float v[16];
-                if (a.S0) {
-                    const float4 *src = reinterpret_cast<const float4 *>(a.S0 + (chain * D + srow) * D + 16 * q);
+            for (int q = 0; q < 4; ++q) {   // i = 32q .. 32q+31
+                float v[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 f = src[e];
-                        v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
-                    }
-                } else {
+                for (int e = 0; e < 32; ++e)
+                    v[e] = a.S0 ? a.S0[(chain * D + 32 * q + e) * D + srow] : 0.f;
+                put_sb(32 * q, v);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                }
-                const uint32_t blk = sb + OFF_SB + (uint32_t)(q >> 2) * 16384u;
-                const uint32_t c16 = (uint32_t)((16 * q) & 63) >> 3;
-                st_row8_bf16(blk + sw128(srow, c16), v);
-                st_row8_bf16(blk + sw128(srow, c16 + 1), v + 8);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] *= gC0;
-                tmem_st16(tmem + lane_base + COL_S + 16 * q, v);
+                for (int e = 0; e < 32; ++e) v[e] *= gC0;
+                tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+                tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
             }
             tmem_st_wait();
             tc_fence_before();
-            fence_proxy_async();
             gsync();
             if (srow == 0) mbar_arrive(bar(B_SRDY));
         }
 
 #pragma unroll 1
         for (int c = 0; c < nch && ok; ++c) {
-            const int b = c & 1;
+            const int b = c % NST;   // gate block
             const int64_t tok0 = (int64_t)c * C;
             if (falcon) {
                 // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
                 //      the output store of chunk c-1 has read the R^T buffer by then
                 if (srow == 0) { TRACE(c, 31); bulk_wait_read0(); }
                 if (!gwait(bar(B_RDONE), (uint32_t)c & 1u) ||
-                    !gwait(bar(B_GV0 + b), (uint32_t)(c >> 1) & 1u)) { ok = false; break; }
+                    !gwait(bar(B_GV0 + b), (uint32_t)(c / NST) & 1u)) { ok = false; break; }
                 if (srow == 0) TRACE(c, 10);
                 tc_fence_after();
                 const float *wc = vec(b) + V_WC / 4;
@@ -940,7 +946,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     reinterpret_cast<float *>(sm + OFF_SGV)[srow] = vec(b)[V_G / 4 + srow];
                 {
                     float r[64];
-                    tmem_ld64(tmem + lane_base + COL_R0 + 64 * b, r);
+                    tmem_ld64(tmem + lane_base + COL_R, r);
 #pragma unroll
                     for (int c16 = 0; c16 < 8; ++c16) {
                         const float4 w0 = *reinterpret_cast<const float4 *>(wc + 8 * c16);
@@ -958,7 +964,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (srow == 0) {
                     TRACE(c, 11);
                     mbar_arrive(bar(B_RRDY));
-                    mbar_arrive(bar(B_RFREE0 + b));
+                    mbar_arrive(bar(B_RFREE));
                 }
             }
 
@@ -971,40 +977,31 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const bool last = (c + 1 == nch);
             float gC_next = 1.f;
             if (falcon && !last) {
-                const int b1 = (c + 1) & 1;
-                if (!gwait(bar(B_GV0 + b1), (uint32_t)((c + 1) >> 1) & 1u)) { ok = false; break; }
+                const int b1 = (c + 1) % NST;
+                if (!gwait(bar(B_GV0 + b1), (uint32_t)((c + 1) / NST) & 1u)) { ok = false; break; }
                 gC_next = vec(b1)[V_GC / 4];
             }
 #pragma unroll 1
-            for (int q4 = 0; q4 < 2; ++q4) {   // 64 columns per TMEM round trip
+            for (int q4 = 0; q4 < 2; ++q4) {   // i = 64 q4 .. 64 q4 + 63: one TMEM round trip
                 float v[64];
                 tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
                 if (srow == 0 && q4 == 0) TRACE(c, 23);
+                if (last) {   // S_T[i][j], consecutive j across the warp
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int q = 4 * q4 + qq;
-                    float *vq = v + 16 * qq;
-                    if (last) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + srow) * D + 16 * q);
+                    for (int e = 0; e < 64; ++e) a.S_T[(chain * D + 64 * q4 + e) * D + srow] = v[e];
+                } else {
+                    put_sb(64 * q4, v);
+                    put_sb(64 * q4 + 32, v + 32);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_float4(vq[4 * e], vq[4 * e + 1], vq[4 * e + 2], vq[4 * e + 3]);
-                    } else {
-                        const uint32_t blk = sb + OFF_SB + (uint32_t)q4 * 16384u;
-                        const uint32_t c16 = (uint32_t)(2 * qq);
-                        st_row8_bf16(blk + sw128(srow, c16), vq);
-                        st_row8_bf16(blk + sw128(srow, c16 + 1), vq + 8);
+                    for (int e = 0; e < 64; ++e) v[e] *= gC_next;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) vq[e] *= gC_next;
-                        tmem_st16(tmem + lane_base + COL_S + 16 * q, vq);
-                    }
+                    for (int qq = 0; qq < 4; ++qq) tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
                 }
             }
             if (srow == 0) TRACE(c, 24);
             tmem_st_wait();
             if (srow == 0) TRACE(c, 25);
             tc_fence_before();
-            fence_proxy_async();
             gsync();
             if (srow == 0) TRACE(c, 13);
             if (!last && srow == 0) mbar_arrive(bar(B_SRDY));
