@@ -67,15 +67,15 @@ constexpr int NST = 3;       // depth of the key/query tile ring (and of the gat
 constexpr uint32_t OFF_XQ0 = 0;         // NST stages of X0 Q0 X1 Q1 (8 KB each)
 constexpr uint32_t XQ_X0 = 0, XQ_Q0 = 8 * KB, XQ_X1 = 16 * KB, XQ_Q1 = 24 * KB;
 constexpr uint32_t OFF_Y0 = 96 * KB;    // V tile (Falcon-1: the only one; linattn: stage 0)
-constexpr uint32_t OFF_Y1 = 112 * KB;   // linattn: V of stage 1; Falcon-1: L (fp32), then T
-constexpr uint32_t OFF_LF = OFF_Y1;            // L, fp32 64x64, 16-byte-group swizzle
-constexpr uint32_t OFF_TB = OFF_Y1;            // T, bf16, K-major rows t (after L is dead)
-constexpr uint32_t OFF_TPB = OFF_Y1 + 8 * KB;  // T diag(Gm), bf16
+constexpr uint32_t OFF_Y1 = 112 * KB;   // linattn: V of stage 1; Falcon-1: solve region 0
+// Falcon-1 solve regions (16 KB each, alternating by chunk parity): L (fp32 64x64,
+// 16-byte-group swizzle), then the bf16 T (K-major rows t) and -T diag(Gm) in its
+// two halves once L is dead; the other region holds the fp32 T of the solve.
 constexpr uint32_t OFF_PB0 = 128 * KB, OFF_PB1 = 136 * KB;   // P, bf16, K-major rows t
 constexpr uint32_t OFF_WTB = 144 * KB;  // -W^T, bf16, rows i (MN-major B operand)
 constexpr uint32_t OFF_RA = 160 * KB;   // R^T, bf16, rows j (K-major A operand)
 constexpr uint32_t OFF_RB = 176 * KB;   // (diag(w) R)^T, bf16, rows j (K-major A operand)
-constexpr uint32_t OFF_TF = 192 * KB;   // T, fp32 64x64, swizzled (linattn: V of stage 2)
+constexpr uint32_t OFF_TF = 192 * KB;   // Falcon-1: solve region 1; linattn: V of stage 2
 constexpr uint32_t OFF_MS = 208 * KB;   // solver scratch: 32 x 32 fp32
 constexpr uint32_t OFF_VEC = 212 * KB;  // NST gate blocks
 constexpr uint32_t VEC_BYTES = 1792;
@@ -203,6 +203,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8u * (uint32_t)i; };
     auto vec = [&](int b) -> float * { return reinterpret_cast<float *>(sm + OFF_VEC + b * VEC_BYTES); };
     auto xq = [&](int st) -> uint32_t { return sb + OFF_XQ0 + (uint32_t)st * 32u * KB; };
+    // solve region of chunk cc (Falcon-1)
+    auto lreg = [&](int cc) -> uint32_t { return (cc & 1) ? OFF_TF : OFF_Y1; };
     // linear attention: V of ring stage st (Falcon-1 keeps its single V tile at OFF_Y0)
     auto yv_of = [&](int st) -> uint32_t { return sb + (st == 0 ? OFF_Y0 : st == 1 ? OFF_Y1 : OFF_TF); };
     auto fail_now = [&]() {
@@ -335,9 +337,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 {   // -W^T = X^T (-T diag Gm)^T, U^T = Y^T T^T
                     const uint32_t id = idesc_bf16(128, 64, true, false);
                     const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);
-                    const uint64_t dtp = sdesc_sw128(sb + OFF_TPB, 16, 1024);
+                    const uint64_t dtp = sdesc_sw128(sb + lreg(c) + 8 * KB, 16, 1024);
                     const uint64_t dy = sdesc_sw128(sb + OFF_Y0, 8192, 1024);
-                    const uint64_t dt = sdesc_sw128(sb + OFF_TB, 16, 1024);
+                    const uint64_t dt = sdesc_sw128(sb + lreg(c), 16, 1024);
                     // two independent accumulator chains, interleaved
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -590,15 +592,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         const int kidx = h * 128 + kt;             // 0..255 within the group
         const int kw = warp & 3;                   // lane quarter
         const uint32_t lane_base = (uint32_t)(kw * 32) << 16;
-        float *Lf = reinterpret_cast<float *>(sm + OFF_LF);
-        float *Tf = reinterpret_cast<float *>(sm + OFF_TF);
         float *Ms = reinterpret_cast<float *>(sm + OFF_MS);
-        // the blocks of T above its diagonal 16x16 blocks are zero and stay so
-        // (linear attention keeps a V tile there instead)
-        for (int i = kidx; falcon && i < 64 * 64; i += KGROUP) {
-            const int r = i >> 6, cc = i & 63;
-            if ((cc >> 4) > (r >> 4)) Tf[f64i(r, cc)] = 0.f;
-        }
+        // L of chunk c and the fp32 T alternate between the two solve regions (the
+        // bf16 T of chunk c overwrites L(c) once L is dead, and L(c+1) goes where
+        // the fp32 T(c) was, while the W/U products of chunk c still read the bf16 T)
         auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool ok = wait_bar(bb, parity, limit, s_abort);
             return !bar_or(BAR_KG, KGROUP, !ok);
@@ -663,73 +660,84 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // runs while chunk c's solve and W/U products do.
         const bool early = !elu;
         if (ok) ok = prep_go(0);
-#pragma unroll 1
-        for (int c = 0; c < nch && ok; ++c) {
-            const int b = c & 1;             // P buffer
-            float *vb = vec(c % NST);        // gate block
-            if (c > 0 && !early && !prep_go(c)) { ok = false; break; }
-            if (kidx == 0) TRACE(c, 2);
-            {   // P buffer b free (chunk c-2's O2 done), Gram of chunk c done, gates of chunk c
-                bool w = c < 2 || wait_bar(bar(B_PFREE0 + b), (uint32_t)((c >> 1) - 1) & 1u, limit, s_abort);
-                w = w && wait_bar(bar(B_GDONE), (uint32_t)c & 1u, limit, s_abort);
-                w = w && wait_bar(bar(B_GV0 + c % NST), (uint32_t)(c / NST) & 1u, limit, s_abort);
-                if (bar_or(BAR_KG, KGROUP, !w)) { ok = false; break; }
+        // L and P of chunk cc (L into Lw): waits for the P buffer (chunk cc-2's O2
+        // done), the Gram and the gates of chunk cc, then releases the Gram region
+        auto lp = [&](int cc, float *Lw) -> bool {
+            const float *vg = vec(cc % NST);
+            if (kidx == 0) TRACE(cc, 2);
+            {
+                bool w = cc < 2 || wait_bar(bar(B_PFREE0 + (cc & 1)), (uint32_t)((cc >> 1) - 1) & 1u, limit, s_abort);
+                w = w && wait_bar(bar(B_GDONE), (uint32_t)cc & 1u, limit, s_abort);
+                w = w && wait_bar(bar(B_GV0 + cc % NST), (uint32_t)(cc / NST) & 1u, limit, s_abort);
+                if (bar_or(BAR_KG, KGROUP, !w)) return false;
             }
             tc_fence_after();
             float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
             tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
-
-            // ---- L and P from G, columns 32h..32h+31 of row kt.  A half's running
-            //      product starts from prod_{i=32}^{u} gamma_i when its row reaches
-            //      past column 31 (division-free).
-            {
-                const float4 *eta4 = reinterpret_cast<const float4 *>(vb + V_ETA / 4) + 8 * h;
-                const float4 *gam4 = reinterpret_cast<const float4 *>(vb + V_GAM / 4) + 8 * h;
-                const bool lrow = kt < C;
-                if (lrow && !falcon) {
-                    // linear attention needs no L
-                } else {
-                    const int t = lrow ? kt : kt - C;
-                    const int top = lrow ? t - 1 : t;        // last active column
-                    float dz = 1.f;
-                    if (h == 0 && top >= 32) dz = vb[V_Q32 / 4 + top];
-#pragma unroll
-                    for (int q = 7; q >= 0; --q) {
-                        const float4 e4 = eta4[q], y4 = gam4[q];
-                        const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
-                        const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
-#pragma unroll
-                        for (int e = 3; e >= 0; --e) {
-                            const int s2 = 4 * q + e;              // local column
-                            const bool act = (32 * h + s2) <= top;
-                            g[s2] = act ? dz * ev[e] * g[s2] : 0.f;
-                            if (act) dz *= yv[e];
+                // ---- L and P from G, columns 32h..32h+31 of row kt.  A half's running
+                //      product starts from prod_{i=32}^{u} gamma_i when its row reaches
+                //      past column 31 (division-free).
+                {
+                    const float4 *eta4 = reinterpret_cast<const float4 *>(vg + V_ETA / 4) + 8 * h;
+                    const float4 *gam4 = reinterpret_cast<const float4 *>(vg + V_GAM / 4) + 8 * h;
+                    const bool lrow = kt < C;
+                    if (lrow && !falcon) {
+                        // linear attention needs no L
+                    } else {
+                        const int t = lrow ? kt : kt - C;
+                        const int top = lrow ? t - 1 : t;        // last active column
+                        float dz = 1.f;
+                        if (h == 0 && top >= 32) dz = vg[V_Q32 / 4 + top];
+    #pragma unroll
+                        for (int q = 7; q >= 0; --q) {
+                            const float4 e4 = eta4[q], y4 = gam4[q];
+                            const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+                            const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+    #pragma unroll
+                            for (int e = 3; e >= 0; --e) {
+                                const int s2 = 4 * q + e;              // local column
+                                const bool act = (32 * h + s2) <= top;
+                                g[s2] = act ? dz * ev[e] * g[s2] : 0.f;
+                                if (act) dz *= yv[e];
+                            }
+                        }
+                        if (lrow) {
+    #pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                *reinterpret_cast<float4 *>(Lw + t * 64 + (((8 * h + q) ^ (t & 15)) << 2)) =
+                                    make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                        } else {
+                            const uint32_t pb = sb + ((cc & 1) ? OFF_PB1 : OFF_PB0);
+    #pragma unroll
+                            for (int c16 = 0; c16 < 4; ++c16)
+                                st_row8_bf16(pb + sw128(t, 4 * h + c16), g + 8 * c16);
                         }
                     }
-                    if (lrow) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4 *>(Lf + t * 64 + (((8 * h + q) ^ (t & 15)) << 2)) =
-                                make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
-                    } else {
-                        const uint32_t pb = sb + (b ? OFF_PB1 : OFF_PB0);
-#pragma unroll
-                        for (int c16 = 0; c16 < 4; ++c16)
-                            st_row8_bf16(pb + sw128(t, 4 * h + c16), g + 8 * c16);
-                    }
                 }
-            }
             tc_fence_before();
             fence_proxy_async();
             gsync();
-            if (kidx == 0) TRACE(c, 3);
-            const bool more = (c + 1 < nch);
-            if (early && more && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
-            if (!falcon) {
+            if (kidx == 0) TRACE(cc, 3);
+            if (early && cc + 1 < nch && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
+            return true;
+        };
+        if (!falcon) {
+#pragma unroll 1
+            for (int c = 0; c < nch && ok; ++c) {
+                if (c > 0 && !early && !prep_go(c)) { ok = false; break; }
+                if (!lp(c, nullptr)) { ok = false; break; }
                 if (kidx == 0) mbar_arrive(bar(B_WRDY));
-                continue;
             }
-
+        }
+        // Falcon-1 (phi = identity): L/P of chunk c+1 runs while the W/U products of
+        // chunk c are in flight
+        if (falcon && ok) ok = lp(0, reinterpret_cast<float *>(sm + lreg(0)));
+#pragma unroll 1
+        for (int c = 0; falcon && c < nch && ok; ++c) {
+            float *vb = vec(c % NST);        // gate block
+            const uint32_t tbo = lreg(c);    // L(c), then the bf16 T and -T diag(Gm) of chunk c
+            float *Lf = reinterpret_cast<float *>(sm + tbo);
+            float *Tf = reinterpret_cast<float *>(sm + lreg(c + 1));
             if (kidx == 0) TRACE(c, 4);
             // ---- T = (I + L)^{-1} on the CUDA cores in fp32 (the warp-level tensor
             //      MMAs would queue behind the chunk MMAs on the shared tensor pipe).
@@ -756,6 +764,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tf[f64i(B0 + r, B0 + j)] = tc[r];
+            } else if (h == 1) {
+                // T[0:16, 16:32] and T[32:48, 48:64] are zero (the merges read them)
+                const int r = kt >> 2, c4 = 4 * (kt & 3);
+                const int rr = (r < 16) ? r : 16 + r, cc4 = (r < 16) ? 16 + c4 : 48 + c4;
+                *reinterpret_cast<float4 *>(Tf + f64i(rr, cc4)) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             gsync();
             if (kidx == 0) TRACE(c, 5);
@@ -834,19 +847,21 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const int r2 = 32 + 16 * rt + g, c2 = 8 * ct + 2 * t4;
                 auto put_t = [&](int r, int cc, float v0, float v1) {   // bf16 pair (r, cc..cc+1)
                     const uint32_t off = sw128((uint32_t)r, (uint32_t)cc >> 3) + ((uint32_t)(cc & 7) << 1);
-                    st_shared_u32(sb + OFF_TB + off, pack_bf16(v0, v1));
-                    st_shared_u32(sb + OFF_TPB + off, pack_bf16(-v0 * gmv[cc], -v1 * gmv[cc + 1]));
+                    st_shared_u32(sb + tbo + off, pack_bf16(v0, v1));
+                    st_shared_u32(sb + tbo + 8 * KB + off, pack_bf16(-v0 * gmv[cc], -v1 * gmv[cc + 1]));
                 };
                 put_t(r2, c2, t2b[0], t2b[1]);
                 put_t(r2 + 8, c2, t2b[2], t2b[3]);
                 // the rest from Tf: row t, columns 16q..16q+15 (rows 32.., columns ..31 are T21 above)
                 const int t = kidx >> 2, q = kidx & 3;
                 if (t < 32 || q >= 2) {
+                    const bool zero = (t < 32 && q >= 2);   // above the diagonal 32-blocks
                     const float4 *gm4 = reinterpret_cast<const float4 *>(gmv) + 4 * q;
                     float tv[16], tp[16];
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
-                        const float4 v4 = *reinterpret_cast<const float4 *>(Tf + f64i(t, 16 * q + 4 * e4));
+                        const float4 v4 = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                               : *reinterpret_cast<const float4 *>(Tf + f64i(t, 16 * q + 4 * e4));
                         const float4 g4 = gm4[e4];
                         tv[4 * e4] = v4.x; tv[4 * e4 + 1] = v4.y; tv[4 * e4 + 2] = v4.z; tv[4 * e4 + 3] = v4.w;
                         tp[4 * e4] = -v4.x * g4.x; tp[4 * e4 + 1] = -v4.y * g4.y;
@@ -855,14 +870,15 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
                     for (int h8 = 0; h8 < 2; ++h8) {
                         const uint32_t off = sw128((uint32_t)t, (uint32_t)(2 * q + h8));
-                        st_row8_bf16(sb + OFF_TB + off, tv + 8 * h8);
-                        st_row8_bf16(sb + OFF_TPB + off, tp + 8 * h8);
+                        st_row8_bf16(sb + tbo + off, tv + 8 * h8);
+                        st_row8_bf16(sb + tbo + 8 * KB + off, tp + 8 * h8);
                     }
                 }
             }
             fence_proxy_async();
             gsync();
             if (kidx == 0) { TRACE(c, 6); mbar_arrive(bar(B_TRDY)); }
+            if (c + 1 < nch && !lp(c + 1, Tf)) { ok = false; break; }   // T(c) fp32 is dead
 
             // ---- -W^T -> bf16 rows i, once W^T(c) is done and R(c-1) has read the old one
             if (!gwait(bar(B_WUDONE), (uint32_t)c & 1u)) { ok = false; break; }
