@@ -50,6 +50,38 @@ def _peaks():
 ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
+KERNEL_SOURCES = {
+    "chunked prefill": ("fw_chunked.cu", "fw_sm100.cuh", "fw_internal.cuh"),
+    "recurrent (SIMT)": ("fw_recurrent.cu", "fw_internal.cuh"),
+}
+
+
+def sources_sha256(kernel):
+    """Hash of the source files a kernel is built from (to tell whether a stored
+    ncu traffic figure was taken on the kernel as it stands)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_token_mixer_gb300", "csrc")
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def stored_traffic(kernel, workload):
+    """DRAM bytes read + written per launch from the committed ncu summary
+    (profiles/traffic.json), or None when the kernel changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get("%s/%s" % (kernel, workload))
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def algorithmic_bytes_prefill(w):
     """Bytes a prefill must move: q, k, v read and o written once, beta and
     lambda read once (Falcon-1), S0 read (when given) and S_T written once."""
@@ -127,6 +159,17 @@ class Clocks:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx or None,
                 "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def job_rate(ms_local, units_per_rank, world, dist=None, device=None):
+    """Whole-job throughput over `world` ranks: the slowest rank's time (max over
+    ranks) and all ranks' units divided by it.  Returns (ms_max, units per second)."""
+    ms = float(ms_local)
+    if dist is not None and world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, units_per_rank * world / (ms / 1e3)
 
 
 def timed(fn, K, W, stream):
@@ -361,27 +404,24 @@ def main():
         dist.barrier()
     fw.check(stream)
     per = [a.elapsed_time(b) for a, b in ev]
-    ms_total = ev[0][0].elapsed_time(ev[-1][1])
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total, value = job_rate(ev[0][0].elapsed_time(ev[-1][1]), w.B * w.T * args.steps, world,
+                               dist, dev)
     kern_ms = statistics.mean(per)
-    tokens = w.B * w.T * args.steps * world
-    value = tokens / (ms_total / 1e3)
 
     algo_bytes = algorithmic_bytes_prefill(w)
     achieved_gbs = algo_bytes / (kern_ms / 1e3) / 1e9
     chunked = w.dtype == torch.bfloat16 and w.d == 128
     if chunked:
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": achieved_gbs / peaks["hbm"], "traffic": None,
+                "frac": achieved_gbs / peaks["hbm"],
+                "traffic": stored_traffic("chunked prefill", w.name),
                 "kernel": "chunked prefill", "peak_source": peaks["src"],
                 "algorithmic_bytes_per_launch": algo_bytes}
     else:
         tf = recurrence_flops(w) / (kern_ms / 1e3) / 1e12
         roof = {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
-                "frac": tf / ALU_FP32_TFLOPS, "traffic": None, "kernel": "recurrent (SIMT)",
+                "frac": tf / ALU_FP32_TFLOPS,
+                "traffic": stored_traffic("recurrent (SIMT)", w.name), "kernel": "recurrent (SIMT)",
                 "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"}
     mm_tf = matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12
 

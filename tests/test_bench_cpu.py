@@ -1,0 +1,77 @@
+"""Host logic of bench.py that needs no GPU: the over-ranks aggregation of a
+multi-process run (two gloo ranks on CPU) and the ncu-traffic lookup that is
+only trusted while the kernel's sources match the capture."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, ms_by_rank, units, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms, rate = bench.job_rate(ms_by_rank[rank], units, world, dist, torch.device("cpu"))
+        out[rank] = (ms, rate)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_job_rate_single_process():
+    ms, rate = bench.job_rate(2.0, 1000, 1)
+    assert ms == 2.0 and rate == pytest.approx(1000 / 2e-3)
+
+
+def test_job_rate_two_gloo_ranks_takes_the_slowest_rank():
+    world, units = 2, 4096
+    ms_by_rank = [1.5, 2.5]
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(world, port, ms_by_rank, units, out), nprocs=world, join=True)
+        got = dict(out)
+    for r in range(world):
+        ms, rate = got[r]
+        assert ms == pytest.approx(2.5)                       # max over ranks
+        assert rate == pytest.approx(world * units / 2.5e-3)  # all ranks' units / slowest time
+
+
+def _fake_root(tmp_path, record_sha):
+    csrc = tmp_path / "linear_token_mixer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in set(n for v in bench.KERNEL_SOURCES.values() for n in v):
+        (csrc / name).write_text("// source of %s\n" % name)
+    (tmp_path / "profiles").mkdir()
+    rec = {"chunked prefill/falcon1_bf16": {"sources_sha256": record_sha,
+                                            "dram_bytes_per_launch": 123456}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    return tmp_path
+
+
+def test_stored_traffic_only_for_the_captured_sources(tmp_path, monkeypatch):
+    root = _fake_root(tmp_path, "0" * 64)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    # sources changed since the capture: no traffic figure
+    assert bench.stored_traffic("chunked prefill", "falcon1_bf16") is None
+    rec = json.loads((root / "profiles" / "traffic.json").read_text())
+    rec["chunked prefill/falcon1_bf16"]["sources_sha256"] = bench.sources_sha256("chunked prefill")
+    (root / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.stored_traffic("chunked prefill", "falcon1_bf16") == 123456
+    # another workload has no record
+    assert bench.stored_traffic("chunked prefill", "linattn_bf16") is None
+    # editing a kernel source invalidates the record
+    (root / "linear_token_mixer_gb300" / "csrc" / "fw_sm100.cuh").write_text("// edited\n")
+    assert bench.stored_traffic("chunked prefill", "falcon1_bf16") is None
