@@ -32,7 +32,8 @@ _lock = threading.Lock()
 _lib = None
 
 PHI = {"identity": 0, "elu1": 1}
-MODE = {"falcon1": 0, "linattn": 1}
+MODE = {"falcon1": 0, "linattn": 1, "falcon1a": 2}
+FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -58,9 +59,9 @@ def _load():
             L = ctypes.c_long
             I = ctypes.c_int
             D = ctypes.c_double
-            lib.orc_falcon1.argtypes = [L, L, I, I, P, P, P, P, P, P, P, I, D, P, P, I]
-            lib.orc_linattn.argtypes = [L, L, I, I, P, P, P, P, I, P, P, I]
-            lib.orc_step.argtypes = [L, I, I, I, P, P, P, P, P, I, D, P, P, I]
+            lib.orc_falcon1.argtypes = [L, L, I, I, P, P, P, P, P, P, P, I, D, I, I, P, P, I]
+            lib.orc_linattn.argtypes = [L, L, I, I, P, P, P, P, I, I, P, P, I]
+            lib.orc_step.argtypes = [L, I, I, I, I, P, P, P, P, P, I, D, P, P, I]
             for f in (lib.orc_falcon1, lib.orc_linattn, lib.orc_step):
                 f.restype = None
             _lib = lib
@@ -84,10 +85,16 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
+def _flags(rbw, same_pair):
+    return (FLAG_RBW if rbw else 0) | (FLAG_SAME_PAIR if same_pair else 0)
+
+
 def falcon1(q, k, v, beta, lam, S0=None, k_init=None, phi="identity", eps=1e-6,
-            nthreads=None):
-    """Falcon-1 prefill.  q,k [..., T, dk]; v [..., T, dv]; beta, lam [..., T];
-    S0 [..., dk, dv] or None (zero state); k_init [..., dk] or None (x_1 = 0).
+            nthreads=None, inner=False, rbw=False, same_pair=False):
+    """Falcon-1 prefill (inner=True: the inner-product family, Falcon-1A).
+    q,k [..., T, dk]; v [..., T, dv]; beta, lam [..., T]; S0 [..., dk, dv] or
+    None (zero state); k_init [..., dk] or None (x_1 = 0).  rbw: read before
+    the write; same_pair: x_t = phi(k_t).
     Returns (o [..., T, dv], S_T [..., dk, dv]) as float64 numpy arrays."""
     q, k, v, beta, lam = map(_f64, (q, k, v, beta, lam))
     S0, k_init = _f64(S0), _f64(k_init)
@@ -100,13 +107,15 @@ def falcon1(q, k, v, beta, lam, S0=None, k_init=None, phi="identity", eps=1e-6,
     o = np.zeros(lead + (T, dv))
     S = np.zeros(lead + (dk, dv))
     _load().orc_falcon1(nc, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
-                        _ptr(S0), _ptr(k_init), PHI[phi], float(eps), _ptr(o), _ptr(S),
-                        nthreads or default_threads())
+                        _ptr(S0), _ptr(k_init), PHI[phi], float(eps),
+                        MODE["falcon1a" if inner else "falcon1"], _flags(rbw, same_pair),
+                        _ptr(o), _ptr(S), nthreads or default_threads())
     return o, S
 
 
-def linattn(q, k, v, S0=None, phi="elu1", nthreads=None):
-    """Plain causal linear attention.  Returns (o, S_T) as float64 arrays."""
+def linattn(q, k, v, S0=None, phi="elu1", nthreads=None, rbw=False):
+    """Plain causal linear attention (rbw: read before the write).
+    Returns (o, S_T) as float64 arrays."""
     q, k, v = map(_f64, (q, k, v))
     S0 = _f64(S0)
     lead = q.shape[:-2]
@@ -116,14 +125,15 @@ def linattn(q, k, v, S0=None, phi="elu1", nthreads=None):
     o = np.zeros(lead + (T, dv))
     S = np.zeros(lead + (dk, dv))
     _load().orc_linattn(nc, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(S0), PHI[phi],
-                        _ptr(o), _ptr(S), nthreads or default_threads())
+                        _flags(rbw, False), _ptr(o), _ptr(S), nthreads or default_threads())
     return o, S
 
 
 def step(q, k_prev, v, beta, lam, S, mode="falcon1", phi="identity", eps=1e-6,
-         nthreads=None):
-    """One decode step.  q,k_prev [..., dk]; v [..., dv]; beta, lam [...] (may be
-    None in linattn mode); S [..., dk, dv].  Returns (o, S_new) as new arrays."""
+         nthreads=None, rbw=False):
+    """One decode step (mode falcon1, falcon1a or linattn; rbw: o = S_old^T q).
+    q,k_prev [..., dk]; v [..., dv]; beta, lam [...] (may be None in linattn
+    mode); S [..., dk, dv].  Returns (o, S_new) as new arrays."""
     q, k_prev, v = map(_f64, (q, k_prev, v))
     beta, lam = _f64(beta), _f64(lam)
     S = _f64(S).copy()
@@ -132,7 +142,8 @@ def step(q, k_prev, v, beta, lam, S, mode="falcon1", phi="identity", eps=1e-6,
     dv = v.shape[-1]
     ns = int(np.prod(lead)) if lead else 1
     o = np.zeros(lead + (dv,))
-    _load().orc_step(ns, dk, dv, MODE[mode], _ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta),
+    _load().orc_step(ns, dk, dv, MODE[mode], _flags(rbw, False), _ptr(q), _ptr(k_prev),
+                     _ptr(v), _ptr(beta),
                      _ptr(lam), PHI[phi], float(eps), _ptr(S), _ptr(o),
                      nthreads or default_threads())
     return o, S

@@ -19,6 +19,12 @@
  *  - same page, §1.4 and §4.1: read after write (o_t = S_t^T q_t), the
  *    shifted training pair (x_t, y_t) = (phi(k_{t-1}), v_t), and the boundary
  *    x_1 := 0, eta_1 := 0 (the first token's write is a no-op).
+ *  - same page, §4.3: the inner-product family (Falcon-1A): the loss
+ *    -<S^T x_t, y_t> + (lambda/2)|S|^2 gives the additive write
+ *        S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t y_t^T
+ *    (no residual); the normalised step is kept as a write-size stabiliser.
+ *  - same page, §3.3 and §4.1: the 2 x 2 design read-after-write /
+ *    read-before-write x same-step pair / shifted pair.
  *  - "Attention is also an FFN" blog, §2.1 and §4.1: plain linear attention
  *    S_i = S_{i-1} + phi(k_i) v_i^T, y_i = phi(q_i)^T S_i, with the feature
  *    map phi(x) = elu(x) + 1, and the state kept in floating point.
@@ -32,6 +38,12 @@
  *    the key it is given (a caller starting a sequence passes beta = 0).
  *  - an optional k_init replaces the zero pair of the first token (so that a
  *    prefill can continue a previous one); then eta_1 follows the formula.
+ *  - Falcon-1A takes Falcon-1's eta_t, pairing and boundary; only the write
+ *    drops the residual (r_t := y_t).
+ *  - read-before-write (no formula printed): o_t = S_{t-1}^T q_t, the read
+ *    taken before token t's write.
+ *  - same-step pair (no formula printed): x_t = phi(k_t) for every t; the
+ *    first token then has a pair of its own (no boundary rule, k_init unused).
  *
  * Layouts (all contiguous, row-major, double):
  *   q, k   [nc][T][dk]     v, o   [nc][T][dv]     beta, lam [nc][T]
@@ -44,7 +56,8 @@
 #include <string.h>
 
 enum { ORC_PHI_IDENTITY = 0, ORC_PHI_ELU1 = 1 };
-enum { ORC_FALCON1 = 0, ORC_LINATTN = 1 };
+enum { ORC_FALCON1 = 0, ORC_LINATTN = 1, ORC_FALCON1A = 2 };
+enum { ORC_RBW = 1, ORC_SAME_PAIR = 2 };
 
 /* elu(z) + 1: z + 1 for z > 0, exp(z) for z <= 0 (blog §4.1). */
 static double orc_phi(int phi, double z)
@@ -53,20 +66,33 @@ static double orc_phi(int phi, double z)
     return z;
 }
 
-/* One Falcon-1 chain, token by token. */
+/* S^T q into out (a read of the state as it stands). */
+static void read_state(int dk, int dv, const double *S, const double *q, double *out)
+{
+    int i, j;
+    for (j = 0; j < dv; ++j) {
+        double c = 0.0;
+        for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * q[i];
+        out[j] = c;
+    }
+}
+
+/* One Falcon-1 (inner == 0) or Falcon-1A (inner == 1) chain, token by token. */
 static void falcon1_chain(long T, int dk, int dv, const double *q, const double *k,
                           const double *v, const double *beta, const double *lam,
                           const double *S0, const double *k_init, int phi, double eps,
-                          double *o, double *S, double *x, double *r)
+                          int inner, int flags, double *o, double *S, double *x, double *r)
 {
     long t;
     int i, j;
+    const int rbw = (flags & ORC_RBW) != 0, same = (flags & ORC_SAME_PAIR) != 0;
     if (S0) memcpy(S, S0, sizeof(double) * (size_t)dk * dv);
     else memset(S, 0, sizeof(double) * (size_t)dk * dv);
 
     for (t = 0; t < T; ++t) {
         double eta = 0.0, gamma, n = 0.0;
-        const double *kprev = (t > 0) ? k + (t - 1) * dk : k_init;
+        const double *kprev = same ? k + t * dk : (t > 0) ? k + (t - 1) * dk : k_init;
+        if (rbw) read_state(dk, dv, S, q + t * dk, o + t * dv);   /* read before write */
         if (kprev) {
             for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kprev[i]);
             for (i = 0; i < dk; ++i) n += x[i] * x[i];
@@ -75,63 +101,57 @@ static void falcon1_chain(long T, int dk, int dv, const double *q, const double 
             for (i = 0; i < dk; ++i) x[i] = 0.0; /* x_1 := 0, eta_1 := 0 */
         }
         gamma = 1.0 - eta * lam[t];
-        /* residual against the state before the write */
+        /* residual against the state before the write (Falcon-1A: the target) */
         for (j = 0; j < dv; ++j) {
             double a = 0.0;
-            for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
+            if (!inner)
+                for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
             r[j] = v[t * dv + j] - a;
         }
         /* the write */
         for (i = 0; i < dk; ++i)
             for (j = 0; j < dv; ++j)
                 S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
-        /* read after write */
-        for (j = 0; j < dv; ++j) {
-            double c = 0.0;
-            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * q[t * dk + i];
-            o[t * dv + j] = c;
-        }
+        if (!rbw) read_state(dk, dv, S, q + t * dk, o + t * dv);   /* read after write */
     }
 }
 
-/* One plain linear-attention chain: S += phi(k_t) v_t^T, o_t = S^T phi(q_t). */
+/* One plain linear-attention chain: S += phi(k_t) v_t^T, o_t = S^T phi(q_t)
+ * (read before the write with ORC_RBW). */
 static void linattn_chain(long T, int dk, int dv, const double *q, const double *k,
-                          const double *v, const double *S0, int phi,
+                          const double *v, const double *S0, int phi, int flags,
                           double *o, double *S, double *x, double *qt)
 {
     long t;
     int i, j;
+    const int rbw = (flags & ORC_RBW) != 0;
     if (S0) memcpy(S, S0, sizeof(double) * (size_t)dk * dv);
     else memset(S, 0, sizeof(double) * (size_t)dk * dv);
     for (t = 0; t < T; ++t) {
         for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, k[t * dk + i]);
         for (i = 0; i < dk; ++i) qt[i] = orc_phi(phi, q[t * dk + i]);
+        if (rbw) read_state(dk, dv, S, qt, o + t * dv);
         for (i = 0; i < dk; ++i)
             for (j = 0; j < dv; ++j)
                 S[(size_t)i * dv + j] += x[i] * v[t * dv + j];
-        for (j = 0; j < dv; ++j) {
-            double c = 0.0;
-            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * qt[i];
-            o[t * dv + j] = c;
-        }
+        if (!rbw) read_state(dk, dv, S, qt, o + t * dv);
     }
 }
 
-/* One decode step of one state (in place). */
-static void step_one(int mode, int dk, int dv, const double *q, const double *kp,
+/* One decode step of one state (in place); qt is scratch for phi(q). */
+static void step_one(int mode, int flags, int dk, int dv, const double *q, const double *kp,
                      const double *v, double beta, double lam, int phi, double eps,
-                     double *S, double *o, double *x, double *r)
+                     double *S, double *o, double *x, double *r, double *qt)
 {
     int i, j;
+    const int rbw = (flags & ORC_RBW) != 0;
     if (mode == ORC_LINATTN) {
         for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kp[i]);
+        for (i = 0; i < dk; ++i) qt[i] = orc_phi(phi, q[i]);
+        if (rbw) read_state(dk, dv, S, qt, o);
         for (i = 0; i < dk; ++i)
             for (j = 0; j < dv; ++j) S[(size_t)i * dv + j] += x[i] * v[j];
-        for (j = 0; j < dv; ++j) {
-            double c = 0.0;
-            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * orc_phi(phi, q[i]);
-            o[j] = c;
-        }
+        if (!rbw) read_state(dk, dv, S, qt, o);
         return;
     }
     {
@@ -140,28 +160,26 @@ static void step_one(int mode, int dk, int dv, const double *q, const double *kp
         for (i = 0; i < dk; ++i) n += x[i] * x[i];
         eta = beta / (n + lam + eps);
         gamma = 1.0 - eta * lam;
+        if (rbw) read_state(dk, dv, S, q, o);
         for (j = 0; j < dv; ++j) {
             double a = 0.0;
-            for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
+            if (mode != ORC_FALCON1A)
+                for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
             r[j] = v[j] - a;
         }
         for (i = 0; i < dk; ++i)
             for (j = 0; j < dv; ++j)
                 S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
-        for (j = 0; j < dv; ++j) {
-            double c = 0.0;
-            for (i = 0; i < dk; ++i) c += S[(size_t)i * dv + j] * q[i];
-            o[j] = c;
-        }
+        if (!rbw) read_state(dk, dv, S, q, o);
     }
 }
 
 /* ---- thread pool over independent chains ------------------------------- */
 
 typedef struct {
-    int kind; /* 0 prefill falcon1, 1 prefill linattn, 2 step */
+    int kind; /* 0 prefill falcon1 / falcon1a, 1 prefill linattn, 2 step */
     long nc, T;
-    int dk, dv, phi, mode;
+    int dk, dv, phi, mode, flags;
     double eps;
     const double *q, *k, *v, *beta, *lam, *S0, *k_init;
     double *o, *S;
@@ -186,16 +204,18 @@ static void *orc_worker(void *arg)
                           J->v + c * J->T * dv, J->beta + c * J->T, J->lam + c * J->T,
                           J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
                           J->k_init ? J->k_init + (size_t)c * dk : NULL, J->phi, J->eps,
-                          J->o + c * J->T * dv, J->S + (size_t)c * dk * dv, x, r);
+                          J->mode == ORC_FALCON1A, J->flags, J->o + c * J->T * dv,
+                          J->S + (size_t)c * dk * dv, x, r);
         } else if (J->kind == 1) {
             linattn_chain(J->T, dk, dv, J->q + c * J->T * dk, J->k + c * J->T * dk,
                           J->v + c * J->T * dv, J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
-                          J->phi, J->o + c * J->T * dv, J->S + (size_t)c * dk * dv, x, qt);
+                          J->phi, J->flags, J->o + c * J->T * dv, J->S + (size_t)c * dk * dv,
+                          x, qt);
         } else {
-            step_one(J->mode, dk, dv, J->q + (size_t)c * dk, J->k + (size_t)c * dk,
+            step_one(J->mode, J->flags, dk, dv, J->q + (size_t)c * dk, J->k + (size_t)c * dk,
                      J->v + (size_t)c * dv, J->beta ? J->beta[c] : 0.0,
                      J->lam ? J->lam[c] : 0.0, J->phi, J->eps,
-                     J->S + (size_t)c * dk * dv, J->o + (size_t)c * dv, x, r);
+                     J->S + (size_t)c * dk * dv, J->o + (size_t)c * dv, x, r, qt);
         }
     }
     free(x);
@@ -222,40 +242,44 @@ static void orc_run(orc_job *J, int nthreads)
 
 /* ---- exported entry points --------------------------------------------- */
 
-/* Falcon-1 prefill over nc independent chains.  S0, k_init may be NULL. */
+/* Falcon-1 (mode ORC_FALCON1) or Falcon-1A (ORC_FALCON1A) prefill over nc
+ * independent chains; flags: ORC_RBW, ORC_SAME_PAIR.  S0, k_init may be NULL. */
 void orc_falcon1(long nc, long T, int dk, int dv, const double *q, const double *k,
                  const double *v, const double *beta, const double *lam, const double *S0,
-                 const double *k_init, int phi, double eps, double *o, double *S_T,
-                 int nthreads)
+                 const double *k_init, int phi, double eps, int mode, int flags, double *o,
+                 double *S_T, int nthreads)
 {
     orc_job J;
     memset(&J, 0, sizeof(J));
     J.kind = 0; J.nc = nc; J.T = T; J.dk = dk; J.dv = dv; J.phi = phi; J.eps = eps;
+    J.mode = mode; J.flags = flags;
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.lam = lam; J.S0 = S0; J.k_init = k_init;
     J.o = o; J.S = S_T;
     orc_run(&J, nthreads);
 }
 
-/* Plain linear-attention prefill over nc chains.  S0 may be NULL. */
+/* Plain linear-attention prefill over nc chains (flags: ORC_RBW).  S0 may be NULL. */
 void orc_linattn(long nc, long T, int dk, int dv, const double *q, const double *k,
-                 const double *v, const double *S0, int phi, double *o, double *S_T,
-                 int nthreads)
+                 const double *v, const double *S0, int phi, int flags, double *o,
+                 double *S_T, int nthreads)
 {
     orc_job J;
     memset(&J, 0, sizeof(J));
-    J.kind = 1; J.nc = nc; J.T = T; J.dk = dk; J.dv = dv; J.phi = phi;
+    J.kind = 1; J.nc = nc; J.T = T; J.dk = dk; J.dv = dv; J.phi = phi; J.flags = flags;
     J.q = q; J.k = k; J.v = v; J.S0 = S0; J.o = o; J.S = S_T;
     orc_run(&J, nthreads);
 }
 
-/* One decode step for ns independent states; S is updated in place. */
-void orc_step(long ns, int dk, int dv, int mode, const double *q, const double *k_prev,
-              const double *v, const double *beta, const double *lam, int phi, double eps,
-              double *S, double *o, int nthreads)
+/* One decode step for ns independent states (flags: ORC_RBW); S is updated in
+ * place. */
+void orc_step(long ns, int dk, int dv, int mode, int flags, const double *q,
+              const double *k_prev, const double *v, const double *beta, const double *lam,
+              int phi, double eps, double *S, double *o, int nthreads)
 {
     orc_job J;
     memset(&J, 0, sizeof(J));
     J.kind = 2; J.nc = ns; J.T = 1; J.dk = dk; J.dv = dv; J.mode = mode; J.phi = phi;
+    J.flags = flags;
     J.eps = eps; J.q = q; J.k = k_prev; J.v = v; J.beta = beta; J.lam = lam;
     J.o = o; J.S = S;
     orc_run(&J, nthreads);
