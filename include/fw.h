@@ -14,7 +14,11 @@
  *
  * on the shifted training pair (x_t, y_t) = (phi(k_{t-1}), v_t) with the
  * boundary x_1 := 0, eta_1 := 0 (§4.1), and reads after the write,
- * o_t = S_t^T q_t (§1.4).  FW_LINATTN selects plain causal linear attention,
+ * o_t = S_t^T q_t (§1.4).  FW_FALCON1A is the same page's inner-product family
+ * (§4.3): the write drops the residual, S_t = (1 - eta_t lambda_t) S_{t-1}
+ * + eta_t x_t y_t^T, with Falcon-1's step, pairing and boundary.  Flags select
+ * the other arms of the page's read / pairing design (§3.3, §4.1): reading
+ * before the write and the same-step pair.  FW_LINATTN selects plain causal linear attention,
  * S_t = S_{t-1} + phi(k_t) v_t^T, o_t = S_t^T phi(q_t) ("Attention is also an
  * FFN" blog, §2.1 and §4.1), the special case without residual or decay.
  *
@@ -24,7 +28,7 @@
  *   - q, k, v, o:  [B][H][T][d] (prefill) or [B][H][d] (step), element type
  *     FW_F32 (float) or FW_BF16 (bfloat16), d innermost.
  *   - beta, lambda: float [B][H][T] (prefill) or [B][H] (step).  Ignored (may
- *     be NULL) in FW_LINATTN mode.
+ *     be NULL) in FW_LINATTN mode, required in FW_FALCON1 and FW_FALCON1A.
  *   - S0, S_T, S: float [B][H][d_k][d_v], S[i][j] = key row i, value column j,
  *     so a read is o_j = sum_i S[i][j] q_i (the blog's y = q @ S).
  *   - Pointers must be 16-byte aligned (vector and TMA loads).
@@ -45,13 +49,24 @@
 extern "C" {
 #endif
 
-#define FW_VERSION 100 /* 1.0.0 */
+#define FW_VERSION 110 /* 1.1.0 */
 
 typedef enum { FW_F32 = 0, FW_BF16 = 1 } fw_dtype;
 
 /* FW_FALCON1: shifted pair, residual write, normalised step and decay.
- * FW_LINATTN: same-step pair, additive write S += phi(k) v^T, no eta/gamma. */
-typedef enum { FW_FALCON1 = 0, FW_LINATTN = 1 } fw_mode;
+ * FW_LINATTN: same-step pair, additive write S += phi(k) v^T, no eta/gamma.
+ * FW_FALCON1A: Falcon-1's pair, step and decay with the additive write
+ *              S = gamma S + eta x v^T (no residual). */
+typedef enum { FW_FALCON1 = 0, FW_LINATTN = 1, FW_FALCON1A = 2 } fw_mode;
+
+/* Flags (bitwise OR) of fw_prefill_ex and fw_step_ex.
+ * FW_FLAG_RBW: read before the write, o_t = S_{t-1}^T q_t (every mode).
+ * FW_FLAG_SAME_PAIR: FW_FALCON1 / FW_FALCON1A pair (phi(k_t), v_t) for every
+ *   token, so the first token writes too and k_init is not used (prefill
+ *   only; FW_LINATTN always pairs this way, and a step pairs whatever key it
+ *   is given).  The pages name these arms without printing formulas; the
+ *   readings above are the plainest ones. */
+typedef enum { FW_FLAG_RBW = 1, FW_FLAG_SAME_PAIR = 2 } fw_flag;
 
 /* Feature map phi.  FW_FALCON1 applies it to the key only (the read uses q as
  * given); FW_LINATTN applies it to both q and k, never to v.
@@ -94,15 +109,15 @@ enum {
  * triangular solve, short inter-chunk recurrence, parallel outputs).
  *
  *   q, k, v  in   [B][H][T][d] of `dtype`
- *   beta     in   float [B][H][T]   (FW_FALCON1; beta_t in [0, 2) keeps the
- *                                     write stable, other values are computed
- *                                     literally)
- *   lambda   in   float [B][H][T]   (FW_FALCON1; >= 0)
+ *   beta     in   float [B][H][T]   (FW_FALCON1, FW_FALCON1A; beta_t in
+ *                                     [0, 2) keeps the Falcon-1 write stable,
+ *                                     other values are computed literally)
+ *   lambda   in   float [B][H][T]   (FW_FALCON1, FW_FALCON1A; >= 0)
  *   S0       in   float [B][H][d][d] or NULL for a zero start state
  *   o        out  [B][H][T][d] of `dtype` (rounded to nearest even for bf16);
  *                 must not overlap any input
  *   S_T      out  float [B][H][d][d], the state after token T; may equal S0
- *   eps      in   >= 0, added to the step's denominator (FW_FALCON1)
+ *   eps      in   >= 0, added to the step's denominator (FW_FALCON1, FW_FALCON1A)
  * Returns FW_OK or a negative FW_ERR_* code.
  */
 int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
@@ -111,19 +126,22 @@ int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
                cudaStream_t stream);
 
 /*
- * fw_prefill_ex -- fw_prefill with two more arguments.
- *   k_init  in  [B][H][d] of `dtype` or NULL.  FW_FALCON1 only: the key that
- *               precedes this call's first token (the last key of a previous
- *               prefill of the same sequence).  Given, the first token's pair
- *               is (phi(k_init), v_1) with the normal step; NULL keeps the
- *               boundary x_1 = 0, eta_1 = 0.  Ignored in FW_LINATTN mode.
+ * fw_prefill_ex -- fw_prefill with three more arguments.
+ *   k_init  in  [B][H][d] of `dtype` or NULL.  FW_FALCON1 / FW_FALCON1A with
+ *               the shifted pair: the key that precedes this call's first
+ *               token (the last key of a previous prefill of the same
+ *               sequence).  Given, the first token's pair is (phi(k_init), v_1)
+ *               with the normal step; NULL keeps the boundary x_1 = 0,
+ *               eta_1 = 0.  Ignored in FW_LINATTN mode and with
+ *               FW_FLAG_SAME_PAIR.
+ *   flags   in  0 or FW_FLAG_* bits (FW_ERR_MODE for unknown bits).
  *   algo    in  FW_ALGO_AUTO, or force one kernel (FW_ERR_UNSUPPORTED if the
  *               chunked kernel cannot take the call).
  */
 int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
                   const float *lambda, const float *S0, const void *k_init, void *o,
                   float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
-                  fw_phi phi, float eps, fw_algo algo, cudaStream_t stream);
+                  fw_phi phi, float eps, unsigned flags, fw_algo algo, cudaStream_t stream);
 
 /*
  * fw_step -- one decode step for B*H independent states, S updated in place.
@@ -135,7 +153,7 @@ int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta
  * sequence with steps pass beta = 0 (an empty first write).
  *
  *   q, k_prev, v  in      [B][H][d] of `dtype`
- *   beta, lambda  in      float [B][H] (FW_FALCON1)
+ *   beta, lambda  in      float [B][H] (FW_FALCON1, FW_FALCON1A)
  *   S             in/out  float [B][H][d][d]
  *   o             out     [B][H][d] of `dtype`, o = S_new^T q
  *   shape         T must be 1
@@ -143,6 +161,15 @@ int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta
 int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
             const float *lambda, float *S, void *o, const fw_shape *shape, fw_dtype dtype,
             fw_mode mode, fw_phi phi, float eps, cudaStream_t stream);
+
+/*
+ * fw_step_ex -- fw_step with flags: FW_FLAG_RBW reads before the write,
+ * o = S_old^T q (FW_FLAG_SAME_PAIR has no effect on a step: the pair is
+ * whatever key is passed as `k_prev`).  Unknown bits give FW_ERR_MODE.
+ */
+int fw_step_ex(const void *q, const void *k_prev, const void *v, const float *beta,
+               const float *lambda, float *S, void *o, const fw_shape *shape, fw_dtype dtype,
+               fw_mode mode, fw_phi phi, float eps, unsigned flags, cudaStream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error word.
  * Returns FW_OK, FW_ERR_TIMEOUT, or FW_ERR_CUDA. */

@@ -65,7 +65,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps) {
+// Modes with the normalised step and decay (beta, lambda, eps used).
+bool gated(fw_mode m) { return m == FW_FALCON1 || m == FW_FALCON1A; }
+
+int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+                 unsigned flags) {
     if (!shape) return FW_ERR_NULL;
     if (shape->B < 1 || shape->H < 1 || shape->T < 1) return FW_ERR_SHAPE;
     if (shape->d_k != 64 && shape->d_k != 128) return FW_ERR_SHAPE;
@@ -73,9 +77,10 @@ int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi
     if (shape->B > (int64_t)1 << 31 || shape->H > (int64_t)1 << 31) return FW_ERR_SHAPE;
     if (shape->B * shape->H > (int64_t)INT32_MAX) return FW_ERR_SHAPE;
     if (dtype != FW_F32 && dtype != FW_BF16) return FW_ERR_DTYPE;
-    if (mode != FW_FALCON1 && mode != FW_LINATTN) return FW_ERR_MODE;
+    if (mode != FW_FALCON1 && mode != FW_LINATTN && mode != FW_FALCON1A) return FW_ERR_MODE;
     if (phi != FW_PHI_IDENTITY && phi != FW_PHI_ELU1) return FW_ERR_MODE;
-    if (mode == FW_FALCON1 && !(std::isfinite(eps) && eps >= 0.f)) return FW_ERR_ARG;
+    if (flags & ~(unsigned)(FW_FLAG_RBW | FW_FLAG_SAME_PAIR)) return FW_ERR_MODE;
+    if (gated(mode) && !(std::isfinite(eps) && eps >= 0.f)) return FW_ERR_ARG;
     return FW_OK;
 }
 
@@ -87,16 +92,17 @@ using namespace fw;
 extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
                              const float *lambda, const float *S0, const void *k_init, void *o,
                              float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
-                             fw_phi phi, float eps, fw_algo algo, cudaStream_t stream) {
-    int st = check_common(shape, dtype, mode, phi, eps);
+                             fw_phi phi, float eps, unsigned flags, fw_algo algo,
+                             cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps, flags);
     if (st != FW_OK) return st;
     if (algo != FW_ALGO_AUTO && algo != FW_ALGO_RECURRENT && algo != FW_ALGO_CHUNKED)
         return FW_ERR_MODE;
     if (!q || !k || !v || !o || !S_T) return FW_ERR_NULL;
-    if (mode == FW_FALCON1 && (!beta || !lambda)) return FW_ERR_NULL;
+    if (gated(mode) && (!beta || !lambda)) return FW_ERR_NULL;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(S_T) ||
-        misaligned(S0) || misaligned(k_init) || (mode == FW_FALCON1 && (misaligned(beta) ||
-                                                                          misaligned(lambda))))
+        misaligned(S0) || misaligned(k_init) || (gated(mode) && (misaligned(beta) ||
+                                                                   misaligned(lambda))))
         return FW_ERR_ALIGN;
 
     const int64_t nc = shape->B * shape->H;
@@ -108,8 +114,8 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     if (overlaps(o, nx, q, nx) || overlaps(o, nx, k, nx) || overlaps(o, nx, v, nx) ||
         overlaps(o, nx, S0, S0 ? ns : 0) || overlaps(o, nx, S_T, ns))
         return FW_ERR_ARG;
-    if (mode == FW_FALCON1 && (overlaps(o, nx, beta, nbl) || overlaps(o, nx, lambda, nbl) ||
-                               overlaps(S_T, ns, beta, nbl) || overlaps(S_T, ns, lambda, nbl)))
+    if (gated(mode) && (overlaps(o, nx, beta, nbl) || overlaps(o, nx, lambda, nbl) ||
+                        overlaps(S_T, ns, beta, nbl) || overlaps(S_T, ns, lambda, nbl)))
         return FW_ERR_ARG;
     if (overlaps(S_T, ns, q, nx) || overlaps(S_T, ns, k, nx) || overlaps(S_T, ns, v, nx))
         return FW_ERR_ARG;
@@ -117,9 +123,12 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
 
     PrefillArgs a;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.S0 = S0;
-    a.k_init = (mode == FW_FALCON1) ? k_init : nullptr;
+    // LINATTN pairs each key with its own value; so do the gated modes with
+    // FW_FLAG_SAME_PAIR (then the bit stays set and k_init is unused)
+    if (mode == FW_LINATTN) flags &= ~(unsigned)FW_FLAG_SAME_PAIR;
+    a.k_init = (gated(mode) && !(flags & FW_FLAG_SAME_PAIR)) ? k_init : nullptr;
     a.o = o; a.S_T = S_T; a.n_chains = nc; a.T = shape->T; a.d = d;
-    a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps;
+    a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps; a.flags = flags;
     a.wait_ns = g_wait_us.load() * 1000LL;
     a.force_timeout = g_force_timeout.load();
 
@@ -141,20 +150,20 @@ extern "C" int fw_prefill(const void *q, const void *k, const void *v, const flo
                           const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi,
                           float eps, cudaStream_t stream) {
     return fw_prefill_ex(q, k, v, beta, lambda, S0, nullptr, o, S_T, shape, dtype, mode, phi,
-                         eps, FW_ALGO_AUTO, stream);
+                         eps, 0u, FW_ALGO_AUTO, stream);
 }
 
-extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
-                       const float *lambda, float *S, void *o, const fw_shape *shape,
-                       fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
-                       cudaStream_t stream) {
-    int st = check_common(shape, dtype, mode, phi, eps);
+extern "C" int fw_step_ex(const void *q, const void *k_prev, const void *v, const float *beta,
+                          const float *lambda, float *S, void *o, const fw_shape *shape,
+                          fw_dtype dtype, fw_mode mode, fw_phi phi, float eps, unsigned flags,
+                          cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps, flags);
     if (st != FW_OK) return st;
     if (shape->T != 1) return FW_ERR_SHAPE;
     if (!q || !k_prev || !v || !S || !o) return FW_ERR_NULL;
-    if (mode == FW_FALCON1 && (!beta || !lambda)) return FW_ERR_NULL;
+    if (gated(mode) && (!beta || !lambda)) return FW_ERR_NULL;
     if (misaligned(q) || misaligned(k_prev) || misaligned(v) || misaligned(S) || misaligned(o) ||
-        (mode == FW_FALCON1 && (misaligned(beta) || misaligned(lambda))))
+        (gated(mode) && (misaligned(beta) || misaligned(lambda))))
         return FW_ERR_ALIGN;
     const int64_t ns = shape->B * shape->H;
     const int d = shape->d_k;
@@ -165,8 +174,8 @@ extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const f
         overlaps(o, nx, S, nst) || overlaps(S, nst, q, nx) || overlaps(S, nst, k_prev, nx) ||
         overlaps(S, nst, v, nx))
         return FW_ERR_ARG;
-    if (mode == FW_FALCON1 && (overlaps(S, nst, beta, ns * 4) || overlaps(S, nst, lambda, ns * 4) ||
-                               overlaps(o, nx, beta, ns * 4) || overlaps(o, nx, lambda, ns * 4)))
+    if (gated(mode) && (overlaps(S, nst, beta, ns * 4) || overlaps(S, nst, lambda, ns * 4) ||
+                        overlaps(o, nx, beta, ns * 4) || overlaps(o, nx, lambda, ns * 4)))
         return FW_ERR_ARG;
 
     int *err = nullptr;
@@ -176,9 +185,17 @@ extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const f
     StepArgs a;
     a.q = q; a.k = k_prev; a.v = v; a.beta = beta; a.lam = lambda; a.S = S; a.o = o;
     a.n_states = ns; a.d = d; a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps;
+    a.flags = flags & (unsigned)FW_FLAG_RBW;
     cudaError_t e = launch_decode(a, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return FW_OK;
+}
+
+extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
+                       const float *lambda, float *S, void *o, const fw_shape *shape,
+                       fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+                       cudaStream_t stream) {
+    return fw_step_ex(q, k_prev, v, beta, lambda, S, o, shape, dtype, mode, phi, eps, 0u, stream);
 }
 
 extern "C" int fw_check(cudaStream_t stream) {

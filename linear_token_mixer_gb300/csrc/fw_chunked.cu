@@ -688,12 +688,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         const int top = lrow ? t - 1 : t;        // last active column
                         float dz = 1.f;
                         if (h == 0 && top >= 32) dz = vg[V_Q32 / 4 + top];
-    #pragma unroll
+#pragma unroll
                         for (int q = 7; q >= 0; --q) {
                             const float4 e4 = eta4[q], y4 = gam4[q];
                             const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
                             const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
-    #pragma unroll
+#pragma unroll
                             for (int e = 3; e >= 0; --e) {
                                 const int s2 = 4 * q + e;              // local column
                                 const bool act = (32 * h + s2) <= top;
@@ -702,13 +702,13 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                             }
                         }
                         if (lrow) {
-    #pragma unroll
+#pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 *reinterpret_cast<float4 *>(Lw + t * 64 + (((8 * h + q) ^ (t & 15)) << 2)) =
                                     make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
                         } else {
                             const uint32_t pb = sb + ((cc & 1) ? OFF_PB1 : OFF_PB0);
-    #pragma unroll
+#pragma unroll
                             for (int c16 = 0; c16 < 4; ++c16)
                                 st_row8_bf16(pb + sw128(t, 4 * h + c16), g + 8 * c16);
                         }
@@ -1109,6 +1109,9 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t b
 // operand accuracy.
 bool chunked_supported(const PrefillArgs &a) {
     if (a.mode == FW_FALCON1 && a.phi == FW_PHI_ELU1) return false;
+    // Falcon-1A and the read-before-write / same-step-pair arms run on the
+    // per-token kernel
+    if (a.mode == FW_FALCON1A || a.flags != 0) return false;
     return a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
            a.n_chains <= (int64_t)INT32_MAX;
 }

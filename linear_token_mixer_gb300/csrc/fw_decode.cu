@@ -11,8 +11,10 @@
 //     S[i][j] <- gamma S[i][j] + eta x_i r_j,
 // the Falcon-1 write and read-after-write of "Fast Weight Attention for
 // Continual Learning" paper reading §3.2/§1.4 with the pair (phi(k_prev), v).
-// Linear-attention mode: x = phi(k), r = v, eta = gamma = 1, read with
-// phi(q) ("Attention is also an FFN" blog §4.1, forward_step).
+// Falcon-1A (§4.3) drops the residual (r = v); FW_FLAG_RBW reads before the
+// write, o_j = c_j.  Linear-attention mode: x = phi(k), r = v,
+// eta = gamma = 1, read with phi(q) ("Attention is also an FFN" blog §4.1,
+// forward_step).
 //
 // Traffic per state: d*d*4 bytes read + the same written, plus 3 d-vectors.
 // The state is read and written with streaming (evict-first) hints since a
@@ -34,7 +36,9 @@ decode_kernel(StepArgs a) {
     const int cq = tid % TPR;
     const int rg = tid / TPR;
     const int64_t s = blockIdx.x;
-    const bool falcon = (a.mode == FW_FALCON1);
+    const bool falcon = (a.mode != FW_LINATTN);   // eta, gamma
+    const bool resid = (a.mode == FW_FALCON1);     // r = v - S^T x
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
     float4 *Sp = reinterpret_cast<float4 *>(a.S + s * D * D);
     float4 Sr[NP];
@@ -98,14 +102,16 @@ decode_kernel(StepArgs a) {
     }
     const float4 vv = *reinterpret_cast<const float4 *>(&vs[cq * 4]);
     float4 r;
-    if (falcon) { r.x = vv.x - A.x; r.y = vv.y - A.y; r.z = vv.z - A.z; r.w = vv.w - A.w; }
+    if (resid) { r.x = vv.x - A.x; r.y = vv.y - A.y; r.z = vv.z - A.z; r.w = vv.w - A.w; }
     else r = vv;
 
     if (rg == 0) {
         const float ex = eta * xq;
-        float4 ov;
-        ov.x = fmaf(gam, C.x, ex * r.x); ov.y = fmaf(gam, C.y, ex * r.y);
-        ov.z = fmaf(gam, C.z, ex * r.z); ov.w = fmaf(gam, C.w, ex * r.w);
+        float4 ov = C;   // read before the write
+        if (!rbw) {
+            ov.x = fmaf(gam, C.x, ex * r.x); ov.y = fmaf(gam, C.y, ex * r.y);
+            ov.z = fmaf(gam, C.z, ex * r.z); ov.w = fmaf(gam, C.w, ex * r.w);
+        }
         TIn *og = static_cast<TIn *>(a.o) + s * D + cq * 4;
         og[0] = from_f32<TIn>(ov.x); og[1] = from_f32<TIn>(ov.y);
         og[2] = from_f32<TIn>(ov.z); og[3] = from_f32<TIn>(ov.w);

@@ -26,6 +26,7 @@ struct PrefillArgs {
     fw_mode mode;
     fw_phi phi;
     float eps;
+    unsigned flags;    // FW_FLAG_* bits
     int *err;          // device error word
     long long wait_ns; // limit of every bounded device wait, nanoseconds
     int force_timeout; // testing hook: wait on a barrier nothing arrives on
@@ -42,6 +43,7 @@ struct StepArgs {
     fw_mode mode;
     fw_phi phi;
     float eps;
+    unsigned flags;    // FW_FLAG_* bits
 };
 
 // Launchers (return a cudaError_t from the launch).

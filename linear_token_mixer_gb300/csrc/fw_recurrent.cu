@@ -11,9 +11,12 @@
 //     S[i][j] <- gamma S[i][j] + eta x_i r_j,
 // i.e. the Falcon-1 write of "Fast Weight Attention for Continual Learning"
 // paper reading §3.2/§4.2 on the pair (phi(k_{t-1}), v_t) with x_1 = 0,
-// eta_1 = 0 (§4.1) and the read after the write (§1.4).  Linear-attention
-// mode uses x = phi(k_t), r = v_t, gamma = eta = 1 and reads with phi(q_t)
-// ("Attention is also an FFN" blog §2.1).
+// eta_1 = 0 (§4.1) and the read after the write (§1.4).  Falcon-1A (§4.3)
+// drops the residual (r = y); with FW_FLAG_SAME_PAIR the pair is
+// (phi(k_t), v_t) for every token, and with FW_FLAG_RBW the read is taken
+// before the write, o_j = c_j (the §3.3 read / pairing arms).
+// Linear-attention mode uses x = phi(k_t), r = v_t, gamma = eta = 1 and reads
+// with phi(q_t) ("Attention is also an FFN" blog §2.1).
 //
 // This kernel serves every shape and dtype (it is the fp32 path and the
 // fallback of the chunked tensor-core kernel); the state never leaves
@@ -36,7 +39,10 @@ recurrent_kernel(PrefillArgs a) {
     const int64_t chain = blockIdx.x;
     const int col0 = (blockIdx.y * kNWarp + warp) * kJW;
     const int64_t T = a.T;
-    const bool falcon = (a.mode == FW_FALCON1);
+    const bool falcon = (a.mode != FW_LINATTN);                     // eta, gamma, beta, lambda
+    const bool resid = (a.mode == FW_FALCON1);                      // r = y - S^T x
+    const bool shifted = falcon && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
     const TIn *q = static_cast<const TIn *>(a.q) + chain * T * DK;
     const TIn *k = static_cast<const TIn *>(a.k) + chain * T * DK;
@@ -57,7 +63,7 @@ recurrent_kernel(PrefillArgs a) {
     // if a previous key is given, else 0 with eta_1 = 0.
     float xprev[RK];
     bool have_prev = false;
-    if (falcon && a.k_init) {
+    if (shifted && a.k_init) {
         const TIn *ki = static_cast<const TIn *>(a.k_init) + chain * DK;
 #pragma unroll
         for (int r = 0; r < RK; ++r) xprev[r] = apply_phi(a.phi, to_f32(ki[lane + 32 * r]));
@@ -93,7 +99,7 @@ recurrent_kernel(PrefillArgs a) {
         float xs[RK];
 #pragma unroll
         for (int r = 0; r < RK; ++r) {
-            xs[r] = falcon ? xprev[r] : kt[r];
+            xs[r] = shifted ? xprev[r] : kt[r];
             if (!falcon) qv[r] = apply_phi(a.phi, qv[r]);
         }
 
@@ -120,7 +126,7 @@ recurrent_kernel(PrefillArgs a) {
 
         float eta = 1.f, gam = 1.f;
         if (falcon) {
-            const bool pair = (t > 0) || have_prev;
+            const bool pair = !shifted || (t > 0) || have_prev;
             eta = pair ? bt / (red[2 * kJW] + lt + a.eps) : 0.f;
             gam = 1.f - eta * lt;
         }
@@ -128,14 +134,14 @@ recurrent_kernel(PrefillArgs a) {
         float outv = 0.f;
 #pragma unroll
         for (int c = 0; c < kJW; ++c) {
-            const float rc = falcon ? vv[c] - red[2 * c] : vv[c];
-            const float oc = fmaf(gam, red[2 * c + 1], eta * rc * xq);
+            const float rc = resid ? vv[c] - red[2 * c] : vv[c];
+            const float oc = rbw ? red[2 * c + 1] : fmaf(gam, red[2 * c + 1], eta * rc * xq);
             if (lane == c) outv = oc;
 #pragma unroll
             for (int r = 0; r < RK; ++r) S[r][c] = fmaf(gam, S[r][c], (eta * xs[r]) * rc);
         }
         if (lane < kJW) o[t * DK + col0 + lane] = from_f32<TIn>(outv);
-        if (falcon) {
+        if (shifted) {
 #pragma unroll
             for (int r = 0; r < RK; ++r) xprev[r] = kt[r];
         }

@@ -15,7 +15,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfw.so")
 
 FW_F32, FW_BF16 = 0, 1
-MODES = {"falcon1": 0, "linattn": 1}
+MODES = {"falcon1": 0, "linattn": 1, "falcon1a": 2}
+FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 PHIS = {"identity": 0, "elu1": 1}
 ALGOS = {"auto": 0, "recurrent": 1, "chunked": 2}
 DTYPES = {torch.float32: FW_F32, torch.bfloat16: FW_BF16}
@@ -40,8 +41,9 @@ class fw_shape(ctypes.Structure):
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
 
 
-EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_check", "fw_status_string",
-           "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us", "fw_debug_force_timeout")
+EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_step_ex", "fw_check",
+           "fw_status_string", "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us",
+           "fw_debug_force_timeout")
 
 _lib = None
 
@@ -57,8 +59,10 @@ def lib():
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         SP = ctypes.POINTER(fw_shape)
         L.fw_prefill.argtypes = [P, P, P, P, P, P, P, P, SP, I, I, I, F, P]
-        L.fw_prefill_ex.argtypes = [P, P, P, P, P, P, P, P, P, SP, I, I, I, F, I, P]
+        U = ctypes.c_uint
+        L.fw_prefill_ex.argtypes = [P, P, P, P, P, P, P, P, P, SP, I, I, I, F, U, I, P]
         L.fw_step.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, P]
+        L.fw_step_ex.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, U, P]
         L.fw_check.argtypes = [P]
         L.fw_status_string.argtypes = [I]
         L.fw_status_string.restype = ctypes.c_char_p
@@ -68,8 +72,8 @@ def lib():
         L.fw_set_wait_limit_us.restype = None
         L.fw_debug_force_timeout.argtypes = [I]
         L.fw_debug_force_timeout.restype = None
-        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_check, L.fw_version,
-                  L.fw_last_cuda_error):
+        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_step_ex, L.fw_check,
+                  L.fw_version, L.fw_last_cuda_error):
             f.restype = I
         _lib = L
     return _lib
@@ -90,12 +94,19 @@ def _stream(stream):
     return s.cuda_stream
 
 
+def _flags(rbw, same_pair):
+    return (FLAG_RBW if rbw else 0) | (FLAG_SAME_PAIR if same_pair else 0)
+
+
 def prefill(q, k, v, beta=None, lam=None, S0=None, *, mode="falcon1", phi="identity",
-            eps=1e-6, k_init=None, algo="auto", o=None, S_T=None, stream=None):
+            eps=1e-6, k_init=None, algo="auto", o=None, S_T=None, stream=None, rbw=False,
+            same_pair=False):
     """Run the recurrence over q, k, v [B, H, T, d] (fp32 or bf16).
 
-    Returns (o [B,H,T,d] in q's dtype, S_T [B,H,d,d] fp32).  beta, lam
-    [B,H,T] fp32 are required in falcon1 mode.  S0 [B,H,d,d] fp32 or None."""
+    mode: "falcon1", "falcon1a" or "linattn"; rbw reads before the write,
+    same_pair pairs each key with its own value.  Returns (o [B,H,T,d] in q's
+    dtype, S_T [B,H,d,d] fp32).  beta, lam [B,H,T] fp32 are required in the
+    falcon modes.  S0 [B,H,d,d] fp32 or None."""
     B, H, T, d = q.shape
     if o is None:
         o = torch.empty_like(q)
@@ -105,23 +116,23 @@ def prefill(q, k, v, beta=None, lam=None, S0=None, *, mode="falcon1", phi="ident
     st = lib().fw_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
                              _ptr(k_init), _ptr(o), _ptr(S_T), ctypes.byref(shp),
                              DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi], float(eps),
-                             ALGOS[algo], _stream(stream))
+                             _flags(rbw, same_pair), ALGOS[algo], _stream(stream))
     if st != FW_OK:
         raise FwError(st, "fw_prefill")
     return o, S_T
 
 
 def step(q, k_prev, v, beta, lam, S, *, mode="falcon1", phi="identity", eps=1e-6, o=None,
-         stream=None):
+         stream=None, rbw=False):
     """One decode step for q, k_prev, v [B, H, d]; S [B, H, d, d] fp32 is
-    updated in place.  Returns o [B, H, d] in q's dtype."""
+    updated in place (rbw: o = S_old^T q).  Returns o [B, H, d] in q's dtype."""
     B, H, d = q.shape
     if o is None:
         o = torch.empty_like(q)
     shp = fw_shape(B, H, 1, d, v.shape[-1])
-    st = lib().fw_step(_ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S), _ptr(o),
-                       ctypes.byref(shp), DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi],
-                       float(eps), _stream(stream))
+    st = lib().fw_step_ex(_ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S),
+                          _ptr(o), ctypes.byref(shp), DTYPES.get(q.dtype, -1), MODES[mode],
+                          PHIS[phi], float(eps), _flags(rbw, False), _stream(stream))
     if st != FW_OK:
         raise FwError(st, "fw_step")
     return o

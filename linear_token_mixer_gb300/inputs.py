@@ -71,6 +71,10 @@ WORKLOADS = {
     "falcon1_long": Workload("falcon1_long", "falcon1", "identity", torch.bfloat16,
                              1, 32, 32768, 128, 1.0, "lognormal", (1.5, 1.99), (0.0, 0.01),
                              0.0, seed=20261206),
+    # the inner-product family on the Falcon-1 bf16 shapes and distributions
+    "falcon1a_bf16": Workload("falcon1a_bf16", "falcon1a", "identity", torch.bfloat16,
+                              8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
+                              seed=20261208),
 }
 
 DECODE = dict(batch=256, H=32, d=128, steps=1024, beta=(0.1, 1.0), lam=(0.0, 0.05),
@@ -110,7 +114,7 @@ def prefill_inputs(w: Workload, device="cpu", seed=None):
     v = (torch.randn(shp, generator=g, device=device, dtype=torch.float32) * w.qkv_scale)
     out = dict(q=q.to(w.dtype), k=k.to(w.dtype), v=v.to(w.dtype), beta=None, lam=None,
                S0=None)
-    if w.mode == "falcon1":
+    if w.mode in ("falcon1", "falcon1a"):
         out["beta"] = _uniform((w.B, w.H, w.T), *w.beta, g, device)
         out["lam"] = _uniform((w.B, w.H, w.T), *w.lam, g, device)
     if w.s0_std > 0:

@@ -21,13 +21,14 @@ def to64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def oracle_prefill(w_mode, phi, eps, x, k_init=None):
+def oracle_prefill(w_mode, phi, eps, x, k_init=None, rbw=False, same_pair=False):
     """Run the oracle on CPU copies of the input dict x (tensors on any device)."""
     c = {k: (t.cpu() if t is not None else None) for k, t in x.items()}
-    if w_mode == "falcon1":
+    if w_mode in ("falcon1", "falcon1a"):
         return oracle.falcon1(c["q"], c["k"], c["v"], c["beta"], c["lam"], S0=c["S0"],
-                              k_init=None if k_init is None else k_init.cpu(), phi=phi, eps=eps)
-    return oracle.linattn(c["q"], c["k"], c["v"], S0=c["S0"], phi=phi)
+                              k_init=None if k_init is None else k_init.cpu(), phi=phi, eps=eps,
+                              inner=(w_mode == "falcon1a"), rbw=rbw, same_pair=same_pair)
+    return oracle.linattn(c["q"], c["k"], c["v"], S0=c["S0"], phi=phi, rbw=rbw)
 
 
 def select_chains(x, idx):

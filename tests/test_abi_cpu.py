@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.fw_version() == 100
+    assert L.fw_version() == 110
     for code, name in fw.STATUS.items():
         assert L.fw_status_string(code).decode().startswith(name)
     assert L.fw_status_string(12345) == b"unknown status"
@@ -55,11 +55,11 @@ P = [A + 0x100000 * i for i in range(12)]
 
 def call_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init=None, o=P[5],
                  S_T=P[6], shape=(1, 1, 8, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6,
-                 algo=0):
+                 flags=0, algo=0):
     shp = fw.fw_shape(*shape) if shape is not None else None
     return L.fw_prefill_ex(q, k, v, beta, lam, S0, k_init, o, S_T,
                            ctypes.byref(shp) if shp is not None else None,
-                           dtype, mode, phi, eps, algo, None)
+                           dtype, mode, phi, eps, flags, algo, None)
 
 
 @no_gpu
@@ -70,6 +70,9 @@ def call_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init
     (dict(shape=(1, 1, 0, 64, 64)), -2), (dict(shape=(1, 1, 8, 96, 96)), -2),
     (dict(shape=(1, 1, 8, 64, 128)), -2), (dict(shape=(1, 1, 8, 32, 32)), -2),
     (dict(dtype=7), -3), (dict(mode=3), -5), (dict(phi=9), -5), (dict(algo=5), -5),
+    (dict(flags=4), -5), (dict(flags=0x80000000), -5),
+    (dict(mode=2, beta=None), -1), (dict(mode=2, lam=None), -1), (dict(mode=2, eps=-1.0), -9),
+    (dict(mode=2, beta=P[3] + 4), -4),
     (dict(q=P[0] + 8), -4), (dict(o=P[5] + 2), -4), (dict(S0=P[7] + 4), -4),
     (dict(k_init=P[8] + 2), -4), (dict(beta=P[3] + 4), -4),
     (dict(eps=-1.0), -9), (dict(eps=float("nan")), -9), (dict(o=P[0]), -9),
@@ -94,22 +97,32 @@ def test_chunked_unsupported_shapes(L):
     assert call_prefill(L, dtype=1, shape=(1, 1, 8, 64, 64), algo=2) == -8
     # Falcon-1 with phi = elu+1 stays on the per-token kernel.
     assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), phi=1, algo=2) == -8
+    # so do Falcon-1A and the read-before-write / same-step-pair arms
+    assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=2, algo=2) == -8
+    assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), flags=1, algo=2) == -8
+    assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), flags=2, algo=2) == -8
 
 
 @no_gpu
 @pytest.mark.parametrize("kw,code", [
     (dict(shape=(1, 1, 2, 64, 64)), -2), (dict(q=None), -1), (dict(S=None), -1),
     (dict(beta=None), -1), (dict(S=P[6] + 4), -4), (dict(o=P[0]), -9), (dict(dtype=5), -3),
+    (dict(mode=2, lam=None), -1), (dict(flags=8), -5), (dict(mode=7), -5),
 ])
 def test_step_validation(L, kw, code):
     args = dict(q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S=P[6], o=P[5],
-                shape=(2, 2, 1, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6)
+                shape=(2, 2, 1, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6, flags=0)
     args.update(kw)
     shp = fw.fw_shape(*args["shape"])
-    st = L.fw_step(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S"],
-                   args["o"], ctypes.byref(shp), args["dtype"], args["mode"], args["phi"],
-                   args["eps"], None)
+    st = L.fw_step_ex(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S"],
+                      args["o"], ctypes.byref(shp), args["dtype"], args["mode"], args["phi"],
+                      args["eps"], args["flags"], None)
     assert st == code
+    if args["flags"] == 0:   # fw_step is fw_step_ex with no flags
+        st2 = L.fw_step(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S"],
+                        args["o"], ctypes.byref(shp), args["dtype"], args["mode"], args["phi"],
+                        args["eps"], None)
+        assert st2 == code
 
 
 @no_gpu
