@@ -194,7 +194,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int64_t chain = blockIdx.x;
     const int64_t T = a.T;
     const int nch = (int)((T + C - 1) / C);
-    const bool falcon = (a.mode == FW_FALCON1);
+    const bool gated = (a.mode != FW_LINATTN);                     // eta, gamma, decays
+    const bool falcon = (a.mode == FW_FALCON1);                    // residual: L, T, W
+    const bool shifted = gated && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;                 // o_t = S_{t-1}^T q_t
     const bool elu = (a.phi == FW_PHI_ELU1);
     const uint64_t limit = (uint64_t)a.wait_ns;
 
@@ -232,7 +235,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
-            const int shift = falcon ? 1 : 0;
+            const int shift = shifted ? 1 : 0;
             int nfill[NST] = {}, ny = 0;
             bool ok = true;
             for (int c = 0; c < nch && ok; ++c) {
@@ -244,19 +247,19 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const uint32_t st = xq(b);
                 const int y = c * C;
                 const uint32_t full = bar(B_FULL0 + b);
-                mbar_expect_tx(full, falcon ? 32 * KB : 48 * KB);
+                mbar_expect_tx(full, gated ? 32 * KB : 48 * KB);
                 tma_load_3d(st + XQ_X0, &tmk, 0, y - shift, (int)chain, full);
                 tma_load_3d(st + XQ_X1, &tmk, 64, y - shift, (int)chain, full);
                 tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
                 tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
-                if (!falcon) {
+                if (!gated) {
                     const uint32_t yv = yv_of(b);
                     tma_load_3d(yv, &tmv, 0, y, (int)chain, full);
                     tma_load_3d(yv + 8 * KB, &tmv, 64, y, (int)chain, full);
                 }
                 ++nfill[b];
                 TRACE(c, 19);
-                if (falcon) {
+                if (gated) {
                     if (c >= 1 && !wait_fast(bar(B_YFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) {
                         ok = false;
                         break;
@@ -313,7 +316,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     issue_g(c);
                     ++gnext;
                 }
-                if (!falcon) continue;
+                if (!gated) continue;
                 {   // T of chunk c; meanwhile the next Gram, once it can go
                     const uint64_t t0 = globaltimer();
                     for (;;) {
@@ -334,7 +337,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     break;
                 }
                 tc_fence_after();
-                {   // -W^T = X^T (-T diag Gm)^T, U^T = Y^T T^T
+                {   // -W^T = X^T (-T diag Gm)^T, U^T = Y^T T^T (Falcon-1A: T = I, no W)
                     const uint32_t id = idesc_bf16(128, 64, true, false);
                     const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);
                     const uint64_t dtp = sdesc_sw128(sb + lreg(c) + 8 * KB, 16, 1024);
@@ -343,7 +346,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     // two independent accumulator chains, interleaved
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        mma_bf16(tmem + COL_W, dx + kk * 128, dtp + kk * 2, id, kk > 0);
+                        if (falcon) mma_bf16(tmem + COL_W, dx + kk * 128, dtp + kk * 2, id, kk > 0);
                         mma_bf16(tmem + COL_R, dy + kk * 128, dt + kk * 2, id, kk > 0);
                     }
                     mma_commit(bar(B_WUDONE));
@@ -367,7 +370,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 // accumulators of chunk c-1 have been read
                 if (!wait_fast(bar(B_WRDY), (uint32_t)c & 1u, limit, s_abort) ||
                     !wait_fast(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort) ||
-                    (!falcon && c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort))) {
+                    (!gated && c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort))) {
                     ok = false;
                     break;
                 }
@@ -378,14 +381,22 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const uint64_t dq = sdesc_sw128(st + XQ_Q0, 16, 1024);
                 const uint64_t dp = sdesc_sw128(pb, 16, 1024);
                 const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);   // X as MN-major B (N = i)
-                if (falcon) {
-                    // R^T += S^T (-W^T), then O1^T = S^T Q^T
-                    const uint32_t id_mm = idesc_bf16(128, 64, false, true);
-                    const uint64_t dw = sdesc_sw128(sb + OFF_WTB, 8192, 1024);
+                if (gated) {
+                    // R^T += S^T (-W^T), then O1^T = S^T Q^T.  Falcon-1A: R = U = Y, so
+                    // R^T is ready once the key-path MMA warp's U^T is.
+                    if (falcon) {
+                        const uint32_t id_mm = idesc_bf16(128, 64, false, true);
+                        const uint64_t dw = sdesc_sw128(sb + OFF_WTB, 8192, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_ta(tmem + COL_R, sa + 8 * kk, dw + kk * 128, id_mm, 1);
-                    mma_commit(bar(B_RDONE));
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16_ta(tmem + COL_R, sa + 8 * kk, dw + kk * 128, id_mm, 1);
+                        mma_commit(bar(B_RDONE));
+                    } else {
+                        if (!wait_fast(bar(B_WUDONE), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                        tc_fence_after();
+                        tc_fence_before();
+                        mbar_arrive(bar(B_RDONE));
+                    }
                     TRACE(c, 0);
                     if (c >= 1 && !wait_fast(bar(B_OFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) { ok = false; break; }
                     tc_fence_after();
@@ -443,7 +454,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // S MMAs of chunk cc - NST, whose completion released the ring stage chunk
         // cc's keys were loaded into.)
         bool ok = true;
-        if (!falcon) {   // linear attention: eta = 1, no decay
+        if (!gated) {   // linear attention: eta = 1, no decay
             for (int b = 0; b < NST; ++b) {
                 float *v = vec(b);
                 for (int t = lane; t < C; t += 32) {
@@ -463,7 +474,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int64_t tok = (int64_t)cc * C + lane + 32 * u;
-                if (falcon && cc < nch && tok < T) {
+                if (gated && cc < nch && tok < T) {
                     nb[u] = a.beta[chain * T + tok];
                     nl[u] = a.lam[chain * T + tok];
                 }
@@ -476,10 +487,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             float *vg = vec(b);
             bool w = wait_bar(bar(B_FULL0 + b), (uint32_t)(cc / NST) & 1u, limit, s_abort);
             // chunk 0's first key row is patched with phi(k_init) before the Gram is released
-            if (falcon && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
+            if (gated && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             if (lane == 0) TRACE(cc, 21);
-            if (falcon) {
+            if (gated) {
                 const uint32_t xs = xq(b);
                 // |x_t|^2: the diagonal of each 16x16 block X_blk X_blk^T, on the warp's
                 // bf16 MMAs (fp32 accumulate).  One ldmatrix.x4 gives the A fragment of
@@ -530,7 +541,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     eta[u] = 0.f;
                     gam[u] = 1.f;
                     if (tok < T) {
-                        const bool pair = (tok > 0) || (a.k_init != nullptr);
+                        // the same-step pair writes from the first token on
+                        const bool pair = !shifted || (tok > 0) || (a.k_init != nullptr);
                         eta[u] = pair ? __fdividef(nb[u], n[u] + nl[u] + a.eps) : 0.f;
                         gam[u] = 1.f - eta[u] * nl[u];
                     }
@@ -618,8 +630,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (elu) {
                     const int t = kidx >> 2, qq = kidx & 3;
                     const uint32_t roff = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
-                    for (int which = 0; which < (falcon ? 1 : 2); ++which) {
-                        const int64_t src = (int64_t)cc * C + t - ((which == 0 && falcon) ? 1 : 0);
+                    for (int which = 0; which < (gated ? 1 : 2); ++which) {
+                        const int64_t src = (int64_t)cc * C + t - ((which == 0 && shifted) ? 1 : 0);
                         if (src < 0 || src >= T) continue;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
@@ -636,7 +648,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     }
                     wrote = true;
                 }
-                if (falcon && cc == 0 && a.k_init) {
+                if (gated && cc == 0 && a.k_init) {
                     if (kidx < 16) {
                         const int hb = kidx >> 3, c16 = kidx & 7;
                         const uint4 u = *reinterpret_cast<const uint4 *>(
@@ -685,7 +697,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         // linear attention needs no L
                     } else {
                         const int t = lrow ? kt : kt - C;
-                        const int top = lrow ? t - 1 : t;        // last active column
+                        // last active column: L is strictly lower; P includes the
+                        // diagonal, except when the read comes before the write
+                        const int top = (lrow || rbw) ? t - 1 : t;
                         float dz = 1.f;
                         if (h == 0 && top >= 32) dz = vg[V_Q32 / 4 + top];
 #pragma unroll
@@ -722,11 +736,30 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             return true;
         };
         if (!falcon) {
+            // Falcon-1A: T = I.  Its bf16 copy (in both solve regions, which this
+            // mode leaves unused) makes the key-path MMA warp's U^T = Y^T T^T the
+            // Y^T the state path takes as R^T.
+            if (gated) {
+                const int t = kidx >> 2, q2 = 2 * (kidx & 3);
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8) {
+                    float e[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) e[u] = (8 * (q2 + h8) + u == t) ? 1.f : 0.f;
+                    const uint32_t off = sw128((uint32_t)t, (uint32_t)(q2 + h8));
+                    st_row8_bf16(sb + lreg(0) + off, e);
+                    st_row8_bf16(sb + lreg(1) + off, e);
+                }
+                fence_proxy_async();
+            }
 #pragma unroll 1
             for (int c = 0; c < nch && ok; ++c) {
                 if (c > 0 && !early && !prep_go(c)) { ok = false; break; }
                 if (!lp(c, nullptr)) { ok = false; break; }
-                if (kidx == 0) mbar_arrive(bar(B_WRDY));
+                if (kidx == 0) {
+                    if (gated) mbar_arrive(bar(B_TRDY));   // the (static) T of chunk c
+                    mbar_arrive(bar(B_WRDY));
+                }
             }
         }
         // Falcon-1 (phi = identity): L/P of chunk c+1 runs while the W/U products of
@@ -922,7 +955,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         // initial state, transposed (this thread holds column j = srow of S):
         // TMEM <- G_{C-1}(chunk 0) S0^T, and the bf16 copy
         float gC0 = 1.f;
-        if (falcon) {
+        if (gated) {
             if (!gwait(bar(B_GV0), 0)) ok = false;
             else gC0 = vec(0)[V_GC / 4];
         }
@@ -949,7 +982,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         for (int c = 0; c < nch && ok; ++c) {
             const int b = c % NST;   // gate block
             const int64_t tok0 = (int64_t)c * C;
-            if (falcon) {
+            if (gated) {
                 // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
                 //      the output store of chunk c-1 has read the R^T buffer by then
                 if (srow == 0) { TRACE(c, 31); bulk_wait_read0(); }
@@ -959,7 +992,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 tc_fence_after();
                 const float *wc = vec(b) + V_WC / 4;
                 if (srow < C)   // the gate warp may recycle this gate block once S(c) is done
-                    reinterpret_cast<float *>(sm + OFF_SGV)[srow] = vec(b)[V_G / 4 + srow];
+                    reinterpret_cast<float *>(sm + OFF_SGV)[srow] =
+                        vec(b)[(rbw ? V_GM : V_G) / 4 + srow];   // G_{t-1} for a read before the write
                 {
                     float r[64];
                     tmem_ld64(tmem + lane_base + COL_R, r);
@@ -992,7 +1026,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tc_fence_after();
             const bool last = (c + 1 == nch);
             float gC_next = 1.f;
-            if (falcon && !last) {
+            if (gated && !last) {
                 const int b1 = (c + 1) % NST;
                 if (!gwait(bar(B_GV0 + b1), (uint32_t)((c + 1) / NST) & 1u)) { ok = false; break; }
                 gC_next = vec(b1)[V_GC / 4];
@@ -1035,7 +1069,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     if (srow == 0) TRACE(c, 26 + 2 * h);
 #pragma unroll
                     for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 g4 = falcon ? *reinterpret_cast<const float4 *>(gv + 32 * h + 4 * e4)
+                        const float4 g4 = gated ? *reinterpret_cast<const float4 *>(gv + 32 * h + 4 * e4)
                                                  : make_float4(1.f, 1.f, 1.f, 1.f);
                         const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
@@ -1102,16 +1136,13 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t b
 
 }  // namespace
 
-// Falcon-1 with phi = elu+1 is declined: phi(k) is close to 1 + k for small
-// keys, and rounding it to a bf16 MMA operand erases most of the key's varying
-// part, which the residual write depends on (the per-token kernel keeps it in
-// fp32).  Linear attention accumulates phi(k) additively and keeps bf16
-// operand accuracy.
+// Falcon-1 and Falcon-1A with phi = elu+1 are declined: phi(k) is close to
+// 1 + k for small keys, and rounding it to a bf16 MMA operand erases most of
+// the key's varying part, which the normalised step and the residual write
+// depend on (the per-token kernel keeps it in fp32).  Linear attention
+// accumulates phi(k) additively and keeps bf16 operand accuracy.
 bool chunked_supported(const PrefillArgs &a) {
-    if (a.mode == FW_FALCON1 && a.phi == FW_PHI_ELU1) return false;
-    // Falcon-1A and the read-before-write / same-step-pair arms run on the
-    // per-token kernel
-    if (a.mode == FW_FALCON1A || a.flags != 0) return false;
+    if (a.mode != FW_LINATTN && a.phi == FW_PHI_ELU1) return false;
     return a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
            a.n_chains <= (int64_t)INT32_MAX;
 }

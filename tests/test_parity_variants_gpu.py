@@ -77,6 +77,38 @@ def test_auto_variants_bf16_d128(T, mode, rbw, same_pair):
     _check(w, x, "auto", rbw, same_pair)
 
 
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 130, 257])
+@pytest.mark.parametrize("mode,rbw,same_pair", [("falcon1a", False, False),
+                                                ("falcon1a", True, False),
+                                                ("falcon1a", False, True),
+                                                ("falcon1a", True, True),
+                                                ("falcon1", True, False),
+                                                ("falcon1", False, True),
+                                                ("falcon1", True, True),
+                                                ("linattn", True, False)])
+def test_chunked_variants(T, mode, rbw, same_pair):
+    # the tensor-core kernel itself; S0 != 0 so the decayed start state is read
+    w, x = _inputs(mode, torch.bfloat16, 128, T=T, B=2, H=2, seed=T)
+    _check(w, x, "chunked", rbw, same_pair)
+
+
+def test_chunked_variants_match_recurrent_kernel():
+    # the two kernels on the same bf16 inputs agree far inside the gate
+    for mode, rbw, sp in (("falcon1a", True, True), ("falcon1", True, True)):
+        w, x = _inputs(mode, torch.bfloat16, 128, T=300, seed=2)
+        oc, Sc = _run(w, x, "chunked", rbw, sp)
+        orr, Sr = _run(w, x, "recurrent", rbw, sp)
+        assert rel_l2(to64(oc), to64(orr)) <= 1e-2
+        assert rel_l2(to64(Sc), to64(Sr)) <= 1e-2
+
+
+def test_chunked_falcon1a_k_init():
+    w, x = _inputs("falcon1a", torch.bfloat16, 128, T=150, seed=7)
+    k_init = torch.randn(w.B, w.H, w.d, generator=torch.Generator().manual_seed(8))
+    k_init = (k_init / k_init.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    _check(w, x, "chunked", False, False, k_init=k_init)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("d", [64, 128])
 def test_linattn_rbw(dtype, d):
