@@ -94,7 +94,8 @@ def algorithmic_bytes_prefill(w):
 
 def matmul_flops_prefill(w, C=64):
     """Dense matmul FLOPs of the chunked form per launch: Falcon-1
-    10 C d + 6 d^2 per head-token, linear attention 4 C d + 4 d^2."""
+    10 C d + 6 d^2 per head-token; linear attention and Falcon-1A (no
+    residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y)."""
     ht = w.B * w.H * w.T
     if w.mode == "falcon1":
         return ht * (10 * C * w.d + 6 * w.d * w.d)
@@ -192,7 +193,7 @@ def timed(fn, K, W, stream):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in ev]
 
 
-def bench_prefill(w, K, W, dev, fw, algo="auto"):
+def bench_prefill(w, K, W, dev, fw, algo="auto", rbw=False, same_pair=False):
     x = I.prefill_inputs(w, device=dev)
     o = torch.empty_like(x["q"])
     S_T = torch.empty(w.B, w.H, w.d, w.d, device=dev)
@@ -200,7 +201,8 @@ def bench_prefill(w, K, W, dev, fw, algo="auto"):
 
     def fn():
         fw.prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], x["S0"], mode=w.mode,
-                   phi=w.phi, eps=w.eps, algo=algo, o=o, S_T=S_T, stream=stream)
+                   phi=w.phi, eps=w.eps, algo=algo, o=o, S_T=S_T, stream=stream, rbw=rbw,
+                   same_pair=same_pair)
 
     total, per = timed(fn, K, W, stream)
     fw.check(stream)
@@ -216,6 +218,8 @@ def bench_prefill(w, K, W, dev, fw, algo="auto"):
         "recurrence_tflops": recurrence_flops(w) / (kern_ms / 1e3) / 1e12,
         "algo": algo,
     }
+    if rbw or same_pair:
+        res["flags"] = [f for f, on in (("rbw", rbw), ("same_pair", same_pair)) if on]
     return res, x
 
 
@@ -450,11 +454,15 @@ def main():
             out["cpu_baseline"] = cpu_baseline(w)
         if not args.no_extra:
             extra = {}
-            for name in ("linattn_bf16", "falcon1_long", "falcon1_fp32"):
+            for name in ("linattn_bf16", "falcon1_long", "falcon1_fp32", "falcon1a_bf16"):
                 wn = I.WORKLOADS[name]
                 r, _ = bench_prefill(wn, 5 if name != "falcon1_long" else 3, 3, dev, fw)
                 r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
                 extra[name] = r
+            # the read-before-write / same-step-pair arms on the headline workload
+            r, _ = bench_prefill(w, 5, 3, dev, fw, rbw=True, same_pair=True)
+            r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
+            extra[w.name + "+rbw+same_pair"] = r
             dec = bench_decode(I.DECODE["steps"], 3, dev, fw)
             dec["hbm_frac"] = dec["hbm_gbs"] / peaks["hbm"]
             extra["decode"] = dec
