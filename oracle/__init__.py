@@ -32,7 +32,7 @@ _lock = threading.Lock()
 _lib = None
 
 PHI = {"identity": 0, "elu1": 1}
-MODE = {"falcon1": 0, "linattn": 1, "falcon1a": 2}
+MODE = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4}
 FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 
 
@@ -113,6 +113,27 @@ def falcon1(q, k, v, beta, lam, S0=None, k_init=None, phi="identity", eps=1e-6,
     return o, S
 
 
+def falcon2(q, k, v, beta, lam, S0=None, k_init=None, phi="identity", eps=1e-6,
+            nthreads=None, inner=False, rbw=False, same_pair=False):
+    """Falcon-2 prefill: a step per value channel (inner=True: Falcon-2A).
+    As falcon1, with beta [..., T, dv].  Returns (o, S_T) as float64 arrays."""
+    q, k, v, beta, lam = map(_f64, (q, k, v, beta, lam))
+    S0, k_init = _f64(S0), _f64(k_init)
+    lead = q.shape[:-2]
+    T, dk = q.shape[-2:]
+    dv = v.shape[-1]
+    nc = int(np.prod(lead)) if lead else 1
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T, dv) and lam.shape == lead + (T,)
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (dk, dv))
+    _load().orc_falcon1(nc, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                        _ptr(S0), _ptr(k_init), PHI[phi], float(eps),
+                        MODE["falcon2a" if inner else "falcon2"], _flags(rbw, same_pair),
+                        _ptr(o), _ptr(S), nthreads or default_threads())
+    return o, S
+
+
 def linattn(q, k, v, S0=None, phi="elu1", nthreads=None, rbw=False):
     """Plain causal linear attention (rbw: read before the write).
     Returns (o, S_T) as float64 arrays."""
@@ -131,9 +152,10 @@ def linattn(q, k, v, S0=None, phi="elu1", nthreads=None, rbw=False):
 
 def step(q, k_prev, v, beta, lam, S, mode="falcon1", phi="identity", eps=1e-6,
          nthreads=None, rbw=False):
-    """One decode step (mode falcon1, falcon1a or linattn; rbw: o = S_old^T q).
-    q,k_prev [..., dk]; v [..., dv]; beta, lam [...] (may be None in linattn
-    mode); S [..., dk, dv].  Returns (o, S_new) as new arrays."""
+    """One decode step (mode falcon1, falcon1a, falcon2, falcon2a or linattn;
+    rbw: o = S_old^T q).  q,k_prev [..., dk]; v [..., dv]; beta, lam [...]
+    (beta [..., dv] for falcon2 / falcon2a; both may be None in linattn mode);
+    S [..., dk, dv].  Returns (o, S_new) as new arrays."""
     q, k_prev, v = map(_f64, (q, k_prev, v))
     beta, lam = _f64(beta), _f64(lam)
     S = _f64(S).copy()

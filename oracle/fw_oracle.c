@@ -19,6 +19,11 @@
  *  - same page, §1.4 and §4.1: read after write (o_t = S_t^T q_t), the
  *    shifted training pair (x_t, y_t) = (phi(k_{t-1}), v_t), and the boundary
  *    x_1 := 0, eta_1 := 0 (the first token's write is a no-op).
+ *  - same page, §4.2: Falcon-2, a step per value channel j,
+ *        eta_{j,t} = beta_{j,t} / (|x_t|^2 + lambda_t + eps),
+ *    with the residual r_t and the feature x_t shared: column j of S takes
+ *    its own scalar write S[:,j] = (1 - eta_{j,t} lambda_t) S[:,j]
+ *    + eta_{j,t} x_t r_{t,j}.
  *  - same page, §4.3: the inner-product family (Falcon-1A): the loss
  *    -<S^T x_t, y_t> + (lambda/2)|S|^2 gives the additive write
  *        S_t = (1 - eta_t lambda_t) S_{t-1} + eta_t x_t y_t^T
@@ -39,7 +44,10 @@
  *  - an optional k_init replaces the zero pair of the first token (so that a
  *    prefill can continue a previous one); then eta_1 follows the formula.
  *  - Falcon-1A takes Falcon-1's eta_t, pairing and boundary; only the write
- *    drops the residual (r_t := y_t).
+ *    drops the residual (r_t := y_t).  Falcon-2A is Falcon-2 with that
+ *    additive write.
+ *  - Falcon-2 keeps lambda_t shared by the channels (the page gives only beta
+ *    a channel index) and Falcon-1's pairing and boundary.
  *  - read-before-write (no formula printed): o_t = S_{t-1}^T q_t, the read
  *    taken before token t's write.
  *  - same-step pair (no formula printed): x_t = phi(k_t) for every t; the
@@ -47,6 +55,7 @@
  *
  * Layouts (all contiguous, row-major, double):
  *   q, k   [nc][T][dk]     v, o   [nc][T][dv]     beta, lam [nc][T]
+ *   beta of Falcon-2 / 2A: [nc][T][dv]
  *   S0, S  [nc][dk][dv]    k_init [nc][dk]
  * S[i][j] is key row i, value column j; reads are o_j = sum_i S[i][j] q_i.
  */
@@ -56,7 +65,7 @@
 #include <string.h>
 
 enum { ORC_PHI_IDENTITY = 0, ORC_PHI_ELU1 = 1 };
-enum { ORC_FALCON1 = 0, ORC_LINATTN = 1, ORC_FALCON1A = 2 };
+enum { ORC_FALCON1 = 0, ORC_LINATTN = 1, ORC_FALCON1A = 2, ORC_FALCON2 = 3, ORC_FALCON2A = 4 };
 enum { ORC_RBW = 1, ORC_SAME_PAIR = 2 };
 
 /* elu(z) + 1: z + 1 for z > 0, exp(z) for z <= 0 (blog §4.1). */
@@ -77,11 +86,14 @@ static void read_state(int dk, int dv, const double *S, const double *q, double 
     }
 }
 
-/* One Falcon-1 (inner == 0) or Falcon-1A (inner == 1) chain, token by token. */
+/* One Falcon-1 / Falcon-1A chain (inner == 1: no residual), token by token.
+ * chan == 1: Falcon-2 / 2A, beta is [T][dv] and every value channel takes its
+ * own step and decay; eta_v, gamma_v are dv scratch values. */
 static void falcon1_chain(long T, int dk, int dv, const double *q, const double *k,
                           const double *v, const double *beta, const double *lam,
                           const double *S0, const double *k_init, int phi, double eps,
-                          int inner, int flags, double *o, double *S, double *x, double *r)
+                          int inner, int chan, int flags, double *o, double *S, double *x,
+                          double *r, double *eta_v, double *gamma_v)
 {
     long t;
     int i, j;
@@ -90,17 +102,20 @@ static void falcon1_chain(long T, int dk, int dv, const double *q, const double 
     else memset(S, 0, sizeof(double) * (size_t)dk * dv);
 
     for (t = 0; t < T; ++t) {
-        double eta = 0.0, gamma, n = 0.0;
+        double n = 0.0;
         const double *kprev = same ? k + t * dk : (t > 0) ? k + (t - 1) * dk : k_init;
         if (rbw) read_state(dk, dv, S, q + t * dk, o + t * dv);   /* read before write */
         if (kprev) {
             for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kprev[i]);
             for (i = 0; i < dk; ++i) n += x[i] * x[i];
-            eta = beta[t] / (n + lam[t] + eps);
         } else {
             for (i = 0; i < dk; ++i) x[i] = 0.0; /* x_1 := 0, eta_1 := 0 */
         }
-        gamma = 1.0 - eta * lam[t];
+        for (j = 0; j < dv; ++j) {
+            const double b = chan ? beta[t * dv + j] : beta[t];
+            eta_v[j] = kprev ? b / (n + lam[t] + eps) : 0.0;
+            gamma_v[j] = 1.0 - eta_v[j] * lam[t];
+        }
         /* residual against the state before the write (Falcon-1A: the target) */
         for (j = 0; j < dv; ++j) {
             double a = 0.0;
@@ -108,10 +123,10 @@ static void falcon1_chain(long T, int dk, int dv, const double *q, const double 
                 for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
             r[j] = v[t * dv + j] - a;
         }
-        /* the write */
+        /* the write, column by column */
         for (i = 0; i < dk; ++i)
             for (j = 0; j < dv; ++j)
-                S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
+                S[(size_t)i * dv + j] = gamma_v[j] * S[(size_t)i * dv + j] + eta_v[j] * x[i] * r[j];
         if (!rbw) read_state(dk, dv, S, q + t * dk, o + t * dv);   /* read after write */
     }
 }
@@ -138,9 +153,10 @@ static void linattn_chain(long T, int dk, int dv, const double *q, const double 
     }
 }
 
-/* One decode step of one state (in place); qt is scratch for phi(q). */
+/* One decode step of one state (in place); qt is scratch for phi(q).  beta
+ * points at this state's step size (Falcon-2 / 2A: dv of them). */
 static void step_one(int mode, int flags, int dk, int dv, const double *q, const double *kp,
-                     const double *v, double beta, double lam, int phi, double eps,
+                     const double *v, const double *beta, double lam, int phi, double eps,
                      double *S, double *o, double *x, double *r, double *qt)
 {
     int i, j;
@@ -155,21 +171,24 @@ static void step_one(int mode, int flags, int dk, int dv, const double *q, const
         return;
     }
     {
-        double n = 0.0, eta, gamma;
+        const int chan = (mode == ORC_FALCON2 || mode == ORC_FALCON2A);
+        const int inner = (mode == ORC_FALCON1A || mode == ORC_FALCON2A);
+        double n = 0.0;
         for (i = 0; i < dk; ++i) x[i] = orc_phi(phi, kp[i]);
         for (i = 0; i < dk; ++i) n += x[i] * x[i];
-        eta = beta / (n + lam + eps);
-        gamma = 1.0 - eta * lam;
         if (rbw) read_state(dk, dv, S, q, o);
         for (j = 0; j < dv; ++j) {
             double a = 0.0;
-            if (mode != ORC_FALCON1A)
+            if (!inner)
                 for (i = 0; i < dk; ++i) a += S[(size_t)i * dv + j] * x[i];
             r[j] = v[j] - a;
         }
-        for (i = 0; i < dk; ++i)
-            for (j = 0; j < dv; ++j)
+        for (j = 0; j < dv; ++j) {
+            const double eta = (chan ? beta[j] : beta[0]) / (n + lam + eps);
+            const double gamma = 1.0 - eta * lam;
+            for (i = 0; i < dk; ++i)
                 S[(size_t)i * dv + j] = gamma * S[(size_t)i * dv + j] + eta * x[i] * r[j];
+        }
         if (!rbw) read_state(dk, dv, S, q, o);
     }
 }
@@ -191,8 +210,10 @@ static void *orc_worker(void *arg)
 {
     orc_job *J = (orc_job *)arg;
     int dk = J->dk, dv = J->dv;
-    double *x = (double *)malloc(sizeof(double) * (size_t)(dk + dv + dk));
-    double *r = x + dk, *qt = r + dv;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(dk + dv + dk + 2 * dv));
+    double *r = x + dk, *qt = r + dv, *eta_v = qt + dk, *gamma_v = eta_v + dv;
+    const int chan = (J->mode == ORC_FALCON2 || J->mode == ORC_FALCON2A);
+    const long bstride = chan ? (long)dv : 1;
     for (;;) {
         long c;
         pthread_mutex_lock(&J->mu);
@@ -201,11 +222,11 @@ static void *orc_worker(void *arg)
         if (c >= J->nc) break;
         if (J->kind == 0) {
             falcon1_chain(J->T, dk, dv, J->q + c * J->T * dk, J->k + c * J->T * dk,
-                          J->v + c * J->T * dv, J->beta + c * J->T, J->lam + c * J->T,
+                          J->v + c * J->T * dv, J->beta + c * J->T * bstride, J->lam + c * J->T,
                           J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
                           J->k_init ? J->k_init + (size_t)c * dk : NULL, J->phi, J->eps,
-                          J->mode == ORC_FALCON1A, J->flags, J->o + c * J->T * dv,
-                          J->S + (size_t)c * dk * dv, x, r);
+                          J->mode == ORC_FALCON1A || J->mode == ORC_FALCON2A, chan, J->flags,
+                          J->o + c * J->T * dv, J->S + (size_t)c * dk * dv, x, r, eta_v, gamma_v);
         } else if (J->kind == 1) {
             linattn_chain(J->T, dk, dv, J->q + c * J->T * dk, J->k + c * J->T * dk,
                           J->v + c * J->T * dv, J->S0 ? J->S0 + (size_t)c * dk * dv : NULL,
@@ -213,7 +234,7 @@ static void *orc_worker(void *arg)
                           x, qt);
         } else {
             step_one(J->mode, J->flags, dk, dv, J->q + (size_t)c * dk, J->k + (size_t)c * dk,
-                     J->v + (size_t)c * dv, J->beta ? J->beta[c] : 0.0,
+                     J->v + (size_t)c * dv, J->beta ? J->beta + c * bstride : NULL,
                      J->lam ? J->lam[c] : 0.0, J->phi, J->eps,
                      J->S + (size_t)c * dk * dv, J->o + (size_t)c * dv, x, r, qt);
         }
@@ -242,8 +263,9 @@ static void orc_run(orc_job *J, int nthreads)
 
 /* ---- exported entry points --------------------------------------------- */
 
-/* Falcon-1 (mode ORC_FALCON1) or Falcon-1A (ORC_FALCON1A) prefill over nc
- * independent chains; flags: ORC_RBW, ORC_SAME_PAIR.  S0, k_init may be NULL. */
+/* Falcon-1 / 1A / 2 / 2A prefill (mode ORC_FALCON1, ORC_FALCON1A, ORC_FALCON2,
+ * ORC_FALCON2A; beta is [nc][T][dv] for the last two) over nc independent
+ * chains; flags: ORC_RBW, ORC_SAME_PAIR.  S0, k_init may be NULL. */
 void orc_falcon1(long nc, long T, int dk, int dv, const double *q, const double *k,
                  const double *v, const double *beta, const double *lam, const double *S0,
                  const double *k_init, int phi, double eps, int mode, int flags, double *o,
@@ -270,8 +292,8 @@ void orc_linattn(long nc, long T, int dk, int dv, const double *q, const double 
     orc_run(&J, nthreads);
 }
 
-/* One decode step for ns independent states (flags: ORC_RBW); S is updated in
- * place. */
+/* One decode step for ns independent states (flags: ORC_RBW; beta is [ns][dv]
+ * for ORC_FALCON2 / ORC_FALCON2A); S is updated in place. */
 void orc_step(long ns, int dk, int dv, int mode, int flags, const double *q,
               const double *k_prev, const double *v, const double *beta, const double *lam,
               int phi, double eps, double *S, double *o, int nthreads)

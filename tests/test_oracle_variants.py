@@ -3,8 +3,9 @@ oracle's own token loop.
 
 Variants (page "Fast Weight Attention for Continual Learning"): the
 inner-product family Falcon-1A (§4.3: additive write, no residual, the same
-normalised step), and the read-before-write / same-step-pair arms of the
-2 x 2 pairing design (§3.3, §4.1).  The pages print no formula for the two
+normalised step), Falcon-2 and 2A (§4.2: a step size per value channel, the
+residual and feature shared), and the read-before-write / same-step-pair
+arms of the 2 x 2 pairing design (§3.3, §4.1).  The pages print no formula for the two
 arms; the readings pinned here are o_t = S_{t-1}^T q_t and x_t = phi(k_t).
 """
 import numpy as np
@@ -180,5 +181,67 @@ def test_prefill_equals_steps_for_the_variants(inner, rbw):
         kp = k[:, t - 1] if t > 0 else np.zeros_like(k[:, 0])
         b = beta[:, t] if t > 0 else np.zeros_like(beta[:, 0])   # empty first write
         ot, Sc = oracle.step(q[:, t], kp, v[:, t], b, lam[:, t], Sc, mode=mode, rbw=rbw)
+        np.testing.assert_allclose(ot, o[:, t], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Sc, S, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ Falcon-2 (per channel)
+
+@pytest.mark.parametrize("inner", [False, True])
+def test_falcon2_with_equal_channel_steps_is_falcon1(inner):
+    q, k, v, beta, lam, S0 = rand_inputs()
+    beta_c = np.repeat(beta[..., None], v.shape[-1], axis=-1)
+    o2, S2 = oracle.falcon2(q, k, v, beta_c, lam, S0, inner=inner)
+    o1, S1 = oracle.falcon1(q, k, v, beta, lam, S0, inner=inner)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(S2, S1, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("inner", [False, True])
+@pytest.mark.parametrize("rbw,same_pair", [(False, False), (True, True)])
+def test_falcon2_channels_are_independent_scalar_writes(inner, rbw, same_pair):
+    # the page's "d_v independent scalar updates sharing one separable
+    # objective": column j of Falcon-2 is Falcon-1 on value column j alone,
+    # with that column's step sizes
+    q, k, v, _, lam, S0 = rand_inputs(T=11)
+    beta_c = RNG.uniform(0.1, 1.9, v.shape)
+    o2, S2 = oracle.falcon2(q, k, v, beta_c, lam, S0, inner=inner, rbw=rbw, same_pair=same_pair)
+    for j in range(v.shape[-1]):
+        o1, S1 = oracle.falcon1(q, k, v[..., j:j + 1], beta_c[..., j], lam, S0[..., j:j + 1],
+                                inner=inner, rbw=rbw, same_pair=same_pair)
+        np.testing.assert_allclose(o2[..., j:j + 1], o1, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(S2[..., j:j + 1], S1, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
+def test_falcon2_step_direct_formula(mode):
+    ns, dk, dv = 3, 6, 5
+    q = RNG.standard_normal((ns, dk))
+    kp = RNG.standard_normal((ns, dk))
+    v = RNG.standard_normal((ns, dv))
+    beta = RNG.uniform(0.1, 1.5, (ns, dv))
+    lam = RNG.uniform(0.0, 0.1, (ns,))
+    S = RNG.standard_normal((ns, dk, dv))
+    n = np.einsum("ci,ci->c", kp, kp)
+    eta = beta / (n + lam + 1e-6)[:, None]           # [ns, dv]
+    g = 1.0 - eta * lam[:, None]
+    r = v - (np.einsum("cij,ci->cj", S, kp) if mode == "falcon2" else 0.0)
+    S_new = g[:, None, :] * S + eta[:, None, :] * np.einsum("ci,cj->cij", kp, r)
+    for rbw in (False, True):
+        o, S2 = oracle.step(q, kp, v, beta, lam, S, mode=mode, rbw=rbw)
+        np.testing.assert_allclose(S2, S_new, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(o, np.einsum("cij,ci->cj", S if rbw else S_new, q),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_falcon2_prefill_equals_steps():
+    q, k, v, _, lam, S0 = rand_inputs(T=6)
+    beta_c = RNG.uniform(0.1, 1.5, v.shape)
+    o, S = oracle.falcon2(q, k, v, beta_c, lam, S0)
+    Sc = S0.copy()
+    for t in range(q.shape[1]):
+        kp = k[:, t - 1] if t > 0 else np.zeros_like(k[:, 0])
+        b = beta_c[:, t] if t > 0 else np.zeros_like(beta_c[:, 0])
+        ot, Sc = oracle.step(q[:, t], kp, v[:, t], b, lam[:, t], Sc, mode="falcon2")
         np.testing.assert_allclose(ot, o[:, t], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(Sc, S, rtol=1e-12, atol=1e-12)
