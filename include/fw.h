@@ -16,7 +16,10 @@
  * boundary x_1 := 0, eta_1 := 0 (§4.1), and reads after the write,
  * o_t = S_t^T q_t (§1.4).  FW_FALCON1A is the same page's inner-product family
  * (§4.3): the write drops the residual, S_t = (1 - eta_t lambda_t) S_{t-1}
- * + eta_t x_t y_t^T, with Falcon-1's step, pairing and boundary.  Flags select
+ * + eta_t x_t y_t^T, with Falcon-1's step, pairing and boundary.  FW_FALCON2 and
+ * FW_FALCON2A take a step size per value channel (§4.2): beta is indexed by the
+ * value column j as well, eta_{j,t} = beta_{j,t} / (|x_t|^2 + lambda_t + eps),
+ * and column j of S takes its own scalar write.  Flags select
  * the other arms of the page's read / pairing design (§3.3, §4.1): reading
  * before the write and the same-step pair.  FW_LINATTN selects plain causal linear attention,
  * S_t = S_{t-1} + phi(k_t) v_t^T, o_t = S_t^T phi(q_t) ("Attention is also an
@@ -27,8 +30,9 @@
  *     never allocates, frees or keeps them.  Rows are contiguous, row-major.
  *   - q, k, v, o:  [B][H][T][d] (prefill) or [B][H][d] (step), element type
  *     FW_F32 (float) or FW_BF16 (bfloat16), d innermost.
- *   - beta, lambda: float [B][H][T] (prefill) or [B][H] (step).  Ignored (may
- *     be NULL) in FW_LINATTN mode, required in FW_FALCON1 and FW_FALCON1A.
+ *   - beta, lambda: float [B][H][T] (prefill) or [B][H] (step); beta of
+ *     FW_FALCON2 / FW_FALCON2A is float [B][H][T][d_v] (prefill) or [B][H][d_v]
+ *     (step).  Ignored (may be NULL) in FW_LINATTN mode, required otherwise.
  *   - S0, S_T, S: float [B][H][d_k][d_v], S[i][j] = key row i, value column j,
  *     so a read is o_j = sum_i S[i][j] q_i (the blog's y = q @ S).
  *   - Pointers must be 16-byte aligned (vector and TMA loads).
@@ -56,8 +60,12 @@ typedef enum { FW_F32 = 0, FW_BF16 = 1 } fw_dtype;
 /* FW_FALCON1: shifted pair, residual write, normalised step and decay.
  * FW_LINATTN: same-step pair, additive write S += phi(k) v^T, no eta/gamma.
  * FW_FALCON1A: Falcon-1's pair, step and decay with the additive write
- *              S = gamma S + eta x v^T (no residual). */
-typedef enum { FW_FALCON1 = 0, FW_LINATTN = 1, FW_FALCON1A = 2 } fw_mode;
+ *              S = gamma S + eta x v^T (no residual).
+ * FW_FALCON2, FW_FALCON2A: FW_FALCON1, FW_FALCON1A with a step size (and so a
+ *              decay) per value channel; beta carries a trailing d_v index. */
+typedef enum {
+    FW_FALCON1 = 0, FW_LINATTN = 1, FW_FALCON1A = 2, FW_FALCON2 = 3, FW_FALCON2A = 4
+} fw_mode;
 
 /* Flags (bitwise OR) of fw_prefill_ex and fw_step_ex.
  * FW_FLAG_RBW: read before the write, o_t = S_{t-1}^T q_t (every mode).
@@ -109,15 +117,16 @@ enum {
  * triangular solve, short inter-chunk recurrence, parallel outputs).
  *
  *   q, k, v  in   [B][H][T][d] of `dtype`
- *   beta     in   float [B][H][T]   (FW_FALCON1, FW_FALCON1A; beta_t in
- *                                     [0, 2) keeps the Falcon-1 write stable,
- *                                     other values are computed literally)
- *   lambda   in   float [B][H][T]   (FW_FALCON1, FW_FALCON1A; >= 0)
+ *   beta     in   float [B][H][T], or [B][H][T][d_v] for FW_FALCON2 /
+ *                 FW_FALCON2A (not FW_LINATTN; beta in [0, 2) keeps the
+ *                 regression write stable, other values are computed
+ *                 literally)
+ *   lambda   in   float [B][H][T]   (not FW_LINATTN; >= 0)
  *   S0       in   float [B][H][d][d] or NULL for a zero start state
  *   o        out  [B][H][T][d] of `dtype` (rounded to nearest even for bf16);
  *                 must not overlap any input
  *   S_T      out  float [B][H][d][d], the state after token T; may equal S0
- *   eps      in   >= 0, added to the step's denominator (FW_FALCON1, FW_FALCON1A)
+ *   eps      in   >= 0, added to the step's denominator (not FW_LINATTN)
  * Returns FW_OK or a negative FW_ERR_* code.
  */
 int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
@@ -153,7 +162,8 @@ int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta
  * sequence with steps pass beta = 0 (an empty first write).
  *
  *   q, k_prev, v  in      [B][H][d] of `dtype`
- *   beta, lambda  in      float [B][H] (FW_FALCON1, FW_FALCON1A)
+ *   beta, lambda  in      float [B][H] (beta [B][H][d_v] for FW_FALCON2 /
+ *                         FW_FALCON2A; not used by FW_LINATTN)
  *   S             in/out  float [B][H][d][d]
  *   o             out     [B][H][d] of `dtype`, o = S_new^T q
  *   shape         T must be 1

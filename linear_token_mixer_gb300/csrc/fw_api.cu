@@ -66,7 +66,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 // Modes with the normalised step and decay (beta, lambda, eps used).
-bool gated(fw_mode m) { return m == FW_FALCON1 || m == FW_FALCON1A; }
+bool gated(fw_mode m) { return m != FW_LINATTN; }
+
+// Modes with a step size per value channel (beta carries a d_v index).
+bool per_channel(fw_mode m) { return m == FW_FALCON2 || m == FW_FALCON2A; }
 
 int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
                  unsigned flags) {
@@ -77,7 +80,9 @@ int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi
     if (shape->B > (int64_t)1 << 31 || shape->H > (int64_t)1 << 31) return FW_ERR_SHAPE;
     if (shape->B * shape->H > (int64_t)INT32_MAX) return FW_ERR_SHAPE;
     if (dtype != FW_F32 && dtype != FW_BF16) return FW_ERR_DTYPE;
-    if (mode != FW_FALCON1 && mode != FW_LINATTN && mode != FW_FALCON1A) return FW_ERR_MODE;
+    if (mode != FW_FALCON1 && mode != FW_LINATTN && mode != FW_FALCON1A && mode != FW_FALCON2 &&
+        mode != FW_FALCON2A)
+        return FW_ERR_MODE;
     if (phi != FW_PHI_IDENTITY && phi != FW_PHI_ELU1) return FW_ERR_MODE;
     if (flags & ~(unsigned)(FW_FLAG_RBW | FW_FLAG_SAME_PAIR)) return FW_ERR_MODE;
     if (gated(mode) && !(std::isfinite(eps) && eps >= 0.f)) return FW_ERR_ARG;
@@ -110,12 +115,13 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     const size_t esz = dtype == FW_F32 ? 4 : 2;
     const size_t nx = (size_t)nc * (size_t)shape->T * d * esz;
     const size_t ns = (size_t)nc * d * d * sizeof(float);
-    const size_t nbl = (size_t)nc * (size_t)shape->T * sizeof(float);
+    const size_t nl = (size_t)nc * (size_t)shape->T * sizeof(float);   // lambda
+    const size_t nbl = nl * (per_channel(mode) ? (size_t)d : 1);           // beta
     if (overlaps(o, nx, q, nx) || overlaps(o, nx, k, nx) || overlaps(o, nx, v, nx) ||
         overlaps(o, nx, S0, S0 ? ns : 0) || overlaps(o, nx, S_T, ns))
         return FW_ERR_ARG;
-    if (gated(mode) && (overlaps(o, nx, beta, nbl) || overlaps(o, nx, lambda, nbl) ||
-                        overlaps(S_T, ns, beta, nbl) || overlaps(S_T, ns, lambda, nbl)))
+    if (gated(mode) && (overlaps(o, nx, beta, nbl) || overlaps(o, nx, lambda, nl) ||
+                        overlaps(S_T, ns, beta, nbl) || overlaps(S_T, ns, lambda, nl)))
         return FW_ERR_ARG;
     if (overlaps(S_T, ns, q, nx) || overlaps(S_T, ns, k, nx) || overlaps(S_T, ns, v, nx))
         return FW_ERR_ARG;
@@ -174,8 +180,9 @@ extern "C" int fw_step_ex(const void *q, const void *k_prev, const void *v, cons
         overlaps(o, nx, S, nst) || overlaps(S, nst, q, nx) || overlaps(S, nst, k_prev, nx) ||
         overlaps(S, nst, v, nx))
         return FW_ERR_ARG;
-    if (gated(mode) && (overlaps(S, nst, beta, ns * 4) || overlaps(S, nst, lambda, ns * 4) ||
-                        overlaps(o, nx, beta, ns * 4) || overlaps(o, nx, lambda, ns * 4)))
+    const size_t nb = (size_t)ns * 4 * (per_channel(mode) ? (size_t)d : 1);
+    if (gated(mode) && (overlaps(S, nst, beta, nb) || overlaps(S, nst, lambda, ns * 4) ||
+                        overlaps(o, nx, beta, nb) || overlaps(o, nx, lambda, ns * 4)))
         return FW_ERR_ARG;
 
     int *err = nullptr;

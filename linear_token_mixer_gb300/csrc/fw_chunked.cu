@@ -1143,6 +1143,9 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t b
 // accumulates phi(k) additively and keeps bf16 operand accuracy.
 bool chunked_supported(const PrefillArgs &a) {
     if (a.mode != FW_LINATTN && a.phi == FW_PHI_ELU1) return false;
+    // a step per value channel gives every channel its own triangular system:
+    // Falcon-2 / 2A run on the per-token kernel
+    if (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A) return false;
     return a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
            a.n_chains <= (int64_t)INT32_MAX;
 }

@@ -11,8 +11,9 @@
 //     S[i][j] <- gamma S[i][j] + eta x_i r_j,
 // the Falcon-1 write and read-after-write of "Fast Weight Attention for
 // Continual Learning" paper reading §3.2/§1.4 with the pair (phi(k_prev), v).
-// Falcon-1A (§4.3) drops the residual (r = v); FW_FLAG_RBW reads before the
-// write, o_j = c_j.  Linear-attention mode: x = phi(k), r = v,
+// Falcon-1A (§4.3) drops the residual (r = v); Falcon-2 / 2A (§4.2) take beta,
+// and so eta and gamma, per value column; FW_FLAG_RBW reads before the write,
+// o_j = c_j.  Linear-attention mode: x = phi(k), r = v,
 // eta = gamma = 1, read with phi(q) ("Attention is also an FFN" blog §4.1,
 // forward_step).
 //
@@ -37,7 +38,8 @@ decode_kernel(StepArgs a) {
     const int rg = tid / TPR;
     const int64_t s = blockIdx.x;
     const bool falcon = (a.mode != FW_LINATTN);   // eta, gamma
-    const bool resid = (a.mode == FW_FALCON1);     // r = v - S^T x
+    const bool resid = (a.mode == FW_FALCON1 || a.mode == FW_FALCON2);   // r = v - S^T x
+    const bool chan = (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A);   // beta per column
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
     float4 *Sp = reinterpret_cast<float4 *>(a.S + s * D * D);
@@ -72,11 +74,15 @@ decode_kernel(StepArgs a) {
     float n = 0.f, xq = 0.f;
 #pragma unroll
     for (int w = 0; w < D / 32; ++w) { n += wsum[w][0]; xq += wsum[w][1]; }
-    float eta = 1.f, gam = 1.f;
+    // eta, gamma of this thread's four value columns cq*4 .. cq*4+3
+    float4 eta = make_float4(1.f, 1.f, 1.f, 1.f), gam = eta;
     if (falcon) {
         const float lt = a.lam[s];
-        eta = a.beta[s] / (n + lt + a.eps);
-        gam = 1.f - eta * lt;
+        const float den = n + lt + a.eps;
+        const float4 b4 = chan ? *reinterpret_cast<const float4 *>(a.beta + s * D + cq * 4)
+                               : make_float4(a.beta[s], a.beta[s], a.beta[s], a.beta[s]);
+        eta = make_float4(b4.x / den, b4.y / den, b4.z / den, b4.w / den);
+        gam = make_float4(1.f - eta.x * lt, 1.f - eta.y * lt, 1.f - eta.z * lt, 1.f - eta.w * lt);
     }
 
     float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pc = pa;
@@ -106,11 +112,10 @@ decode_kernel(StepArgs a) {
     else r = vv;
 
     if (rg == 0) {
-        const float ex = eta * xq;
         float4 ov = C;   // read before the write
         if (!rbw) {
-            ov.x = fmaf(gam, C.x, ex * r.x); ov.y = fmaf(gam, C.y, ex * r.y);
-            ov.z = fmaf(gam, C.z, ex * r.z); ov.w = fmaf(gam, C.w, ex * r.w);
+            ov.x = fmaf(gam.x, C.x, eta.x * xq * r.x); ov.y = fmaf(gam.y, C.y, eta.y * xq * r.y);
+            ov.z = fmaf(gam.z, C.z, eta.z * xq * r.z); ov.w = fmaf(gam.w, C.w, eta.w * xq * r.w);
         }
         TIn *og = static_cast<TIn *>(a.o) + s * D + cq * 4;
         og[0] = from_f32<TIn>(ov.x); og[1] = from_f32<TIn>(ov.y);
@@ -120,10 +125,10 @@ decode_kernel(StepArgs a) {
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
         const int row = p * RPP + rg;
-        const float ex = eta * xs[row];
+        const float xr = xs[row];
         float4 nv;
-        nv.x = fmaf(gam, Sr[p].x, ex * r.x); nv.y = fmaf(gam, Sr[p].y, ex * r.y);
-        nv.z = fmaf(gam, Sr[p].z, ex * r.z); nv.w = fmaf(gam, Sr[p].w, ex * r.w);
+        nv.x = fmaf(gam.x, Sr[p].x, eta.x * xr * r.x); nv.y = fmaf(gam.y, Sr[p].y, eta.y * xr * r.y);
+        nv.z = fmaf(gam.z, Sr[p].z, eta.z * xr * r.z); nv.w = fmaf(gam.w, Sr[p].w, eta.w * xr * r.w);
         __stcs(&Sp[row * TPR + cq], nv);
     }
 }

@@ -12,7 +12,8 @@
 // i.e. the Falcon-1 write of "Fast Weight Attention for Continual Learning"
 // paper reading §3.2/§4.2 on the pair (phi(k_{t-1}), v_t) with x_1 = 0,
 // eta_1 = 0 (§4.1) and the read after the write (§1.4).  Falcon-1A (§4.3)
-// drops the residual (r = y); with FW_FLAG_SAME_PAIR the pair is
+// drops the residual (r = y); Falcon-2 / 2A (§4.2) take beta, and so eta and
+// gamma, per value column; with FW_FLAG_SAME_PAIR the pair is
 // (phi(k_t), v_t) for every token, and with FW_FLAG_RBW the read is taken
 // before the write, o_j = c_j (the §3.3 read / pairing arms).
 // Linear-attention mode uses x = phi(k_t), r = v_t, gamma = eta = 1 and reads
@@ -40,14 +41,15 @@ recurrent_kernel(PrefillArgs a) {
     const int col0 = (blockIdx.y * kNWarp + warp) * kJW;
     const int64_t T = a.T;
     const bool falcon = (a.mode != FW_LINATTN);                     // eta, gamma, beta, lambda
-    const bool resid = (a.mode == FW_FALCON1);                      // r = y - S^T x
+    const bool resid = (a.mode == FW_FALCON1 || a.mode == FW_FALCON2);   // r = y - S^T x
+    const bool chan = (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A);   // beta per column
     const bool shifted = falcon && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
     const TIn *q = static_cast<const TIn *>(a.q) + chain * T * DK;
     const TIn *k = static_cast<const TIn *>(a.k) + chain * T * DK;
     const TIn *v = static_cast<const TIn *>(a.v) + chain * T * DK;
-    const float *beta = falcon ? a.beta + chain * T : nullptr;
+    const float *beta = falcon ? a.beta + chain * T * (chan ? DK : 1) : nullptr;
     const float *lam = falcon ? a.lam + chain * T : nullptr;
     TIn *o = static_cast<TIn *>(a.o) + chain * T * DK;
 
@@ -74,7 +76,7 @@ recurrent_kernel(PrefillArgs a) {
     }
 
     // Register prefetch of the next token's inputs.
-    float nq[RK], nk[RK], nv[kJW], nb = 0.f, nl = 0.f;
+    float nq[RK], nk[RK], nv[kJW], nb[kJW], nl = 0.f;
     auto load = [&](int64_t t) {
 #pragma unroll
         for (int r = 0; r < RK; ++r) {
@@ -83,13 +85,19 @@ recurrent_kernel(PrefillArgs a) {
         }
 #pragma unroll
         for (int c = 0; c < kJW; ++c) nv[c] = to_f32(v[t * DK + col0 + c]);
-        if (falcon) { nb = beta[t]; nl = lam[t]; }
+        if (falcon) {
+#pragma unroll
+            for (int c = 0; c < kJW; ++c) nb[c] = chan ? beta[t * DK + col0 + c] : beta[t];
+            nl = lam[t];
+        }
     };
     if (T > 0) load(0);
 
     for (int64_t t = 0; t < T; ++t) {
-        float qv[RK], kt[RK], vv[kJW];
-        const float bt = nb, lt = nl;
+        float qv[RK], kt[RK], vv[kJW], bt[kJW];
+        const float lt = nl;
+#pragma unroll
+        for (int c = 0; c < kJW; ++c) bt[c] = nb[c];
 #pragma unroll
         for (int r = 0; r < RK; ++r) { qv[r] = nq[r]; kt[r] = apply_phi(a.phi, nk[r]); }
 #pragma unroll
@@ -124,16 +132,17 @@ recurrent_kernel(PrefillArgs a) {
 #pragma unroll
             for (int i = 0; i < NV; ++i) red[i] += __shfl_xor_sync(0xffffffffu, red[i], off);
 
-        float eta = 1.f, gam = 1.f;
-        if (falcon) {
-            const bool pair = !shifted || (t > 0) || have_prev;
-            eta = pair ? bt / (red[2 * kJW] + lt + a.eps) : 0.f;
-            gam = 1.f - eta * lt;
-        }
+        const bool pair = !shifted || (t > 0) || have_prev;
+        const float den = red[2 * kJW] + lt + a.eps;
         const float xq = red[2 * kJW + 1];
         float outv = 0.f;
 #pragma unroll
         for (int c = 0; c < kJW; ++c) {
+            float eta = 1.f, gam = 1.f;
+            if (falcon) {
+                eta = pair ? (chan ? bt[c] : bt[0]) / den : 0.f;
+                gam = 1.f - eta * lt;
+            }
             const float rc = resid ? vv[c] - red[2 * c] : vv[c];
             const float oc = rbw ? red[2 * c + 1] : fmaf(gam, red[2 * c + 1], eta * rc * xq);
             if (lane == c) outv = oc;

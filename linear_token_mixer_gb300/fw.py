@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfw.so")
 
 FW_F32, FW_BF16 = 0, 1
-MODES = {"falcon1": 0, "linattn": 1, "falcon1a": 2}
+MODES = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4}
 FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 PHIS = {"identity": 0, "elu1": 1}
 ALGOS = {"auto": 0, "recurrent": 1, "chunked": 2}
@@ -103,10 +103,11 @@ def prefill(q, k, v, beta=None, lam=None, S0=None, *, mode="falcon1", phi="ident
             same_pair=False):
     """Run the recurrence over q, k, v [B, H, T, d] (fp32 or bf16).
 
-    mode: "falcon1", "falcon1a" or "linattn"; rbw reads before the write,
-    same_pair pairs each key with its own value.  Returns (o [B,H,T,d] in q's
-    dtype, S_T [B,H,d,d] fp32).  beta, lam [B,H,T] fp32 are required in the
-    falcon modes.  S0 [B,H,d,d] fp32 or None."""
+    mode: "falcon1", "falcon1a", "falcon2", "falcon2a" or "linattn"; rbw reads
+    before the write, same_pair pairs each key with its own value.  Returns
+    (o [B,H,T,d] in q's dtype, S_T [B,H,d,d] fp32).  beta, lam [B,H,T] fp32 are
+    required in the falcon modes (beta [B,H,T,d] for falcon2 / falcon2a).  S0
+    [B,H,d,d] fp32 or None."""
     B, H, T, d = q.shape
     if o is None:
         o = torch.empty_like(q)

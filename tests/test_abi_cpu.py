@@ -69,10 +69,11 @@ def call_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init
     (dict(shape=(0, 1, 8, 64, 64)), -2), (dict(shape=(1, 0, 8, 64, 64)), -2),
     (dict(shape=(1, 1, 0, 64, 64)), -2), (dict(shape=(1, 1, 8, 96, 96)), -2),
     (dict(shape=(1, 1, 8, 64, 128)), -2), (dict(shape=(1, 1, 8, 32, 32)), -2),
-    (dict(dtype=7), -3), (dict(mode=3), -5), (dict(phi=9), -5), (dict(algo=5), -5),
+    (dict(dtype=7), -3), (dict(mode=9), -5), (dict(phi=9), -5), (dict(algo=5), -5),
     (dict(flags=4), -5), (dict(flags=0x80000000), -5),
     (dict(mode=2, beta=None), -1), (dict(mode=2, lam=None), -1), (dict(mode=2, eps=-1.0), -9),
-    (dict(mode=2, beta=P[3] + 4), -4),
+    (dict(mode=2, beta=P[3] + 4), -4), (dict(mode=3, beta=None), -1), (dict(mode=4, lam=None), -1),
+    (dict(mode=5), -5), (dict(mode=3, beta=P[3] + 8), -4),
     (dict(q=P[0] + 8), -4), (dict(o=P[5] + 2), -4), (dict(S0=P[7] + 4), -4),
     (dict(k_init=P[8] + 2), -4), (dict(beta=P[3] + 4), -4),
     (dict(eps=-1.0), -9), (dict(eps=float("nan")), -9), (dict(o=P[0]), -9),
@@ -104,6 +105,9 @@ def test_chunked_unsupported_shapes(L):
         assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), flags=flags,
                             algo=2) in (-6, -10)
     assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=2, algo=2) in (-6, -10)
+    # a step per value channel stays on the per-token kernel
+    for mode in (3, 4):
+        assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=mode, algo=2) == -8
 
 
 @no_gpu

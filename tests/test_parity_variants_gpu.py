@@ -172,3 +172,51 @@ def test_falcon1a_workload_full_size_sampled(rbw, same_pair):
     Sg = to64(S.reshape(-1, w.d, w.d)[chains])[None]
     eo, es = rel_l2(og, o_ref), rel_l2(Sg, S_ref)
     assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], (eo, es)
+
+
+# ------------------------------------------------- Falcon-2 / 2A (a step per channel)
+
+def _channel_betas(x, dv, seed=12):
+    g = torch.Generator().manual_seed(seed)
+    lead = tuple(x["beta"].shape)
+    return torch.rand(lead + (dv,), generator=g) * 1.4 + 0.1   # U(0.1, 1.5) per channel
+
+
+@pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
+@pytest.mark.parametrize("rbw,same_pair", [(False, False), (True, True)])
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.bfloat16, 128)])
+def test_falcon2_prefill(mode, rbw, same_pair, dtype, d):
+    w, x = _inputs("falcon1", dtype, d, T=70)
+    x["beta"] = _channel_betas(x, d)
+    g = {k: (t.to(DEV) if t is not None else None) for k, t in x.items()}
+    o, S = fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=mode,
+                      eps=w.eps, rbw=rbw, same_pair=same_pair)   # AUTO: the per-token kernel
+    fw.check()
+    c = {k: t.cpu() for k, t in x.items()}
+    o_ref, S_ref = oracle.falcon2(c["q"], c["k"], c["v"], c["beta"], c["lam"], c["S0"],
+                                  eps=w.eps, inner=(mode == "falcon2a"), rbw=rbw,
+                                  same_pair=same_pair)
+    tol = TOL[dtype]
+    eo, es = rel_l2(to64(o), o_ref), rel_l2(to64(S), S_ref)
+    assert eo <= tol and es <= tol, (eo, es)
+
+
+@pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("rbw", [False, True])
+def test_falcon2_decode(mode, dtype, rbw):
+    steps, Bn, H, d = 4, 3, 2, 128
+    x = I.decode_inputs(steps, Bn, H, d, dtype=dtype, seed=13)
+    gb = torch.Generator().manual_seed(14)
+    beta = torch.rand(steps, Bn, H, d, generator=gb) * 1.4 + 0.1
+    S0 = torch.randn(Bn, H, d, d, generator=torch.Generator().manual_seed(15)) * 0.1
+    Sg = S0.to(DEV)
+    Sr = S0.double().numpy()
+    for s in range(steps):
+        og = fw.step(x["q"][s].to(DEV), x["k_prev"][s].to(DEV), x["v"][s].to(DEV),
+                     beta[s].to(DEV), x["lam"][s].to(DEV), Sg, mode=mode, rbw=rbw)
+        o_r, Sr = oracle.step(x["q"][s], x["k_prev"][s], x["v"][s], beta[s], x["lam"][s], Sr,
+                              mode=mode, rbw=rbw)
+        assert rel_l2(to64(og), o_r) <= TOL[dtype]
+    fw.check()
+    assert rel_l2(to64(Sg), Sr) <= TOL[dtype]
