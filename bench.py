@@ -84,10 +84,12 @@ def stored_traffic(kernel, workload):
 
 def algorithmic_bytes_prefill(w):
     """Bytes a prefill must move: q, k, v read and o written once, beta and
-    lambda read once (Falcon-1), S0 read (when given) and S_T written once."""
+    lambda read once (beta per value channel for Falcon-2), S0 read (when
+    given) and S_T written once."""
     esz = 2 if w.dtype == torch.bfloat16 else 4
     ht = w.B * w.H * w.T
-    per_ht = 4 * w.d * esz + (8 if w.mode == "falcon1" else 0)
+    gates = {"falcon1": 8, "falcon1a": 8, "falcon2": 4 * w.d + 4, "falcon2a": 4 * w.d + 4}
+    per_ht = 4 * w.d * esz + gates.get(w.mode, 0)
     state = w.B * w.H * w.d * w.d * 4
     return ht * per_ht + state * (2 if w.s0_std > 0 else 1)
 
@@ -97,7 +99,7 @@ def matmul_flops_prefill(w, C=64):
     10 C d + 6 d^2 per head-token; linear attention and Falcon-1A (no
     residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y)."""
     ht = w.B * w.H * w.T
-    if w.mode == "falcon1":
+    if w.mode in ("falcon1", "falcon2"):
         return ht * (10 * C * w.d + 6 * w.d * w.d)
     return ht * (4 * C * w.d + 4 * w.d * w.d)
 
@@ -454,9 +456,11 @@ def main():
             out["cpu_baseline"] = cpu_baseline(w)
         if not args.no_extra:
             extra = {}
-            for name in ("linattn_bf16", "falcon1_long", "falcon1_fp32", "falcon1a_bf16"):
+            for name in ("linattn_bf16", "falcon1_long", "falcon1_fp32", "falcon1a_bf16",
+                         "falcon2_bf16"):
                 wn = I.WORKLOADS[name]
-                r, _ = bench_prefill(wn, 5 if name != "falcon1_long" else 3, 3, dev, fw)
+                r, _ = bench_prefill(wn, 5 if name not in ("falcon1_long", "falcon2_bf16") else 3,
+                                     3, dev, fw)
                 r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
                 extra[name] = r
             # the read-before-write / same-step-pair arms on the headline workload

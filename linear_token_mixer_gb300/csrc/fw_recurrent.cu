@@ -30,7 +30,9 @@ namespace {
 constexpr int kJW = 8;     // value columns per warp
 constexpr int kNWarp = 4;  // warps per block -> 32 columns per block
 
-template <int DK, typename TIn>
+// CHAN: Falcon-2 / 2A, a step size per value column (a separate instantiation,
+// so the scalar-step modes keep a single division per token).
+template <int DK, typename TIn, bool CHAN>
 __global__ void __launch_bounds__(kNWarp * 32)
 recurrent_kernel(PrefillArgs a) {
     constexpr int RK = DK / 32;                // key rows per lane: i = lane + 32 r
@@ -42,14 +44,14 @@ recurrent_kernel(PrefillArgs a) {
     const int64_t T = a.T;
     const bool falcon = (a.mode != FW_LINATTN);                     // eta, gamma, beta, lambda
     const bool resid = (a.mode == FW_FALCON1 || a.mode == FW_FALCON2);   // r = y - S^T x
-    const bool chan = (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A);   // beta per column
+    constexpr int NB = CHAN ? kJW : 1;                                  // betas per token
     const bool shifted = falcon && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
     const TIn *q = static_cast<const TIn *>(a.q) + chain * T * DK;
     const TIn *k = static_cast<const TIn *>(a.k) + chain * T * DK;
     const TIn *v = static_cast<const TIn *>(a.v) + chain * T * DK;
-    const float *beta = falcon ? a.beta + chain * T * (chan ? DK : 1) : nullptr;
+    const float *beta = falcon ? a.beta + chain * T * (CHAN ? DK : 1) : nullptr;
     const float *lam = falcon ? a.lam + chain * T : nullptr;
     TIn *o = static_cast<TIn *>(a.o) + chain * T * DK;
 
@@ -76,7 +78,7 @@ recurrent_kernel(PrefillArgs a) {
     }
 
     // Register prefetch of the next token's inputs.
-    float nq[RK], nk[RK], nv[kJW], nb[kJW], nl = 0.f;
+    float nq[RK], nk[RK], nv[kJW], nb[NB], nl = 0.f;
     auto load = [&](int64_t t) {
 #pragma unroll
         for (int r = 0; r < RK; ++r) {
@@ -87,17 +89,17 @@ recurrent_kernel(PrefillArgs a) {
         for (int c = 0; c < kJW; ++c) nv[c] = to_f32(v[t * DK + col0 + c]);
         if (falcon) {
 #pragma unroll
-            for (int c = 0; c < kJW; ++c) nb[c] = chan ? beta[t * DK + col0 + c] : beta[t];
+            for (int c = 0; c < NB; ++c) nb[c] = CHAN ? beta[t * DK + col0 + c] : beta[t];
             nl = lam[t];
         }
     };
     if (T > 0) load(0);
 
     for (int64_t t = 0; t < T; ++t) {
-        float qv[RK], kt[RK], vv[kJW], bt[kJW];
+        float qv[RK], kt[RK], vv[kJW], bt[NB];
         const float lt = nl;
 #pragma unroll
-        for (int c = 0; c < kJW; ++c) bt[c] = nb[c];
+        for (int c = 0; c < NB; ++c) bt[c] = nb[c];
 #pragma unroll
         for (int r = 0; r < RK; ++r) { qv[r] = nq[r]; kt[r] = apply_phi(a.phi, nk[r]); }
 #pragma unroll
@@ -133,14 +135,18 @@ recurrent_kernel(PrefillArgs a) {
             for (int i = 0; i < NV; ++i) red[i] += __shfl_xor_sync(0xffffffffu, red[i], off);
 
         const bool pair = !shifted || (t > 0) || have_prev;
-        const float den = red[2 * kJW] + lt + a.eps;
+        float eta0 = 1.f, gam0 = 1.f;   // one step size per token (Falcon-2: per column below)
+        if (falcon && !CHAN) {
+            eta0 = pair ? bt[0] / (red[2 * kJW] + lt + a.eps) : 0.f;
+            gam0 = 1.f - eta0 * lt;
+        }
         const float xq = red[2 * kJW + 1];
         float outv = 0.f;
 #pragma unroll
         for (int c = 0; c < kJW; ++c) {
-            float eta = 1.f, gam = 1.f;
-            if (falcon) {
-                eta = pair ? (chan ? bt[c] : bt[0]) / den : 0.f;
+            float eta = eta0, gam = gam0;
+            if constexpr (CHAN) {
+                eta = pair ? bt[c] / (red[2 * kJW] + lt + a.eps) : 0.f;
                 gam = 1.f - eta * lt;
             }
             const float rc = resid ? vv[c] - red[2 * c] : vv[c];
@@ -166,7 +172,10 @@ recurrent_kernel(PrefillArgs a) {
 template <int DK, typename TIn>
 cudaError_t launch_t(const PrefillArgs &a, cudaStream_t s) {
     dim3 grid((unsigned)a.n_chains, DK / (kJW * kNWarp));
-    recurrent_kernel<DK, TIn><<<grid, kNWarp * 32, 0, s>>>(a);
+    if (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A)
+        recurrent_kernel<DK, TIn, true><<<grid, kNWarp * 32, 0, s>>>(a);
+    else
+        recurrent_kernel<DK, TIn, false><<<grid, kNWarp * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 

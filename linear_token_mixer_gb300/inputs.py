@@ -71,10 +71,14 @@ WORKLOADS = {
     "falcon1_long": Workload("falcon1_long", "falcon1", "identity", torch.bfloat16,
                              1, 32, 32768, 128, 1.0, "lognormal", (1.5, 1.99), (0.0, 0.01),
                              0.0, seed=20261206),
-    # the inner-product family on the Falcon-1 bf16 shapes and distributions
+    # the inner-product family and the per-channel step on the Falcon-1 bf16
+    # shapes and distributions (beta per value channel for Falcon-2)
     "falcon1a_bf16": Workload("falcon1a_bf16", "falcon1a", "identity", torch.bfloat16,
                               8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
                               seed=20261208),
+    "falcon2_bf16": Workload("falcon2_bf16", "falcon2", "identity", torch.bfloat16,
+                             8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
+                             seed=20261209),
 }
 
 DECODE = dict(batch=256, H=32, d=128, steps=1024, beta=(0.1, 1.0), lam=(0.0, 0.05),
@@ -116,6 +120,9 @@ def prefill_inputs(w: Workload, device="cpu", seed=None):
                S0=None)
     if w.mode in ("falcon1", "falcon1a"):
         out["beta"] = _uniform((w.B, w.H, w.T), *w.beta, g, device)
+        out["lam"] = _uniform((w.B, w.H, w.T), *w.lam, g, device)
+    elif w.mode in ("falcon2", "falcon2a"):   # a step size per value channel
+        out["beta"] = _uniform((w.B, w.H, w.T, w.d), *w.beta, g, device)
         out["lam"] = _uniform((w.B, w.H, w.T), *w.lam, g, device)
     if w.s0_std > 0:
         out["S0"] = torch.randn((w.B, w.H, w.d, w.d), generator=g, device=device,
