@@ -14,7 +14,9 @@ the GPU.
 Pins: every function here is pinned by the CPU tests in
 ``tests/test_oracle_pins.py`` (exact recall, textbook NLMS, ridge fixed point,
 first-token boundary, masked quadratic form of linear attention, orthonormal
-recall, per-step descent, norm bound, hand-worked golden cases).
+recall, per-step descent, norm bound, hand-worked golden cases), the variants
+by ``tests/test_oracle_variants.py`` and the Falcon-3 window by
+``tests/test_oracle_window.py``.
 """
 from __future__ import annotations
 
@@ -32,7 +34,8 @@ _lock = threading.Lock()
 _lib = None
 
 PHI = {"identity": 0, "elu1": 1}
-MODE = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4}
+MODE = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4,
+        "falcon3": 5, "falcon3a": 6}
 FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 
 
@@ -62,7 +65,12 @@ def _load():
             lib.orc_falcon1.argtypes = [L, L, I, I, P, P, P, P, P, P, P, I, D, I, I, P, P, I]
             lib.orc_linattn.argtypes = [L, L, I, I, P, P, P, P, I, I, P, P, I]
             lib.orc_step.argtypes = [L, I, I, I, I, P, P, P, P, P, I, D, P, P, I]
-            for f in (lib.orc_falcon1, lib.orc_linattn, lib.orc_step):
+            lib.orc_falcon3.argtypes = [L, L, I, I, I, P, P, P, P, P, P, P, P, P, P, I, D, I, I,
+                                        P, P, P, P, P, P, I]
+            lib.orc_step3.argtypes = [L, I, I, I, I, I, P, P, P, P, P, I, D, P, P, P, P, P, P,
+                                      P, P, I]
+            for f in (lib.orc_falcon1, lib.orc_linattn, lib.orc_step, lib.orc_falcon3,
+                      lib.orc_step3):
                 f.restype = None
             _lib = lib
     return _lib
@@ -169,3 +177,71 @@ def step(q, k_prev, v, beta, lam, S, mode="falcon1", phi="identity", eps=1e-6,
                      _ptr(lam), PHI[phi], float(eps), _ptr(S), _ptr(o),
                      nthreads or default_threads())
     return o, S
+
+
+def _window_in(win, lead, W, dk, dv):
+    """Carried window (x [..., W-1, dk], y [..., W-1, dv], n [...]) or None."""
+    if win is None or W == 1:
+        return None, None, None
+    cx, cy = _f64(win[0]), _f64(win[1])
+    cn = np.ascontiguousarray(np.asarray(win[2], dtype=np.int32))
+    assert cx.shape == lead + (W - 1, dk) and cy.shape == lead + (W - 1, dv)
+    assert cn.shape == lead and cn.min() >= 0 and cn.max() <= W - 1
+    return cx, cy, cn
+
+
+def falcon3(q, k, v, beta, lam, W, S0=None, k_init=None, win=None, phi="identity", eps=1e-6,
+            nthreads=None, inner=False, rbw=False, same_pair=False, want_mu=False):
+    """Falcon-3 prefill with a window of the last W pairs (inner=True:
+    Falcon-3A).  Shapes as falcon1 (beta, lam [..., T]); win is the window
+    carried from an earlier call, (x [..., W-1, dk] with phi applied,
+    y [..., W-1, dv], n [...] pairs held in the newest slots), or None.
+    Returns (o, S_T, win_out) or, with want_mu, (o, S_T, win_out, mu [..., T])."""
+    q, k, v, beta, lam = map(_f64, (q, k, v, beta, lam))
+    S0, k_init = _f64(S0), _f64(k_init)
+    lead = q.shape[:-2]
+    T, dk = q.shape[-2:]
+    dv = v.shape[-1]
+    nc = int(np.prod(lead)) if lead else 1
+    assert 1 <= W <= 64
+    assert k.shape == q.shape and v.shape == lead + (T, dv)
+    assert beta.shape == lead + (T,) and lam.shape == lead + (T,)
+    cx, cy, cn = _window_in(win, lead, W, dk, dv)
+    o = np.zeros(lead + (T, dv))
+    S = np.zeros(lead + (dk, dv))
+    ox = np.zeros(lead + (W - 1, dk))
+    oy = np.zeros(lead + (W - 1, dv))
+    on = np.zeros(lead, dtype=np.int32)
+    mu = np.zeros(lead + (T,))
+    _load().orc_falcon3(nc, T, dk, dv, W, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam),
+                        _ptr(S0), _ptr(k_init), _ptr(cx), _ptr(cy), _ptr(cn), PHI[phi],
+                        float(eps), MODE["falcon3a" if inner else "falcon3"],
+                        _flags(rbw, same_pair), _ptr(o), _ptr(S), _ptr(ox), _ptr(oy),
+                        _ptr(on), _ptr(mu), nthreads or default_threads())
+    out = (o, S, (ox, oy, on))
+    return out + (mu,) if want_mu else out
+
+
+def step3(q, k_prev, v, beta, lam, S, W, win=None, phi="identity", eps=1e-6, nthreads=None,
+          inner=False, rbw=False):
+    """One Falcon-3 (inner=True: 3A) decode step with a window of W pairs:
+    the carried window win (as falcon3's, or None = empty) plus the new pair
+    (phi(k_prev), v).  q,k_prev [..., dk]; v [..., dv]; beta, lam [...];
+    S [..., dk, dv].  Returns (o, S_new, win_out) as new arrays."""
+    q, k_prev, v, beta, lam = map(_f64, (q, k_prev, v, beta, lam))
+    S = _f64(S).copy()
+    lead = q.shape[:-1]
+    dk = q.shape[-1]
+    dv = v.shape[-1]
+    ns = int(np.prod(lead)) if lead else 1
+    assert 1 <= W <= 64
+    cx, cy, cn = _window_in(win, lead, W, dk, dv)
+    o = np.zeros(lead + (dv,))
+    ox = np.zeros(lead + (W - 1, dk))
+    oy = np.zeros(lead + (W - 1, dv))
+    on = np.zeros(lead, dtype=np.int32)
+    _load().orc_step3(ns, dk, dv, W, MODE["falcon3a" if inner else "falcon3"],
+                      _flags(rbw, False), _ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta),
+                      _ptr(lam), PHI[phi], float(eps), _ptr(S), _ptr(cx), _ptr(cy), _ptr(cn),
+                      _ptr(o), _ptr(ox), _ptr(oy), _ptr(on), nthreads or default_threads())
+    return o, S, (ox, oy, on)
