@@ -19,7 +19,16 @@
  * + eta_t x_t y_t^T, with Falcon-1's step, pairing and boundary.  FW_FALCON2 and
  * FW_FALCON2A take a step size per value channel (§4.2): beta is indexed by the
  * value column j as well, eta_{j,t} = beta_{j,t} / (|x_t|^2 + lambda_t + eps),
- * and column j of S takes its own scalar write.  Flags select
+ * and column j of S takes its own scalar write.  FW_FALCON3 and FW_FALCON3A
+ * (§4.2, §4.3; entry points fw_window_prefill / fw_window_step) write with one
+ * gradient step on the average loss of the last W pairs (the window),
+ *     S_t = (1 - eta_t lambda_t) S_{t-1}
+ *           + (eta_t / B_t) sum_{j in window} x_j (y_j - S_{t-1}^T x_j)^T,
+ *     eta_t = beta_t / (mu_t + lambda_t + eps),
+ *     mu_t = largest eigenvalue of (1/B_t) sum_{j in window} x_j x_j^T,
+ * where the window holds the pairs t-W+1 .. t that exist and B_t counts them
+ * (eta_t = 0 when none does); FW_FALCON3A writes y_j in place of the
+ * residual.  With W = 1 they are FW_FALCON1 and FW_FALCON1A.  Flags select
  * the other arms of the page's read / pairing design (§3.3, §4.1): reading
  * before the write and the same-step pair.  FW_LINATTN selects plain causal linear attention,
  * S_t = S_{t-1} + phi(k_t) v_t^T, o_t = S_t^T phi(q_t) ("Attention is also an
@@ -53,7 +62,7 @@
 extern "C" {
 #endif
 
-#define FW_VERSION 110 /* 1.1.0 */
+#define FW_VERSION 120 /* 1.2.0 */
 
 typedef enum { FW_F32 = 0, FW_BF16 = 1 } fw_dtype;
 
@@ -62,10 +71,28 @@ typedef enum { FW_F32 = 0, FW_BF16 = 1 } fw_dtype;
  * FW_FALCON1A: Falcon-1's pair, step and decay with the additive write
  *              S = gamma S + eta x v^T (no residual).
  * FW_FALCON2, FW_FALCON2A: FW_FALCON1, FW_FALCON1A with a step size (and so a
- *              decay) per value channel; beta carries a trailing d_v index. */
+ *              decay) per value channel; beta carries a trailing d_v index.
+ * FW_FALCON3, FW_FALCON3A: the window modes, taken only by fw_window_prefill
+ *              and fw_window_step (the other calls return FW_ERR_MODE). */
 typedef enum {
-    FW_FALCON1 = 0, FW_LINATTN = 1, FW_FALCON1A = 2, FW_FALCON2 = 3, FW_FALCON2A = 4
+    FW_FALCON1 = 0, FW_LINATTN = 1, FW_FALCON1A = 2, FW_FALCON2 = 3, FW_FALCON2A = 4,
+    FW_FALCON3 = 5, FW_FALCON3A = 6
 } fw_mode;
+
+/* Largest window (number of pairs W) of FW_FALCON3 / FW_FALCON3A. */
+#define FW_WINDOW_MAX 8
+
+/* The pairs that a Falcon-3 window carries from one call to the next: the
+ * newest W-1 training pairs of every chain, which the next token's window
+ * still holds.  Device pointers owned by the caller.  For W = 1 nothing is
+ * carried and the struct is not read. */
+typedef struct {
+    float *x;    /* [B][H][W-1][d_k] the pairs' keys, phi applied, oldest first */
+    float *y;    /* [B][H][W-1][d_v] their targets (values), as fp32 */
+    int32_t *n;  /* [B][H] how many pairs are held, in the newest n slots
+                    (0 .. W-1); the other slots are ignored on input and
+                    written as zeros */
+} fw_window;
 
 /* Flags (bitwise OR) of fw_prefill_ex and fw_step_ex.
  * FW_FLAG_RBW: read before the write, o_t = S_{t-1}^T q_t (every mode).
@@ -97,10 +124,12 @@ typedef struct {
 enum {
     FW_OK = 0,
     FW_ERR_NULL = -1,        /* a required pointer is NULL */
-    FW_ERR_SHAPE = -2,       /* B, H or T < 1, d_k not in {64,128}, d_v != d_k, T != 1 in fw_step */
+    FW_ERR_SHAPE = -2,       /* B, H or T < 1, d_k not in {64,128}, d_v != d_k, T != 1 in a
+                                step, window outside 1 .. FW_WINDOW_MAX */
     FW_ERR_DTYPE = -3,       /* unknown fw_dtype */
     FW_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
-    FW_ERR_MODE = -5,        /* unknown fw_mode, fw_phi or fw_algo */
+    FW_ERR_MODE = -5,        /* unknown fw_mode, fw_phi, fw_algo or flag bit, or a mode
+                                the call does not take */
     FW_ERR_CUDA = -6,        /* a CUDA call failed; see fw_last_cuda_error() */
     FW_ERR_TIMEOUT = -7,     /* a bounded device wait ran out (reported by fw_check) */
     FW_ERR_UNSUPPORTED = -8, /* FW_ALGO_CHUNKED asked for a call it does not support */
@@ -180,6 +209,56 @@ int fw_step(const void *q, const void *k_prev, const void *v, const float *beta,
 int fw_step_ex(const void *q, const void *k_prev, const void *v, const float *beta,
                const float *lambda, float *S, void *o, const fw_shape *shape, fw_dtype dtype,
                fw_mode mode, fw_phi phi, float eps, unsigned flags, cudaStream_t stream);
+
+/*
+ * fw_window_prefill -- FW_FALCON3 / FW_FALCON3A over T tokens for B*H chains,
+ * with a window of `window` pairs (1 .. FW_WINDOW_MAX).
+ *
+ * Passage: "Fast Weight Attention for Continual Learning" paper reading,
+ * §4.2 (Falcon-3, the sliding-window minibatch step) and §4.3 (Falcon-3A);
+ * pairing, boundary and read as fw_prefill (§4.1, §1.4).  The pages give the
+ * window no size and no start-of-sequence rule: the window holds the pairs
+ * that exist (the first token's shifted pair does not, unless k_init is
+ * given), B_t counts them, and a carried window supplies the pairs of an
+ * earlier call.
+ *
+ *   q, k, v, beta, lambda, S0, k_init, o, S_T, eps
+ *            as fw_prefill_ex (beta, lambda float [B][H][T]; phi applies to
+ *            the key only; o must not overlap an input)
+ *   win_in   in   the window carried from an earlier call of the same
+ *                 sequences, or NULL (no pairs before this call)
+ *   win_out  out  the window after token T, or NULL (not wanted); its arrays
+ *                 must not overlap win_in's or any other argument
+ *   window   W, 1 .. FW_WINDOW_MAX (FW_ERR_SHAPE otherwise)
+ *   mode     FW_FALCON3 or FW_FALCON3A (FW_ERR_MODE otherwise)
+ *   flags    FW_FLAG_RBW (read before the write), FW_FLAG_SAME_PAIR (pair
+ *            (phi(k_t), v_t) for every token; k_init unused)
+ * Evaluated by a per-token SIMT kernel in fp32.  Returns FW_OK or FW_ERR_*.
+ */
+int fw_window_prefill(const void *q, const void *k, const void *v, const float *beta,
+                      const float *lambda, const float *S0, const void *k_init,
+                      const fw_window *win_in, void *o, float *S_T, const fw_window *win_out,
+                      const fw_shape *shape, int window, fw_dtype dtype, fw_mode mode,
+                      fw_phi phi, float eps, unsigned flags, cudaStream_t stream);
+
+/*
+ * fw_window_step -- one FW_FALCON3 / FW_FALCON3A decode step for B*H states:
+ * the window is the carried pairs plus the new pair (phi(k_prev), v); S is
+ * updated in place and the carried window moves on by one pair.
+ *
+ * Passage: as fw_window_prefill; the step is the same write for one token.
+ *
+ *   q, k_prev, v, beta, lambda, S, o, eps   as fw_step (beta, lambda [B][H])
+ *   win_in   in   the carried window, or NULL (empty)
+ *   win_out  out  the window after this step, or NULL; it must not overlap
+ *                 win_in (alternate two buffers from step to step)
+ *   window, mode  as fw_window_prefill; flags: FW_FLAG_RBW only
+ *   shape    T must be 1
+ */
+int fw_window_step(const void *q, const void *k_prev, const void *v, const float *beta,
+                   const float *lambda, float *S, const fw_window *win_in, void *o,
+                   const fw_window *win_out, const fw_shape *shape, int window, fw_dtype dtype,
+                   fw_mode mode, fw_phi phi, float eps, unsigned flags, cudaStream_t stream);
 
 /* Synchronise `stream`, then read and clear the device error word.
  * Returns FW_OK, FW_ERR_TIMEOUT, or FW_ERR_CUDA. */

@@ -81,11 +81,47 @@ int check_common(const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi
     if (shape->B * shape->H > (int64_t)INT32_MAX) return FW_ERR_SHAPE;
     if (dtype != FW_F32 && dtype != FW_BF16) return FW_ERR_DTYPE;
     if (mode != FW_FALCON1 && mode != FW_LINATTN && mode != FW_FALCON1A && mode != FW_FALCON2 &&
-        mode != FW_FALCON2A)
+        mode != FW_FALCON2A && mode != FW_FALCON3 && mode != FW_FALCON3A)
         return FW_ERR_MODE;
     if (phi != FW_PHI_IDENTITY && phi != FW_PHI_ELU1) return FW_ERR_MODE;
     if (flags & ~(unsigned)(FW_FLAG_RBW | FW_FLAG_SAME_PAIR)) return FW_ERR_MODE;
     if (gated(mode) && !(std::isfinite(eps) && eps >= 0.f)) return FW_ERR_ARG;
+    return FW_OK;
+}
+
+bool window_mode(fw_mode m) { return m == FW_FALCON3 || m == FW_FALCON3A; }
+
+// Byte extents of a carried window's arrays (x, y, n) for nc chains.
+struct WinExtent {
+    size_t x, y, n;
+};
+WinExtent win_extent(int64_t nc, int W, int d) {
+    return {(size_t)nc * (size_t)(W - 1) * d * sizeof(float),
+            (size_t)nc * (size_t)(W - 1) * d * sizeof(float), (size_t)nc * sizeof(int32_t)};
+}
+
+bool win_overlaps(const fw_window *w, const WinExtent &e, const void *p, size_t n) {
+    return w && (overlaps(w->x, e.x, p, n) || overlaps(w->y, e.y, p, n) ||
+                 overlaps(w->n, e.n, p, n));
+}
+
+// Checks of the window arguments shared by fw_window_prefill and
+// fw_window_step; `in` and `out` may be NULL.
+int check_window(const fw_window *in, const fw_window *out, int W, const WinExtent &e) {
+    if (W < 2) return FW_OK;   // nothing carried
+    for (const fw_window *w : {in, out}) {
+        if (!w) continue;
+        if (!w->x || !w->y || !w->n) return FW_ERR_NULL;
+        if (misaligned(w->x) || misaligned(w->y) || misaligned(w->n)) return FW_ERR_ALIGN;
+    }
+    if (out) {
+        if (overlaps(out->x, e.x, out->y, e.y) || overlaps(out->x, e.x, out->n, e.n) ||
+            overlaps(out->y, e.y, out->n, e.n))
+            return FW_ERR_ARG;
+        if (in && (win_overlaps(in, e, out->x, e.x) || win_overlaps(in, e, out->y, e.y) ||
+                   win_overlaps(in, e, out->n, e.n)))
+            return FW_ERR_ARG;
+    }
     return FW_OK;
 }
 
@@ -101,6 +137,7 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
                              cudaStream_t stream) {
     int st = check_common(shape, dtype, mode, phi, eps, flags);
     if (st != FW_OK) return st;
+    if (window_mode(mode)) return FW_ERR_MODE;   // fw_window_prefill
     if (algo != FW_ALGO_AUTO && algo != FW_ALGO_RECURRENT && algo != FW_ALGO_CHUNKED)
         return FW_ERR_MODE;
     if (!q || !k || !v || !o || !S_T) return FW_ERR_NULL;
@@ -165,6 +202,7 @@ extern "C" int fw_step_ex(const void *q, const void *k_prev, const void *v, cons
                           cudaStream_t stream) {
     int st = check_common(shape, dtype, mode, phi, eps, flags);
     if (st != FW_OK) return st;
+    if (window_mode(mode)) return FW_ERR_MODE;   // fw_window_step
     if (shape->T != 1) return FW_ERR_SHAPE;
     if (!q || !k_prev || !v || !S || !o) return FW_ERR_NULL;
     if (gated(mode) && (!beta || !lambda)) return FW_ERR_NULL;
@@ -203,6 +241,128 @@ extern "C" int fw_step(const void *q, const void *k_prev, const void *v, const f
                        fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
                        cudaStream_t stream) {
     return fw_step_ex(q, k_prev, v, beta, lambda, S, o, shape, dtype, mode, phi, eps, 0u, stream);
+}
+
+extern "C" int fw_window_prefill(const void *q, const void *k, const void *v, const float *beta,
+                                 const float *lambda, const float *S0, const void *k_init,
+                                 const fw_window *win_in, void *o, float *S_T,
+                                 const fw_window *win_out, const fw_shape *shape, int window,
+                                 fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+                                 unsigned flags, cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps, flags);
+    if (st != FW_OK) return st;
+    if (!window_mode(mode)) return FW_ERR_MODE;
+    if (window < 1 || window > FW_WINDOW_MAX) return FW_ERR_SHAPE;
+    if (!q || !k || !v || !o || !S_T || !beta || !lambda) return FW_ERR_NULL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o) || misaligned(S_T) ||
+        misaligned(S0) || misaligned(k_init) || misaligned(beta) || misaligned(lambda))
+        return FW_ERR_ALIGN;
+    const int64_t nc = shape->B * shape->H;
+    const int d = shape->d_k;
+    const WinExtent we = win_extent(nc, window, d);
+    if ((st = check_window(win_in, win_out, window, we)) != FW_OK) return st;
+
+    const size_t esz = dtype == FW_F32 ? 4 : 2;
+    const size_t nx = (size_t)nc * (size_t)shape->T * d * esz;
+    const size_t ns = (size_t)nc * d * d * sizeof(float);
+    const size_t nl = (size_t)nc * (size_t)shape->T * sizeof(float);
+    const size_t nki = (size_t)nc * d * esz;
+    if (overlaps(o, nx, q, nx) || overlaps(o, nx, k, nx) || overlaps(o, nx, v, nx) ||
+        overlaps(o, nx, S0, S0 ? ns : 0) || overlaps(o, nx, S_T, ns) ||
+        overlaps(o, nx, beta, nl) || overlaps(o, nx, lambda, nl) ||
+        overlaps(o, nx, k_init, k_init ? nki : 0))
+        return FW_ERR_ARG;
+    if (overlaps(S_T, ns, q, nx) || overlaps(S_T, ns, k, nx) || overlaps(S_T, ns, v, nx) ||
+        overlaps(S_T, ns, beta, nl) || overlaps(S_T, ns, lambda, nl) ||
+        overlaps(S_T, ns, k_init, k_init ? nki : 0))
+        return FW_ERR_ARG;
+    if (S0 && S0 != S_T && overlaps(S_T, ns, S0, ns)) return FW_ERR_ARG;
+    const bool carry_in = window > 1 && win_in, carry_out = window > 1 && win_out;
+    if (carry_in && (win_overlaps(win_in, we, o, nx) || win_overlaps(win_in, we, S_T, ns)))
+        return FW_ERR_ARG;
+    if (carry_out) {
+        const void *ins[] = {q, k, v, beta, lambda, S0, k_init, o, S_T};
+        const size_t nin[] = {nx, nx, nx, nl, nl, S0 ? ns : 0, k_init ? nki : 0, nx, ns};
+        for (int i = 0; i < 9; ++i)
+            if (win_overlaps(win_out, we, ins[i], nin[i])) return FW_ERR_ARG;
+    }
+
+    WindowArgs a;
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.S0 = S0;
+    a.k_init = (flags & FW_FLAG_SAME_PAIR) ? nullptr : k_init;
+    a.cx = carry_in ? win_in->x : nullptr;
+    a.cy = carry_in ? win_in->y : nullptr;
+    a.cn = carry_in ? win_in->n : nullptr;
+    a.o = o; a.S_T = S_T;
+    a.ox = carry_out ? win_out->x : nullptr;
+    a.oy = carry_out ? win_out->y : nullptr;
+    a.on = carry_out ? win_out->n : nullptr;
+    a.n_chains = nc; a.T = shape->T; a.d = d; a.W = window; a.dtype = dtype;
+    a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+
+    int *err = nullptr;
+    if ((st = device_setup(&err)) != FW_OK) return st;
+    cudaError_t e = launch_window_prefill(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FW_OK;
+}
+
+extern "C" int fw_window_step(const void *q, const void *k_prev, const void *v,
+                              const float *beta, const float *lambda, float *S,
+                              const fw_window *win_in, void *o, const fw_window *win_out,
+                              const fw_shape *shape, int window, fw_dtype dtype, fw_mode mode,
+                              fw_phi phi, float eps, unsigned flags, cudaStream_t stream) {
+    int st = check_common(shape, dtype, mode, phi, eps, flags);
+    if (st != FW_OK) return st;
+    if (!window_mode(mode)) return FW_ERR_MODE;
+    if (flags & ~(unsigned)FW_FLAG_RBW) return FW_ERR_MODE;
+    if (shape->T != 1 || window < 1 || window > FW_WINDOW_MAX) return FW_ERR_SHAPE;
+    if (!q || !k_prev || !v || !S || !o || !beta || !lambda) return FW_ERR_NULL;
+    if (misaligned(q) || misaligned(k_prev) || misaligned(v) || misaligned(S) || misaligned(o) ||
+        misaligned(beta) || misaligned(lambda))
+        return FW_ERR_ALIGN;
+    const int64_t ns = shape->B * shape->H;
+    const int d = shape->d_k;
+    const WinExtent we = win_extent(ns, window, d);
+    if ((st = check_window(win_in, win_out, window, we)) != FW_OK) return st;
+    const size_t esz = dtype == FW_F32 ? 4 : 2;
+    const size_t nx = (size_t)ns * d * esz;
+    const size_t nst = (size_t)ns * d * d * sizeof(float);
+    const size_t nl = (size_t)ns * sizeof(float);
+    const void *ins[] = {q, k_prev, v, beta, lambda};
+    const size_t nin[] = {nx, nx, nx, nl, nl};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(o, nx, ins[i], nin[i]) || overlaps(S, nst, ins[i], nin[i]))
+            return FW_ERR_ARG;
+    if (overlaps(o, nx, S, nst)) return FW_ERR_ARG;
+    const bool carry_in = window > 1 && win_in, carry_out = window > 1 && win_out;
+    if (carry_in && (win_overlaps(win_in, we, o, nx) || win_overlaps(win_in, we, S, nst)))
+        return FW_ERR_ARG;
+    if (carry_out) {
+        for (int i = 0; i < 5; ++i)
+            if (win_overlaps(win_out, we, ins[i], nin[i])) return FW_ERR_ARG;
+        if (win_overlaps(win_out, we, o, nx) || win_overlaps(win_out, we, S, nst))
+            return FW_ERR_ARG;
+    }
+
+    WindowArgs a;
+    a.q = q; a.k = k_prev; a.v = v; a.beta = beta; a.lam = lambda; a.S0 = S;
+    a.k_init = nullptr;
+    a.cx = carry_in ? win_in->x : nullptr;
+    a.cy = carry_in ? win_in->y : nullptr;
+    a.cn = carry_in ? win_in->n : nullptr;
+    a.o = o; a.S_T = S;
+    a.ox = carry_out ? win_out->x : nullptr;
+    a.oy = carry_out ? win_out->y : nullptr;
+    a.on = carry_out ? win_out->n : nullptr;
+    a.n_chains = ns; a.T = 1; a.d = d; a.W = window; a.dtype = dtype;
+    a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+
+    int *err = nullptr;
+    if ((st = device_setup(&err)) != FW_OK) return st;
+    cudaError_t e = launch_window_step(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FW_OK;
 }
 
 extern "C" int fw_check(cudaStream_t stream) {

@@ -46,7 +46,32 @@ struct StepArgs {
     unsigned flags;    // FW_FLAG_* bits
 };
 
+// Arguments of one Falcon-3 / 3A call (prefill, or a step with T = 1 and
+// S0 == S_T == the state), already validated.
+struct WindowArgs {
+    const void *q, *k, *v;
+    const float *beta, *lam, *S0;
+    const void *k_init;           // shifted pair of the first token, or NULL
+    const float *cx, *cy;         // carried window in (NULL: empty)
+    const int *cn;
+    void *o;
+    float *S_T;
+    float *ox, *oy;               // window out (NULL: not wanted)
+    int *on;
+    int64_t n_chains;
+    int64_t T;
+    int d;                        // d_k == d_v
+    int W;                        // window, 1 .. FW_WINDOW_MAX
+    fw_dtype dtype;
+    bool inner;                   // Falcon-3A
+    fw_phi phi;
+    float eps;
+    unsigned flags;
+};
+
 // Launchers (return a cudaError_t from the launch).
+cudaError_t launch_window_prefill(const WindowArgs &a, cudaStream_t s);
+cudaError_t launch_window_step(const WindowArgs &a, cudaStream_t s);
 cudaError_t launch_recurrent(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode(const StepArgs &a, cudaStream_t s);
 // Chunked tensor-core prefill.  supported() tells whether it takes the call.

@@ -15,7 +15,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfw.so")
 
 FW_F32, FW_BF16 = 0, 1
-MODES = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4}
+MODES = {"falcon1": 0, "linattn": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4,
+         "falcon3": 5, "falcon3a": 6}
+WINDOW_MAX = 8
 FLAG_RBW, FLAG_SAME_PAIR = 1, 2
 PHIS = {"identity": 0, "elu1": 1}
 ALGOS = {"auto": 0, "recurrent": 1, "chunked": 2}
@@ -41,7 +43,12 @@ class fw_shape(ctypes.Structure):
                 ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32)]
 
 
-EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_step_ex", "fw_check",
+class fw_window(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("n", ctypes.c_void_p)]
+
+
+EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_step_ex", "fw_window_prefill",
+           "fw_window_step", "fw_check",
            "fw_status_string", "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us",
            "fw_debug_force_timeout")
 
@@ -63,6 +70,10 @@ def lib():
         L.fw_prefill_ex.argtypes = [P, P, P, P, P, P, P, P, P, SP, I, I, I, F, U, I, P]
         L.fw_step.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, P]
         L.fw_step_ex.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, U, P]
+        WP = ctypes.POINTER(fw_window)
+        L.fw_window_prefill.argtypes = [P, P, P, P, P, P, P, WP, P, P, WP, SP, I, I, I, I, F, U,
+                                        P]
+        L.fw_window_step.argtypes = [P, P, P, P, P, P, WP, P, WP, SP, I, I, I, I, F, U, P]
         L.fw_check.argtypes = [P]
         L.fw_status_string.argtypes = [I]
         L.fw_status_string.restype = ctypes.c_char_p
@@ -72,8 +83,8 @@ def lib():
         L.fw_set_wait_limit_us.restype = None
         L.fw_debug_force_timeout.argtypes = [I]
         L.fw_debug_force_timeout.restype = None
-        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_step_ex, L.fw_check,
-                  L.fw_version, L.fw_last_cuda_error):
+        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_step_ex, L.fw_window_prefill,
+                  L.fw_window_step, L.fw_check, L.fw_version, L.fw_last_cuda_error):
             f.restype = I
         _lib = L
     return _lib
@@ -137,6 +148,68 @@ def step(q, k_prev, v, beta, lam, S, *, mode="falcon1", phi="identity", eps=1e-6
     if st != FW_OK:
         raise FwError(st, "fw_step")
     return o
+
+
+def new_window(B, H, d, window, device="cuda"):
+    """An empty carried window (x, y, n) for `window` pairs: x, y
+    [B, H, window-1, d] fp32, n [B, H] int32, all zero."""
+    return (torch.zeros((B, H, window - 1, d), device=device, dtype=torch.float32),
+            torch.zeros((B, H, window - 1, d), device=device, dtype=torch.float32),
+            torch.zeros((B, H), device=device, dtype=torch.int32))
+
+
+def _window(w):
+    if w is None:
+        return None
+    x, y, n = w
+    if n.dtype != torch.int32 or x.dtype != torch.float32 or y.dtype != torch.float32:
+        raise ValueError("fw: a window is (x fp32, y fp32, n int32)")
+    return ctypes.byref(fw_window(_ptr(x), _ptr(y), _ptr(n)))
+
+
+def window_prefill(q, k, v, beta, lam, window, S0=None, *, mode="falcon3", phi="identity",
+                   eps=1e-6, k_init=None, win_in=None, win_out=None, o=None, S_T=None,
+                   stream=None, rbw=False, same_pair=False):
+    """Falcon-3 ("falcon3") or 3A ("falcon3a") over q, k, v [B, H, T, d] with a
+    window of `window` pairs.  win_in: the window carried from an earlier call
+    (as returned here), or None; win_out: tensors to receive the window after
+    the last token (allocated when None).  Returns (o, S_T, win_out)."""
+    B, H, T, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if S_T is None:
+        S_T = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    if win_out is None:
+        win_out = new_window(B, H, d, window, q.device)
+    shp = fw_shape(B, H, T, d, v.shape[-1])
+    st = lib().fw_window_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+                                 _ptr(k_init), _window(win_in), _ptr(o), _ptr(S_T),
+                                 _window(win_out), ctypes.byref(shp), int(window),
+                                 DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi], float(eps),
+                                 _flags(rbw, same_pair), _stream(stream))
+    if st != FW_OK:
+        raise FwError(st, "fw_window_prefill")
+    return o, S_T, win_out
+
+
+def window_step(q, k_prev, v, beta, lam, S, window, win_in=None, win_out=None, *,
+                mode="falcon3", phi="identity", eps=1e-6, o=None, stream=None, rbw=False):
+    """One Falcon-3 / 3A decode step for q, k_prev, v [B, H, d]; S [B, H, d, d]
+    fp32 is updated in place; the window moves from win_in (None: empty) to
+    win_out (allocated when None; must not be win_in).  Returns (o, win_out)."""
+    B, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if win_out is None:
+        win_out = new_window(B, H, d, window, q.device)
+    shp = fw_shape(B, H, 1, d, v.shape[-1])
+    st = lib().fw_window_step(_ptr(q), _ptr(k_prev), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S),
+                              _window(win_in), _ptr(o), _window(win_out), ctypes.byref(shp),
+                              int(window), DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi],
+                              float(eps), _flags(rbw, False), _stream(stream))
+    if st != FW_OK:
+        raise FwError(st, "fw_window_step")
+    return o, win_out
 
 
 def check(stream=None):

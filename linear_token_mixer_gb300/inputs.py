@@ -18,6 +18,9 @@ Workloads (all synthetic; the pages fix no dataset for this path):
   T=32768 d=128; q,v ~ N(0,1); keys = uniform direction times a
   LogNormal(0,1) norm (not normalised); beta ~ U(1.5,1.99);
   lambda ~ U(0,0.01); eps = 1e-6; S0 = 0.
+* ``falcon3_bf16``, ``falcon3a_bf16``  Falcon-3 / 3A with a window of W = 4
+  pairs on the Falcon-1 bf16 shapes and distributions (the pages fix no
+  window size; 4 is a small window of the kind the method is meant for).
 * ``decode``         single-token Falcon-1 decode: 256 sequences x H=32,
   d=128, fp32 state starting at 0, 1024 consecutive steps, each with fresh
   bf16 q, k_prev, v ~ N(0,1), k_prev L2-normalised, beta ~ U(0.1,1),
@@ -39,7 +42,8 @@ import torch
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    mode: str            # "falcon1" | "linattn"
+    mode: str            # "falcon1" | "falcon1a" | "falcon2" | "falcon2a" | "falcon3"
+                         # | "falcon3a" | "linattn"
     phi: str             # "identity" | "elu1"
     dtype: torch.dtype   # dtype of q, k, v, o
     B: int
@@ -53,6 +57,7 @@ class Workload:
     s0_std: float        # 0 -> S0 is None
     eps: float = 1e-6
     seed: int = 0
+    window: int = 1      # Falcon-3 / 3A: pairs in the window
 
     def with_shape(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -79,6 +84,13 @@ WORKLOADS = {
     "falcon2_bf16": Workload("falcon2_bf16", "falcon2", "identity", torch.bfloat16,
                              8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
                              seed=20261209),
+    # the window family: one step on the average loss of the last 4 pairs
+    "falcon3_bf16": Workload("falcon3_bf16", "falcon3", "identity", torch.bfloat16,
+                             8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
+                             seed=20261210, window=4),
+    "falcon3a_bf16": Workload("falcon3a_bf16", "falcon3a", "identity", torch.bfloat16,
+                              8, 16, 4096, 128, 1.0, "unit", (0.1, 1.5), (0.0, 0.1), 0.1,
+                              seed=20261211, window=4),
 }
 
 DECODE = dict(batch=256, H=32, d=128, steps=1024, beta=(0.1, 1.0), lam=(0.0, 0.05),
@@ -118,7 +130,7 @@ def prefill_inputs(w: Workload, device="cpu", seed=None):
     v = (torch.randn(shp, generator=g, device=device, dtype=torch.float32) * w.qkv_scale)
     out = dict(q=q.to(w.dtype), k=k.to(w.dtype), v=v.to(w.dtype), beta=None, lam=None,
                S0=None)
-    if w.mode in ("falcon1", "falcon1a"):
+    if w.mode in ("falcon1", "falcon1a", "falcon3", "falcon3a"):
         out["beta"] = _uniform((w.B, w.H, w.T), *w.beta, g, device)
         out["lam"] = _uniform((w.B, w.H, w.T), *w.lam, g, device)
     elif w.mode in ("falcon2", "falcon2a"):   # a step size per value channel

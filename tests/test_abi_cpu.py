@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.fw_version() == 110
+    assert L.fw_version() == 120
     for code, name in fw.STATUS.items():
         assert L.fw_status_string(code).decode().startswith(name)
     assert L.fw_status_string(12345) == b"unknown status"
@@ -144,3 +144,75 @@ def test_binding_refuses_cpu_tensors(L):
     x = torch.zeros(1, 1, 4, 64)
     with pytest.raises(ValueError):
         fw.prefill(x, x, x, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4))
+
+
+def _win(x, y, n):
+    return ctypes.byref(fw.fw_window(x, y, n))
+
+
+def call_window_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init=None,
+                        win_in=None, o=P[5], S_T=P[6], win_out=None, shape=(1, 1, 8, 64, 64),
+                        window=4, dtype=1, mode=5, phi=0, eps=1e-6, flags=0):
+    shp = fw.fw_shape(*shape)
+    return L.fw_window_prefill(q, k, v, beta, lam, S0, k_init, win_in, o, S_T, win_out,
+                               ctypes.byref(shp), window, dtype, mode, phi, eps, flags, None)
+
+
+W_IN = (P[7], P[8], P[9])
+W_OUT = (P[10], P[11], P[11] + 0x80000)
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=0), -5), (dict(mode=1), -5), (dict(mode=3), -5), (dict(mode=7), -5),
+    (dict(window=0), -2), (dict(window=9), -2), (dict(flags=4), -5),
+    (dict(beta=None), -1), (dict(lam=None), -1), (dict(q=None), -1), (dict(S_T=None), -1),
+    (dict(eps=-1.0), -9), (dict(q=P[0] + 8), -4), (dict(k_init=P[8] + 2), -4),
+    (dict(o=P[1]), -9), (dict(S_T=P[0]), -9),
+    (dict(win_in=_win(P[7], None, P[9])), -1), (dict(win_out=_win(P[10], P[11], None)), -1),
+    (dict(win_in=_win(P[7] + 4, P[8], P[9])), -4), (dict(win_out=_win(*W_OUT[:2], P[9] + 2)), -4),
+    (dict(win_in=_win(*W_IN), win_out=_win(P[7], P[11], P[10])), -9),    # out overlaps in
+    (dict(win_out=_win(P[0], P[11], P[10])), -9),                         # out overlaps q
+    (dict(win_out=_win(P[10], P[10], P[11])), -9),                        # x and y overlap
+    (dict(win_in=_win(P[5], P[8], P[9])), -9),                            # in overlaps o
+])
+def test_window_prefill_validation(L, kw, code):
+    assert call_window_prefill(L, **kw) == code
+
+
+@no_gpu
+def test_window_prefill_valid_calls_reach_the_device_query(L):
+    for kw in (dict(), dict(mode=6), dict(window=1), dict(window=8), dict(flags=3),
+               dict(win_in=_win(*W_IN), win_out=_win(*W_OUT)),
+               # with a window of one pair nothing is carried: the structs are not read
+               dict(window=1, win_in=_win(None, None, None), win_out=_win(P[0], P[0], P[0]))):
+        assert call_window_prefill(L, **kw) in (-6, -10), kw
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(shape=(1, 1, 2, 64, 64)), -2), (dict(window=0), -2), (dict(window=9), -2),
+    (dict(mode=0), -5), (dict(flags=2), -5), (dict(q=None), -1), (dict(S=None), -1),
+    (dict(beta=None), -1), (dict(S=P[6] + 4), -4), (dict(o=P[0]), -9),
+    (dict(win_in=_win(*W_IN), win_out=_win(*W_IN)), -9),
+    (dict(win_out=_win(P[6], P[11], P[10])), -9),                         # out overlaps S
+])
+def test_window_step_validation(L, kw, code):
+    args = dict(q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S=P[6], win_in=None, o=P[5],
+                win_out=None, shape=(2, 2, 1, 64, 64), window=4, dtype=1, mode=5, phi=0,
+                eps=1e-6, flags=0)
+    args.update(kw)
+    shp = fw.fw_shape(*args.pop("shape"))
+    st = L.fw_window_step(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S"],
+                          args["win_in"], args["o"], args["win_out"], ctypes.byref(shp),
+                          args["window"], args["dtype"], args["mode"], args["phi"], args["eps"],
+                          args["flags"], None)
+    assert st == code
+
+
+@no_gpu
+def test_window_step_valid_call_reaches_the_device_query(L):
+    shp = fw.fw_shape(2, 2, 1, 64, 64)
+    st = L.fw_window_step(P[0], P[1], P[2], P[3], P[4], P[6], _win(*W_IN), P[5], _win(*W_OUT),
+                          ctypes.byref(shp), 4, 1, 6, 0, 1e-6, 1, None)
+    assert st in (-6, -10)
