@@ -299,9 +299,9 @@ extern "C" int fw_window_prefill(const void *q, const void *k, const void *v, co
     a.on = carry_out ? win_out->n : nullptr;
     a.n_chains = nc; a.T = shape->T; a.d = d; a.W = window; a.dtype = dtype;
     a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+    a.wait_ns = g_wait_us.load() * 1000LL;
 
-    int *err = nullptr;
-    if ((st = device_setup(&err)) != FW_OK) return st;
+    if ((st = device_setup(&a.err)) != FW_OK) return st;
     cudaError_t e = launch_window_prefill(a, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return FW_OK;
@@ -357,9 +357,9 @@ extern "C" int fw_window_step(const void *q, const void *k_prev, const void *v,
     a.on = carry_out ? win_out->n : nullptr;
     a.n_chains = ns; a.T = 1; a.d = d; a.W = window; a.dtype = dtype;
     a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+    a.wait_ns = g_wait_us.load() * 1000LL;
 
-    int *err = nullptr;
-    if ((st = device_setup(&err)) != FW_OK) return st;
+    if ((st = device_setup(&a.err)) != FW_OK) return st;
     cudaError_t e = launch_window_step(a, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return FW_OK;

@@ -67,6 +67,8 @@ struct WindowArgs {
     fw_phi phi;
     float eps;
     unsigned flags;
+    int *err;                     // device error word
+    long long wait_ns;            // limit of every bounded device wait, nanoseconds
 };
 
 // Launchers (return a cudaError_t from the launch).

@@ -142,6 +142,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src
         : "memory");
 }
 
+// Untiled bulk copy global -> shared, completing `bytes` of transaction on the
+// mbarrier at `bar` (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Every committed bulk store of this thread has finished reading shared memory.

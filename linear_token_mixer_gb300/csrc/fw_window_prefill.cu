@@ -11,16 +11,17 @@
 // pair that does not exist has x = 0, so it drops out of every sum; B_t
 // counts the ones that do.
 //
-// Work split.  The value columns are independent given the window's keys and
-// step sizes, so a CTA owns 32 columns of one chain and every column is held
-// by four threads, one per quarter of the key rows (the state never leaves
-// registers).  Tokens are staged in blocks: the keys of the block's pairs
-// (plus the W pairs before it), its queries and its targets go to shared
-// memory, and everything that depends on keys alone is formed there for the
-// whole block at once: the dot products x_a . x_b of pairs up to W apart,
-// q_t . x_{t-j}, the window Gram matrices and their largest eigenvalue (one
-// thread per token), eta_t, gamma_t and c_t.  The token loop then only reads
-// the state twice per token.
+// Work split.  One CTA per chain.  The value columns are independent given
+// the window's keys and step sizes, so a compute thread holds two columns
+// over a quarter of the key rows (2 d_k compute threads) and the state never
+// leaves registers.  One more warp, the producer, works a
+// block of tokens ahead: it stages the block's keys (with the W pairs before
+// it), queries and targets (with the same W pairs) in shared memory and
+// forms everything that
+// depends on keys alone -- the dot products x_a . x_b of pairs up to W apart,
+// q_t . x_{t-j}, each token's window Gram matrix and its largest eigenvalue
+// (one lane per token), eta_t, gamma_t and c_t -- into the other of two
+// buffers.  Buffers change hands through mbarriers whose waits are bounded.
 //
 // Residual reads by recursion.  Of the W residual reads S_{t-1}^T x_{t-j}
 // only the newest pair's (j = 0) is a product with the state: for j >= 1 the
@@ -31,42 +32,61 @@
 // where the first term is the previous token's read of the same pair.  The
 // read after the write is expanded the same way,
 //     o_t = S_t^T q_t = gamma_t S_{t-1}^T q_t + sum_j (x_{t-j} . q_t) c_t r_{t,j}.
-// Per token and column this leaves two length-d_k reads and the rank-W write.
-// The call's first token has no previous reads and forms all W.
+// Per token and column this leaves two length-d_k reads and the rank-W write,
+// issued as packed two-wide fp32 FMAs.  Before the call's first token the
+// reads of the pairs already in its window are formed directly (S0^T x), and
+// the recursion starts from them with gamma = 1 and no previous write.
 #include "fw_window.cuh"
+#include "fw_sm100.cuh"
 
 namespace fw {
 namespace {
 
-constexpr int kCG = 32;             // value columns per CTA
-constexpr int kThreads = 4 * kCG;   // four threads (key-row quarters) per column
+using namespace sm100;
+
+constexpr int kNB = 32;   // tokens per staged block (one producer lane each)
 
 template <int DK, int WM>
 struct WinLayout {
-    static constexpr int NB = (WM <= 4) ? 32 : 16;  // tokens per staged block
-    static constexpr int RQ = DK / 4;               // key rows per thread
-    static constexpr int QS = RQ + 4;               // padded quarter: the four
-                                                    // quarters start in different banks
-    static constexpr int LD = 4 * QS;               // padded row
+    static constexpr int NB = kNB;
+    // compute threads: CPT value columns x RPT key rows each; the RG threads
+    // of a column group split the key rows.  Four columns per thread halve
+    // the shared-memory reads per FMA; a window of up to 8 pairs keeps two,
+    // for registers.
+    static constexpr int CPT = WM <= 4 ? 4 : 2;
+    static constexpr int RG = WM <= 4 ? 8 : 4;
+    static constexpr int RPT = DK / RG;
+    static constexpr int NCT = (DK / CPT) * RG;
+    static constexpr int RQ = RPT;                  // key rows per compute thread
+    static constexpr int QS = RQ + 4;               // padded row group: the groups
+                                                    // start in different banks
+    static constexpr int LD = RG * QS;              // padded row
     static constexpr int NXR = NB + WM;             // key rows: pairs p0-WM .. p0+NB-1
-    // offsets in floats
+    // one buffer, offsets in floats
     static constexpr int X = 0;
     static constexpr int Q = X + NXR * LD;
-    static constexpr int DOT = Q + NB * LD;          // [NXR][WM] x_r . x_{r-delta}
-    static constexpr int E = DOT + NXR * WM;         // [NB][WM]  q_t . x_{t-j}
+    static constexpr int V = Q + NB * LD;            // [NXR][DK] targets, rows as X
+    static constexpr int E = V + NXR * DK;           // [NB][WM]  q_t . x_{t-j}
     static constexpr int M = E + NB * WM;            // [NB][WM][WM] recursion weights
     static constexpr int GAM = M + NB * WM * WM;     // [NB] gamma_t
     static constexpr int CC = GAM + NB;              // [NB] c_t = eta_t / B_t
-    static constexpr int BETA = CC + NB;             // [NB]
-    static constexpr int LAM = BETA + NB;            // [NB]
-    static constexpr int V = LAM + NB;               // [NB][kCG] targets of the CTA's columns
-    static constexpr int O = V + NB * kCG;           // [NB][kCG] outputs
-    static constexpr int VAL = O + NB * kCG;         // [NXR] 1 if the pair exists
-    static constexpr int TOTAL = VAL + NXR;
-    static constexpr size_t BYTES = (size_t)TOTAL * sizeof(float);
+    static constexpr int VAL = CC + NB;              // [NXR] 1 if the pair exists
+    static constexpr int BUF = (VAL + NXR + 3) / 4 * 4;
+    // producer scratch and barriers after the two buffers
+    static constexpr int DOT = 2 * BUF;              // [NXR][WM] x_r . x_{r-delta}
+    static constexpr int BL = DOT + NXR * WM;        // [NB][2] beta, lambda
+    static constexpr int BARS = (BL + 2 * NB + 3) / 4 * 4;   // 5 mbarriers
+    // raw input rows as loaded (element type TIn): keys of the block's pairs,
+    // its queries, the targets of its pairs
+    static constexpr int RAW = BARS + 16;
+    template <typename TIn>
+    static constexpr size_t raw_bytes() { return (size_t)(2 * NXR + NB) * DK * sizeof(TIn); }
+    template <typename TIn>
+    static constexpr size_t bytes() { return (size_t)RAW * sizeof(float) + raw_bytes<TIn>(); }
 };
 
-// Position of key element i in a padded row.
+// Position of key element i in a padded row (groups of RQ elements, each
+// followed by four floats of padding).
 template <int RQ>
 __device__ __forceinline__ int padded(int i) {
     return (i / RQ) * (RQ + 4) + (i % RQ);
@@ -82,300 +102,480 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// Dot product of two padded rows (the padding is skipped).
-template <int DK>
-__device__ __forceinline__ float row_dot(const float *u, const float *w) {
-    constexpr int RQ = DK / 4;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-        for (int m = 0; m < RQ; m += 4) {
-            const float4 a = load4(u + qq * (RQ + 4) + m), b = load4(w + qq * (RQ + 4) + m);
-            s0 = fmaf(a.x, b.x, s0); s1 = fmaf(a.y, b.y, s1);
-            s2 = fmaf(a.z, b.z, s2); s3 = fmaf(a.w, b.w, s3);
-        }
-    return (s0 + s1) + (s2 + s3);
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// N consecutive floats (N = 2 or 4, 8- or 16-byte aligned).
+template <int N>
+__device__ __forceinline__ void load_n(const float *p, float (&v)[N]) {
+    if constexpr (N == 4) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    } else {
+        const float2 u = *reinterpret_cast<const float2 *>(p);
+        v[0] = u.x; v[1] = u.y;
+    }
+}
+template <int N>
+__device__ __forceinline__ void store_n(float *p, const float (&v)[N]) {
+    if constexpr (N == 4) *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    else *reinterpret_cast<float2 *>(p) = make_float2(v[0], v[1]);
+}
+template <int N>
+__device__ __forceinline__ void store_n(__nv_bfloat16 *p, const float (&v)[N]) {
+    __nv_bfloat162 *q = reinterpret_cast<__nv_bfloat162 *>(p);
+    q[0] = __floats2bfloat162_rn(v[0], v[1]);
+    if constexpr (N == 4) q[1] = __floats2bfloat162_rn(v[2], v[3]);
 }
 
 template <int DK, int WM, typename TIn, bool INNER>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(WinLayout<DK, WM>::NCT + 32, 1)
 window_prefill_kernel(WindowArgs a) {
     using L = WinLayout<DK, WM>;
     constexpr int NB = L::NB, RQ = L::RQ, QS = L::QS, LD = L::LD, NXR = L::NXR;
+    constexpr int CPT = L::CPT, RG = L::RG, NCT = L::NCT;
+    constexpr int NCW = NCT / 32;        // compute warps
     extern __shared__ __align__(16) float sm[];
-    float *X = sm + L::X, *Qs = sm + L::Q, *DOT = sm + L::DOT, *E = sm + L::E,
-          *Mw = sm + L::M, *GAM = sm + L::GAM, *CC = sm + L::CC, *BETA = sm + L::BETA,
-          *LAM = sm + L::LAM, *V = sm + L::V, *O = sm + L::O, *VAL = sm + L::VAL;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + 2), rawbar = smem_u32(bars + 4);
 
-    const int tid = threadIdx.x, qr = tid & 3, cl = tid >> 2;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int64_t chain = blockIdx.x;
-    const int col0 = blockIdx.y * kCG, col = col0 + cl;
     const int W = a.W;
     const int64_t T = a.T;
-    const bool same = (a.flags & FW_FLAG_SAME_PAIR) != 0;
-    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
-    const TIn *qg = static_cast<const TIn *>(a.q) + chain * T * DK;
-    const TIn *kg = static_cast<const TIn *>(a.k) + chain * T * DK;
-    const TIn *vg = static_cast<const TIn *>(a.v) + chain * T * DK;
-    const TIn *ki = a.k_init ? static_cast<const TIn *>(a.k_init) + chain * DK : nullptr;
-    const float *bg = a.beta + chain * T, *lg = a.lam + chain * T;
-    TIn *og = static_cast<TIn *>(a.o) + chain * T * DK;
+    const int64_t nblk = (T + NB - 1) / NB;
+    const uint64_t limit = (uint64_t)a.wait_ns;
     const int64_t cs = (int64_t)(W - 1) * DK;   // carried window, per chain
-    const float *cx = a.cx ? a.cx + chain * cs : nullptr;
-    const float *cy = a.cy ? a.cy + chain * cs : nullptr;
     int cn = a.cn ? a.cn[chain] : 0;
     cn = cn < 0 ? 0 : (cn > W - 1 ? W - 1 : cn);
 
-    float S[RQ];   // S[qr*RQ + m][col]
-#pragma unroll
-    for (int m = 0; m < RQ; ++m)
-        S[m] = a.S0 ? a.S0[chain * DK * DK + (int64_t)(qr * RQ + m) * DK + col] : 0.f;
-
-    // vr[j]: target of pair p - j; pairs before the call come from the carry
-    // (pair -j sits in slot W-1-j, held if j <= cn)
-    float vr[WM], a_prev[WM], coef_prev[WM];
-#pragma unroll
-    for (int j = 0; j < WM; ++j) {
-        vr[j] = (j >= 1 && j < W && j <= cn && cy) ? cy[(int64_t)(W - 1 - j) * DK + col] : 0.f;
-        a_prev[j] = 0.f;
-        coef_prev[j] = 0.f;
+    if (tid == 0) {
+        mbar_init(full0, 1);
+        mbar_init(full0 + 8, 1);
+        mbar_init(empty0, NCW);
+        mbar_init(empty0 + 8, NCW);
+        mbar_init(rawbar, 1);
+        fence_mbar_init();
     }
+    __syncthreads();
+
+    if (tid >= NCT) {
+        // ================= producer warp =================
+        const bool same = (a.flags & FW_FLAG_SAME_PAIR) != 0;
+        const TIn *qg = static_cast<const TIn *>(a.q) + chain * T * DK;
+        const TIn *kg = static_cast<const TIn *>(a.k) + chain * T * DK;
+        const TIn *vg = static_cast<const TIn *>(a.v) + chain * T * DK;
+        const TIn *ki = a.k_init ? static_cast<const TIn *>(a.k_init) + chain * DK : nullptr;
+        const float *cx = a.cx ? a.cx + chain * cs : nullptr;
+        const float *cy = a.cy ? a.cy + chain * cs : nullptr;
+        float *DOT = sm + L::DOT, *BL = sm + L::BL;
+        constexpr uint32_t ROWB = DK * sizeof(TIn);
+        const int sh = same ? 0 : 1;   // pair m holds key m - sh
+        const TIn *rawK = reinterpret_cast<const TIn *>(sm + L::RAW);
+        const TIn *rawQ = rawK + NXR * DK, *rawV = rawQ + NB * DK;
+        const uint32_t rawK_s = smem_u32(rawK), rawQ_s = smem_u32(rawQ), rawV_s = smem_u32(rawV);
+        // bulk copies of block kb's rows that lie inside the sequence: keys
+        // (row r <-> key p0 - WM - sh + r), queries, targets (row r <-> pair p0 - WM + r)
+        auto issue = [&](int64_t kb) {
+            const int64_t p0 = kb * NB;
+            const int64_t nt = T - p0 < NB ? T - p0 : NB;
+            const int64_t kbase = p0 - WM - sh, vbase = p0 - WM;
+            const int64_t klo = kbase > 0 ? kbase : 0, vlo = vbase > 0 ? vbase : 0;
+            const int64_t khi = p0 + NB - 1 - sh < T - 1 ? p0 + NB - 1 - sh : T - 1;
+            const int64_t vhi = p0 + NB - 1 < T - 1 ? p0 + NB - 1 : T - 1;
+            const uint32_t nk = khi >= klo ? (uint32_t)(khi - klo + 1) : 0u;
+            const uint32_t nv = vhi >= vlo ? (uint32_t)(vhi - vlo + 1) : 0u;
+            mbar_expect_tx(rawbar, (nk + (uint32_t)nt + nv) * ROWB);
+            if (nk) bulk_g2s(rawK_s + (uint32_t)(klo - kbase) * ROWB, kg + klo * DK, nk * ROWB, rawbar);
+            bulk_g2s(rawQ_s, qg + p0 * DK, (uint32_t)nt * ROWB, rawbar);
+            if (nv) bulk_g2s(rawV_s + (uint32_t)(vlo - vbase) * ROWB, vg + vlo * DK, nv * ROWB, rawbar);
+        };
+        if (lane == 0) issue(0);
+        for (int64_t kb = 0; kb < nblk; ++kb) {
+            const int b = (int)(kb & 1);
+            float *X = sm + b * L::BUF + L::X, *Qs = sm + b * L::BUF + L::Q,
+                  *V = sm + b * L::BUF + L::V, *E = sm + b * L::BUF + L::E,
+                  *Mw = sm + b * L::BUF + L::M, *GAM = sm + b * L::BUF + L::GAM,
+                  *CC = sm + b * L::BUF + L::CC, *VAL = sm + b * L::BUF + L::VAL;
+            const int64_t p0 = kb * NB;
+            const int nt = (int)(T - p0 < NB ? T - p0 : NB);
+            const float bt_l = lane < nt ? a.beta[chain * T + p0 + lane] : 0.f;
+            const float lt_l = lane < nt ? a.lam[chain * T + p0 + lane] : 0.f;
+            // this block's raw rows (then no copy is in flight), then its buffer
+            if (!mbar_wait(rawbar, (uint32_t)(kb & 1), limit) ||
+                (kb >= 2 && !mbar_wait(empty0 + 8 * b, (uint32_t)(((kb >> 1) + 1) & 1), limit))) {
+                atomicExch(a.err, kDevErrTimeout);
+                return;
+            }
+            // keys: row r holds pair m = p0 - WM + r, phi applied, 0 if it does not exist
+#pragma unroll 4
+            for (int e = lane; e < NXR * (DK / 4); e += 32) {
+                const int r = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+                const int64_t m = p0 - WM + r;
+                float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+                bool have = false;
+                if (m < 0) {
+                    const int64_t s = m + W - 1;
+                    if (cx && s >= 0 && s >= W - 1 - cn) {
+                        xv = load4(cx + s * DK + i4);
+                        have = true;
+                    }
+                } else if (m < T) {
+                    const TIn *src = m - sh >= 0 ? rawK + r * DK : ki;
+                    if (src) {
+                        xv = load4(src + i4);
+                        xv.x = apply_phi(a.phi, xv.x); xv.y = apply_phi(a.phi, xv.y);
+                        xv.z = apply_phi(a.phi, xv.z); xv.w = apply_phi(a.phi, xv.w);
+                        have = true;
+                    }
+                }
+                *reinterpret_cast<float4 *>(X + r * LD + padded<RQ>(i4)) = xv;
+                if (i4 == 0) VAL[r] = have ? 1.f : 0.f;
+            }
+#pragma unroll 4
+            for (int e = lane; e < NB * (DK / 4); e += 32) {
+                const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+                const float4 qv = t < nt ? load4(rawQ + t * DK + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(Qs + t * LD + padded<RQ>(i4)) = qv;
+            }
+            // targets: row r holds the target of pair m = p0 - WM + r (v_m; the
+            // carried y for m < 0), 0 where the pair does not exist
+#pragma unroll 4
+            for (int e = lane; e < NXR * (DK / 4); e += 32) {
+                const int r = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+                const int64_t m = p0 - WM + r;
+                float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (m < 0) {
+                    const int64_t s = m + W - 1;
+                    if (cy && s >= 0 && s >= W - 1 - cn) vv = load4(cy + s * DK + i4);
+                } else if (m < T) {
+                    vv = load4(rawV + r * DK + i4);
+                }
+                *reinterpret_cast<float4 *>(V + r * DK + i4) = vv;
+            }
+            // the raw rows are read out: prefetch the next block's behind the
+            // rest of this block's work
+            __syncwarp();
+            if (lane == 0 && kb + 1 < nblk) {
+                fence_proxy_async();
+                issue(kb + 1);
+            }
+            BL[2 * lane] = bt_l;
+            BL[2 * lane + 1] = lt_l;
+            // dot products of keys up to W-1 pairs apart (DOT, rows as X) and of
+            // the queries with their window's keys (E): one product per lane at
+            // a time, each lane starting at its own offset along d_k so that the
+            // lanes' loads spread over the banks.  The first WM rows repeat the
+            // previous block's last WM rows: their products are copied.
+            const int r0 = kb == 0 ? 0 : WM;
+            if (kb > 0)
+                for (int e = lane; e < WM * WM; e += 32) DOT[e] = DOT[NB * WM + e];
+            __syncwarp();
+            for (int it = r0 * WM + lane; it < (NXR + NB) * WM; it += 32) {
+                const int r = it / WM, dl = it - r * WM;
+                const float *u = r < NXR ? X + r * LD : Qs + (r - NXR) * LD;
+                const int top = r < NXR ? r : r - NXR + WM;   // row of the newest key paired with u
+                float s = 0.f;   // 0 outside the window: the compute threads sum over WM slots
+                if (dl < W && top - dl >= 0) {
+                    const float *w = X + (top - dl) * LD;
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 8
+                    for (int k = 0; k < DK / 4; ++k) {
+                        const int i = padded<RQ>(((k + lane) & (DK / 4 - 1)) * 4);
+                        const float4 x = load4(u + i), y = load4(w + i);
+                        s0 = fmaf(x.x, y.x, s0); s1 = fmaf(x.y, y.y, s1);
+                        s2 = fmaf(x.z, y.z, s2); s3 = fmaf(x.w, y.w, s3);
+                    }
+                    s = (s0 + s1) + (s2 + s3);
+                }
+                if (r < NXR) DOT[r * WM + dl] = s;
+                else E[(r - NXR) * WM + dl] = s;
+            }
+            __syncwarp();
+            // step size of every token of the block (lane t), and the weights
+            // of the residual-read recursion, M[t][j][j'] = x_{p-1-j'} . x_{p-j}
+            if (lane < nt) {
+                const int t = lane, rr = t + WM;   // row of pair p
+                float G[WM][WM];
+                int nb = 0;
+#pragma unroll
+                for (int i = 0; i < WM; ++i) {
+                    if (i < W && VAL[rr - i] != 0.f) ++nb;
+#pragma unroll
+                    for (int j = 0; j < WM; ++j) {
+                        const int lo = i < j ? i : j, dl = i < j ? j - i : i - j;
+                        G[i][j] = (i < W && j < W) ? DOT[(rr - lo) * WM + dl] : 0.f;
+                    }
+                }
+                const float bt = BL[2 * t], lt = BL[2 * t + 1];
+                float eta = 0.f;
+                if (nb > 0) {
+                    const float mu = window_max_eig<WM>(G) / (float)nb;
+                    eta = bt / (mu + lt + a.eps);
+                }
+                GAM[t] = 1.f - eta * lt;
+                CC[t] = nb > 0 ? eta / (float)nb : 0.f;
+#pragma unroll
+                for (int j = 0; j < WM; ++j)
+#pragma unroll
+                    for (int jp = 0; jp < WM; ++jp) {
+                        float w = 0.f;
+                        if (j >= 1 && j < W && jp < W) {
+                            const int ra = rr - 1 - jp, rb = rr - j;
+                            w = ra > rb ? DOT[ra * WM + (ra - rb)] : DOT[rb * WM + (rb - ra)];
+                        }
+                        Mw[(t * WM + j) * WM + jp] = w;
+                    }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full0 + 8 * b);
+            if (kb == nblk - 1 && a.ox) {
+                // carried window out, keys: pair T-(W-1)+s sits in row T-(W-1)+s-p0+WM
+                for (int e = lane; e < (W - 1) * DK; e += 32) {
+                    const int s = e / DK, i = e % DK;
+                    const int r = (int)(T - (W - 1) + s - p0) + WM;
+                    const bool held = VAL[r] != 0.f;
+                    a.ox[chain * cs + e] = held ? X[r * LD + padded<RQ>(i)] : 0.f;
+                    a.oy[chain * cs + e] = held ? V[r * DK + i] : 0.f;
+                }
+                if (lane == 0) {
+                    int n = 0;
+                    for (int s = 0; s < W - 1; ++s)
+                        n += VAL[(int)(T - (W - 1) + s - p0) + WM] != 0.f;
+                    a.on[chain] = n;
+                }
+            }
+        }
+        return;
+    }
+
+    // ================= compute threads =================
+    // thread = (column group, row group rg): columns c0 .. c0 + CPT - 1, key
+    // rows rg*RQ .. rg*RQ + RQ - 1, held as pairs of rows so that a float4 of
+    // keys feeds two packed FMAs per column
+    const int rg = tid % RG, c0 = (tid / RG) * CPT;
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
+    TIn *og = static_cast<TIn *>(a.o) + chain * T * DK;
+
+    float2 S[CPT][RQ / 2];   // S[c][i] = rows rg*RQ + 2i, 2i + 1 of column c0 + c
+#pragma unroll
+    for (int m = 0; m < RQ; m += 2) {
+        float r0[CPT], r1[CPT];
+        if (a.S0) {
+            const float *s0 = a.S0 + chain * DK * DK + (int64_t)(rg * RQ + m) * DK + c0;
+            load_n<CPT>(s0, r0);
+            load_n<CPT>(s0 + DK, r1);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) r0[c] = r1[c] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) S[c][m / 2] = f2(r0[c], r1[c]);
+    }
+
+    // per column: the previous token's reads of its window's pairs and its
+    // write coefficients
+    float a_prev[CPT][WM], coef_prev[CPT][WM];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int j = 0; j < WM; ++j) {
+            a_prev[c][j] = 0.f;
+            coef_prev[c][j] = 0.f;
+        }
     float gam_prev = 1.f;
 
-    for (int64_t p0 = 0; p0 < T; p0 += NB) {
+    for (int64_t kb = 0; kb < nblk; ++kb) {
+        const int b = (int)(kb & 1);
+        const float *X = sm + b * L::BUF + L::X, *Qs = sm + b * L::BUF + L::Q,
+                    *V = sm + b * L::BUF + L::V, *E = sm + b * L::BUF + L::E,
+                    *Mw = sm + b * L::BUF + L::M, *GAM = sm + b * L::BUF + L::GAM,
+                    *CC = sm + b * L::BUF + L::CC;
+        const int64_t p0 = kb * NB;
         const int nt = (int)(T - p0 < NB ? T - p0 : NB);
-        __syncthreads();   // the previous block is read out
-        // keys: row r holds pair m = p0 - WM + r, phi applied, 0 if it does not exist
-        for (int e = tid; e < NXR * (DK / 4); e += kThreads) {
-            const int r = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
-            const int64_t m = p0 - WM + r;
-            float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-            bool have = false;
-            if (m < 0) {
-                const int64_t s = m + W - 1;
-                if (cx && s >= 0 && s >= W - 1 - cn) {
-                    xv = load4(cx + s * DK + i4);
-                    have = true;
-                }
-            } else if (m < T) {
-                const int64_t kk = same ? m : m - 1;
-                const TIn *src = kk >= 0 ? kg + kk * DK : ki;
-                if (src) {
-                    xv = load4(src + i4);
-                    xv.x = apply_phi(a.phi, xv.x); xv.y = apply_phi(a.phi, xv.y);
-                    xv.z = apply_phi(a.phi, xv.z); xv.w = apply_phi(a.phi, xv.w);
-                    have = true;
-                }
-            }
-            *reinterpret_cast<float4 *>(X + r * LD + padded<RQ>(i4)) = xv;
-            if (i4 == 0) VAL[r] = have ? 1.f : 0.f;
+        if (!mbar_wait(full0 + 8 * b, (uint32_t)((kb >> 1) & 1), limit)) {
+            atomicExch(a.err, kDevErrTimeout);
+            return;
         }
-        for (int e = tid; e < NB * (DK / 4); e += kThreads) {
-            const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
-            const float4 qv = t < nt ? load4(qg + (p0 + t) * DK + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4 *>(Qs + t * LD + padded<RQ>(i4)) = qv;
-        }
-        for (int e = tid; e < NB * kCG; e += kThreads) {
-            const int t = e / kCG, c = e % kCG;
-            V[e] = t < nt ? to_f32(vg[(p0 + t) * DK + col0 + c]) : 0.f;
-        }
-        if (tid < NB) {
-            BETA[tid] = tid < nt ? bg[p0 + tid] : 0.f;
-            LAM[tid] = tid < nt ? lg[p0 + tid] : 0.f;
-        }
-        __syncthreads();
-        // dot products of keys up to W-1 pairs apart, and of queries with the
-        // keys of their window
-        for (int e = tid; e < (NXR + NB) * W; e += kThreads) {
-            const int i = e / W, dl = e % W;
-            if (i < NXR) {
-                DOT[i * WM + dl] = i - dl >= 0 ? row_dot<DK>(X + i * LD, X + (i - dl) * LD) : 0.f;
-            } else {
-                const int t = i - NXR;
-                E[t * WM + dl] = row_dot<DK>(Qs + t * LD, X + (t + WM - dl) * LD);
-            }
-        }
-        __syncthreads();
-        // step size of every token of the block, and the weights of the
-        // residual-read recursion, M[t][j][j'] = x_{p-1-j'} . x_{p-j}
-        if (tid < nt) {
-            const int t = tid, rr = t + WM;   // row of pair p
-            float G[WM][WM];
-            int nb = 0;
+        if (!INNER && kb == 0) {
+            // the first token has no previous reads: form S0^T x of the pairs
+            // before it (rows WM-j), so that the recursion starts from them with
+            // gamma = 1 and no previous write
+            for (int j = 1; j < W; ++j) {
+                const float *xj = X + (WM - j) * LD + rg * QS;
+                float2 acc[CPT];
 #pragma unroll
-            for (int i = 0; i < WM; ++i) {
-                if (i < W && VAL[rr - i] != 0.f) ++nb;
+                for (int c = 0; c < CPT; ++c) acc[c] = f2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < WM; ++j) {
-                    const int lo = i < j ? i : j, dl = i < j ? j - i : i - j;
-                    G[i][j] = (i < W && j < W) ? DOT[(rr - lo) * WM + dl] : 0.f;
-                }
-            }
-            float eta = 0.f;
-            if (nb > 0) {
-                const float mu = window_max_eig<WM>(G) / (float)nb;
-                eta = BETA[t] / (mu + LAM[t] + a.eps);
-            }
-            GAM[t] = 1.f - eta * LAM[t];
-            CC[t] = nb > 0 ? eta / (float)nb : 0.f;
+                for (int m = 0; m < RQ; m += 4) {
+                    const float4 x4 = load4(xj + m);
 #pragma unroll
-            for (int j = 0; j < WM; ++j)
-#pragma unroll
-                for (int jp = 0; jp < WM; ++jp) {
-                    float w = 0.f;
-                    if (j >= 1 && j < W && jp < W) {
-                        const int ra = rr - 1 - jp, rb = rr - j;
-                        w = ra > rb ? DOT[ra * WM + (ra - rb)] : DOT[rb * WM + (rb - ra)];
+                    for (int c = 0; c < CPT; ++c) {
+                        acc[c] = __ffma2_rn(S[c][m / 2], f2(x4.x, x4.y), acc[c]);
+                        acc[c] = __ffma2_rn(S[c][m / 2 + 1], f2(x4.z, x4.w), acc[c]);
                     }
-                    Mw[(t * WM + j) * WM + jp] = w;
                 }
+#pragma unroll
+                for (int c = 0; c < CPT; ++c) {
+                    float r = acc[c].x + acc[c].y;
+#pragma unroll
+                    for (int off = 1; off < RG; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+#pragma unroll
+                    for (int jj = 0; jj < WM; ++jj)
+                        if (jj == j - 1) a_prev[c][jj] = r;
+                }
+            }
         }
-        __syncthreads();
-
         for (int t = 0; t < nt; ++t) {
             const int64_t p = p0 + t;
             const int rr = t + WM;
             const float gam = GAM[t], cc = CC[t];
-            vr[0] = V[t * kCG + cl];
-            const float *xp = X + rr * LD + qr * QS, *qp = Qs + t * LD + qr * QS;
-            float xa[RQ];
-            float pa0 = 0.f, pa1 = 0.f, pc0 = 0.f, pc1 = 0.f;
+            const float *xp = X + rr * LD + rg * QS, *qp = Qs + t * LD + rg * QS;
+            float2 pa[CPT], pc[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) pa[c] = pc[c] = f2(0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < RQ; m += 4) {
-                const float4 x4 = load4(xp + m), q4 = load4(qp + m);
-                xa[m] = x4.x; xa[m + 1] = x4.y; xa[m + 2] = x4.z; xa[m + 3] = x4.w;
-                pa0 = fmaf(S[m], x4.x, pa0); pa1 = fmaf(S[m + 1], x4.y, pa1);
-                pa0 = fmaf(S[m + 2], x4.z, pa0); pa1 = fmaf(S[m + 3], x4.w, pa1);
-                pc0 = fmaf(S[m], q4.x, pc0); pc1 = fmaf(S[m + 1], q4.y, pc1);
-                pc0 = fmaf(S[m + 2], q4.z, pc0); pc1 = fmaf(S[m + 3], q4.w, pc1);
-            }
-            float pa = pa0 + pa1, pc = pc0 + pc1;
-            pa += __shfl_xor_sync(0xffffffffu, pa, 1);
-            pc += __shfl_xor_sync(0xffffffffu, pc, 1);
-            pa += __shfl_xor_sync(0xffffffffu, pa, 2);
-            pc += __shfl_xor_sync(0xffffffffu, pc, 2);
-
-            float aj[WM], coef[WM];
-            if constexpr (!INNER) {
-                aj[0] = pa;
-                if (p == 0) {
-                    // no reads of the previous token: form the older pairs' reads
+                const float4 q4 = load4(qp + m);
+                if constexpr (!INNER) {
+                    const float4 x4 = load4(xp + m);
 #pragma unroll
-                    for (int j = 1; j < WM; ++j) {
-                        float s = 0.f;
-                        if (j < W) {
-                            const float *xj = X + (rr - j) * LD + qr * QS;
-#pragma unroll
-                            for (int m = 0; m < RQ; ++m) s = fmaf(S[m], xj[m], s);
-                            s += __shfl_xor_sync(0xffffffffu, s, 1);
-                            s += __shfl_xor_sync(0xffffffffu, s, 2);
-                        }
-                        aj[j] = s;
+                    for (int c = 0; c < CPT; ++c) {
+                        pa[c] = __ffma2_rn(S[c][m / 2], f2(x4.x, x4.y), pa[c]);
+                        pa[c] = __ffma2_rn(S[c][m / 2 + 1], f2(x4.z, x4.w), pa[c]);
                     }
-                } else {
-                    const float *mt = Mw + t * WM * WM;
+                }
 #pragma unroll
-                    for (int j = 1; j < WM; ++j) {
-                        float s = 0.f;
-                        if (j < W) {
-                            s = gam_prev * a_prev[j - 1];
+                for (int c = 0; c < CPT; ++c) {
+                    pc[c] = __ffma2_rn(S[c][m / 2], f2(q4.x, q4.y), pc[c]);
+                    pc[c] = __ffma2_rn(S[c][m / 2 + 1], f2(q4.z, q4.w), pc[c]);
+                }
+            }
+            // reductions over the row groups: reads of the new pair (ra) and
+            // of the query (rc)
+            float ra[CPT], rc[CPT];
 #pragma unroll
-                            for (int jp = 0; jp < WM; ++jp)
-                                if (jp < W) s = fmaf(mt[j * WM + jp], coef_prev[jp], s);
+            for (int c = 0; c < CPT; ++c) {
+                ra[c] = pa[c].x + pa[c].y;
+                rc[c] = pc[c].x + pc[c].y;
+            }
+#pragma unroll
+            for (int off = 1; off < RG; off <<= 1)
+#pragma unroll
+                for (int c = 0; c < CPT; ++c) {
+                    if constexpr (!INNER) ra[c] += __shfl_xor_sync(0xffffffffu, ra[c], off);
+                    rc[c] += __shfl_xor_sync(0xffffffffu, rc[c], off);
+                }
+
+            // per column: the reads of the older pairs by recursion (descending
+            // j, so that a_prev is replaced in place after its last use), the
+            // residuals and the write coefficients
+            float coef[CPT][WM];
+            {
+                const float *mt = Mw + t * WM * WM;
+#pragma unroll
+                for (int j = WM - 1; j >= 0; --j) {
+                    const bool in = j < W;   // slot j of the window (else coefficient 0)
+                    float y[CPT];            // targets of pair p - j in this thread's columns
+                    load_n<CPT>(V + (rr - j) * DK + c0, y);
+#pragma unroll
+                    for (int c = 0; c < CPT; ++c) {
+                        float aj = 0.f;
+                        if constexpr (!INNER) {
+                            if (j == 0) {
+                                aj = ra[c];
+                            } else {
+                                // M and the previous coefficients are 0 outside the window
+                                aj = gam_prev * a_prev[c][j - 1];
+#pragma unroll
+                                for (int jp = 0; jp < WM; ++jp)
+                                    aj = fmaf(mt[j * WM + jp], coef_prev[c][jp], aj);
+                            }
+                            a_prev[c][j] = in ? aj : 0.f;
                         }
-                        aj[j] = s;
+                        coef[c][j] = in ? cc * (y[c] - aj) : 0.f;
                     }
                 }
             }
-#pragma unroll
-            for (int j = 0; j < WM; ++j)
-                coef[j] = j < W ? cc * (INNER ? vr[j] : vr[j] - aj[j]) : 0.f;
 
-            if (qr == 0) {
-                float ov = pc;   // read before the write
+            if (rg == 0) {
+                float ov[CPT];
+#pragma unroll
+                for (int c = 0; c < CPT; ++c) ov[c] = rc[c];   // read before the write
                 if (!rbw) {
-                    ov = gam * pc;
 #pragma unroll
-                    for (int j = 0; j < WM; ++j)
-                        if (j < W) ov = fmaf(coef[j], E[t * WM + j], ov);
+                    for (int c = 0; c < CPT; ++c) {
+                        ov[c] *= gam;
+#pragma unroll
+                        for (int j = 0; j < WM; ++j) ov[c] = fmaf(coef[c][j], E[t * WM + j], ov[c]);
+                    }
                 }
-                O[t * kCG + cl] = ov;
+                store_n<CPT>(og + p * DK + c0, ov);
             }
             // the write: S = gamma S + sum_j x_{p-j} coef_j
+            {
+                const float2 g2 = f2(gam, gam);
 #pragma unroll
-            for (int m = 0; m < RQ; ++m) S[m] = fmaf(xa[m], coef[0], gam * S[m]);
+                for (int c = 0; c < CPT; ++c)
 #pragma unroll
-            for (int j = 1; j < WM; ++j) {
-                if (j < W) {
-                    const float *xj = X + (rr - j) * LD + qr * QS;
-                    const float cj = coef[j];
+                    for (int i = 0; i < RQ / 2; ++i) S[c][i] = __fmul2_rn(S[c][i], g2);
+                const float *x0 = X + rr * LD + rg * QS;
 #pragma unroll
-                    for (int m = 0; m < RQ; m += 4) {
-                        const float4 x4 = load4(xj + m);
-                        S[m] = fmaf(x4.x, cj, S[m]); S[m + 1] = fmaf(x4.y, cj, S[m + 1]);
-                        S[m + 2] = fmaf(x4.z, cj, S[m + 2]); S[m + 3] = fmaf(x4.w, cj, S[m + 3]);
+                for (int m = 0; m < RQ; m += 4) {
+#pragma unroll
+                    for (int j = 0; j < WM; ++j) {   // slots outside the window add 0
+                        const float4 x4 = load4(x0 - j * LD + m);
+                        const float2 lo = f2(x4.x, x4.y), hi = f2(x4.z, x4.w);
+#pragma unroll
+                        for (int c = 0; c < CPT; ++c) {
+                            const float2 cf = f2(coef[c][j], coef[c][j]);
+                            S[c][m / 2] = __ffma2_rn(lo, cf, S[c][m / 2]);
+                            S[c][m / 2 + 1] = __ffma2_rn(hi, cf, S[c][m / 2 + 1]);
+                        }
                     }
                 }
             }
-            if (p == T - 1 && a.oy && qr == 0) {
-                // carried window out: slot s holds pair T-(W-1)+s = p - (W-2-s)
-                for (int s = 0; s < W - 1; ++s) {
-                    const int j = W - 2 - s;
-                    float y = 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < WM; ++jj)
-                        if (jj == j) y = vr[jj];
-                    a.oy[chain * cs + (int64_t)s * DK + col] = VAL[rr - j] != 0.f ? y : 0.f;
-                }
-            }
+            for (int c = 0; c < CPT; ++c)
 #pragma unroll
-            for (int j = 0; j < WM; ++j) {
-                if constexpr (!INNER) a_prev[j] = aj[j];
-                coef_prev[j] = coef[j];
-            }
+                for (int j = 0; j < WM; ++j) coef_prev[c][j] = coef[c][j];
             gam_prev = gam;
-#pragma unroll
-            for (int j = WM - 1; j >= 1; --j) vr[j] = vr[j - 1];
         }
-        __syncthreads();
-        for (int e = tid; e < nt * kCG; e += kThreads)
-            og[(p0 + e / kCG) * DK + col0 + e % kCG] = from_f32<TIn>(O[e]);
-        if (p0 + NB >= T && blockIdx.y == 0 && a.ox) {
-            // carried window out, keys: pair T-(W-1)+s sits in row T-(W-1)+s-p0+WM
-            for (int e = tid; e < (W - 1) * DK; e += kThreads) {
-                const int s = e / DK, i = e % DK;
-                const int r = (int)(T - (W - 1) + s - p0) + WM;
-                a.ox[chain * cs + e] = VAL[r] != 0.f ? X[r * LD + padded<RQ>(i)] : 0.f;
-            }
-            if (tid == 0) {
-                int n = 0;
-                for (int s = 0; s < W - 1; ++s) n += VAL[(int)(T - (W - 1) + s - p0) + WM] != 0.f;
-                a.on[chain] = n;
-            }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * b);
     }
 
 #pragma unroll
-    for (int m = 0; m < RQ; ++m)
-        a.S_T[chain * DK * DK + (int64_t)(qr * RQ + m) * DK + col] = S[m];
+    for (int m = 0; m < RQ; m += 2) {
+        float r0[CPT], r1[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            r0[c] = S[c][m / 2].x;
+            r1[c] = S[c][m / 2].y;
+        }
+        float *s0 = a.S_T + chain * DK * DK + (int64_t)(rg * RQ + m) * DK + c0;
+        store_n<CPT>(s0, r0);
+        store_n<CPT>(s0 + DK, r1);
+    }
 }
 
 template <int DK, int WM, typename TIn, bool INNER>
 cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
     auto kern = window_prefill_kernel<DK, WM, TIn, INNER>;
-    constexpr size_t bytes = WinLayout<DK, WM>::BYTES;
-    static_assert(bytes <= 56 * 1024, "four CTAs per SM");
+    constexpr size_t bytes = WinLayout<DK, WM>::template bytes<TIn>();
+    static_assert(bytes <= 227 * 1024, "shared memory of one CTA");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)a.n_chains, DK / kCG);
-    kern<<<grid, kThreads, bytes, s>>>(a);
+    kern<<<(unsigned)a.n_chains, WinLayout<DK, WM>::NCT + 32, bytes, s>>>(a);
     return cudaGetLastError();
 }
 
+// The window's slots are compile-time (WM = 2, 4 or 8 >= W); slots past W
+// carry zero coefficients.
 template <int DK, typename TIn>
 cudaError_t launch_d(const WindowArgs &a, cudaStream_t s) {
+    if (a.W <= 2)
+        return a.inner ? launch_t<DK, 2, TIn, true>(a, s) : launch_t<DK, 2, TIn, false>(a, s);
     if (a.W <= 4)
         return a.inner ? launch_t<DK, 4, TIn, true>(a, s) : launch_t<DK, 4, TIn, false>(a, s);
     return a.inner ? launch_t<DK, 8, TIn, true>(a, s) : launch_t<DK, 8, TIn, false>(a, s);
