@@ -44,7 +44,9 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kNB = 32;   // tokens per staged block (one producer lane each)
+constexpr int kNB = 32;          // tokens per staged block
+constexpr int kProducers = 128;  // producer threads (four warps, one per SM sub-partition)
+constexpr int kBarProd = 1;      // named barrier of the producer warps
 
 template <int DK, int WM>
 struct WinLayout {
@@ -128,12 +130,13 @@ __device__ __forceinline__ void store_n(__nv_bfloat16 *p, const float (&v)[N]) {
 }
 
 template <int DK, int WM, typename TIn, bool INNER>
-__global__ void __launch_bounds__(WinLayout<DK, WM>::NCT + 32, 1)
+__global__ void __launch_bounds__(WinLayout<DK, WM>::NCT + kProducers, 1)
 window_prefill_kernel(WindowArgs a) {
     using L = WinLayout<DK, WM>;
     constexpr int NB = L::NB, RQ = L::RQ, QS = L::QS, LD = L::LD, NXR = L::NXR;
     constexpr int CPT = L::CPT, RG = L::RG, NCT = L::NCT;
     constexpr int NCW = NCT / 32;        // compute warps
+    constexpr int NPT = kProducers;      // producer threads
     extern __shared__ __align__(16) float sm[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + 2), rawbar = smem_u32(bars + 4);
@@ -159,7 +162,8 @@ window_prefill_kernel(WindowArgs a) {
     __syncthreads();
 
     if (tid >= NCT) {
-        // ================= producer warp =================
+        // ================= producer warps =================
+        const int pt = tid - NCT;   // producer thread 0 .. NPT-1
         const bool same = (a.flags & FW_FLAG_SAME_PAIR) != 0;
         const TIn *qg = static_cast<const TIn *>(a.q) + chain * T * DK;
         const TIn *kg = static_cast<const TIn *>(a.k) + chain * T * DK;
@@ -189,7 +193,7 @@ window_prefill_kernel(WindowArgs a) {
             bulk_g2s(rawQ_s, qg + p0 * DK, (uint32_t)nt * ROWB, rawbar);
             if (nv) bulk_g2s(rawV_s + (uint32_t)(vlo - vbase) * ROWB, vg + vlo * DK, nv * ROWB, rawbar);
         };
-        if (lane == 0) issue(0);
+        if (pt == 0) issue(0);
         for (int64_t kb = 0; kb < nblk; ++kb) {
             const int b = (int)(kb & 1);
             float *X = sm + b * L::BUF + L::X, *Qs = sm + b * L::BUF + L::Q,
@@ -198,17 +202,20 @@ window_prefill_kernel(WindowArgs a) {
                   *CC = sm + b * L::BUF + L::CC, *VAL = sm + b * L::BUF + L::VAL;
             const int64_t p0 = kb * NB;
             const int nt = (int)(T - p0 < NB ? T - p0 : NB);
-            const float bt_l = lane < nt ? a.beta[chain * T + p0 + lane] : 0.f;
-            const float lt_l = lane < nt ? a.lam[chain * T + p0 + lane] : 0.f;
-            // this block's raw rows (then no copy is in flight), then its buffer
-            if (!mbar_wait(rawbar, (uint32_t)(kb & 1), limit) ||
-                (kb >= 2 && !mbar_wait(empty0 + 8 * b, (uint32_t)(((kb >> 1) + 1) & 1), limit))) {
-                atomicExch(a.err, kDevErrTimeout);
+            const float bt_l = pt < nt ? a.beta[chain * T + p0 + pt] : 0.f;
+            const float lt_l = pt < nt ? a.lam[chain * T + p0 + pt] : 0.f;
+            // this block's raw rows (then no copy is in flight), then its
+            // buffer; the producer warps agree on the outcome before leaving
+            const bool late = !mbar_wait(rawbar, (uint32_t)(kb & 1), limit) ||
+                              (kb >= 2 && !mbar_wait(empty0 + 8 * b,
+                                                     (uint32_t)(((kb >> 1) + 1) & 1), limit));
+            if (bar_or(kBarProd, NPT, late)) {
+                if (pt == 0) atomicExch(a.err, kDevErrTimeout);
                 return;
             }
             // keys: row r holds pair m = p0 - WM + r, phi applied, 0 if it does not exist
 #pragma unroll 4
-            for (int e = lane; e < NXR * (DK / 4); e += 32) {
+            for (int e = pt; e < NXR * (DK / 4); e += NPT) {
                 const int r = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
                 const int64_t m = p0 - WM + r;
                 float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -232,7 +239,7 @@ window_prefill_kernel(WindowArgs a) {
                 if (i4 == 0) VAL[r] = have ? 1.f : 0.f;
             }
 #pragma unroll 4
-            for (int e = lane; e < NB * (DK / 4); e += 32) {
+            for (int e = pt; e < NB * (DK / 4); e += NPT) {
                 const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
                 const float4 qv = t < nt ? load4(rawQ + t * DK + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
                 *reinterpret_cast<float4 *>(Qs + t * LD + padded<RQ>(i4)) = qv;
@@ -240,7 +247,7 @@ window_prefill_kernel(WindowArgs a) {
             // targets: row r holds the target of pair m = p0 - WM + r (v_m; the
             // carried y for m < 0), 0 where the pair does not exist
 #pragma unroll 4
-            for (int e = lane; e < NXR * (DK / 4); e += 32) {
+            for (int e = pt; e < NXR * (DK / 4); e += NPT) {
                 const int r = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
                 const int64_t m = p0 - WM + r;
                 float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -252,25 +259,28 @@ window_prefill_kernel(WindowArgs a) {
                 }
                 *reinterpret_cast<float4 *>(V + r * DK + i4) = vv;
             }
+            if (pt < NB) {
+                BL[2 * pt] = bt_l;
+                BL[2 * pt + 1] = lt_l;
+            }
             // the raw rows are read out: prefetch the next block's behind the
             // rest of this block's work
-            __syncwarp();
-            if (lane == 0 && kb + 1 < nblk) {
+            bar_sync(kBarProd, NPT);
+            if (pt == 0 && kb + 1 < nblk) {
                 fence_proxy_async();
                 issue(kb + 1);
             }
-            BL[2 * lane] = bt_l;
-            BL[2 * lane + 1] = lt_l;
             // dot products of keys up to W-1 pairs apart (DOT, rows as X) and of
             // the queries with their window's keys (E): one product per lane at
             // a time, each lane starting at its own offset along d_k so that the
             // lanes' loads spread over the banks.  The first WM rows repeat the
             // previous block's last WM rows: their products are copied.
             const int r0 = kb == 0 ? 0 : WM;
-            if (kb > 0)
-                for (int e = lane; e < WM * WM; e += 32) DOT[e] = DOT[NB * WM + e];
-            __syncwarp();
-            for (int it = r0 * WM + lane; it < (NXR + NB) * WM; it += 32) {
+            if (kb > 0) {
+                for (int e = pt; e < WM * WM; e += NPT) DOT[e] = DOT[NB * WM + e];
+                bar_sync(kBarProd, NPT);
+            }
+            for (int it = r0 * WM + pt; it < (NXR + NB) * WM; it += NPT) {
                 const int r = it / WM, dl = it - r * WM;
                 const float *u = r < NXR ? X + r * LD : Qs + (r - NXR) * LD;
                 const int top = r < NXR ? r : r - NXR + WM;   // row of the newest key paired with u
@@ -280,7 +290,7 @@ window_prefill_kernel(WindowArgs a) {
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll 8
                     for (int k = 0; k < DK / 4; ++k) {
-                        const int i = padded<RQ>(((k + lane) & (DK / 4 - 1)) * 4);
+                        const int i = padded<RQ>(((k + pt) & (DK / 4 - 1)) * 4);
                         const float4 x = load4(u + i), y = load4(w + i);
                         s0 = fmaf(x.x, y.x, s0); s1 = fmaf(x.y, y.y, s1);
                         s2 = fmaf(x.z, y.z, s2); s3 = fmaf(x.w, y.w, s3);
@@ -290,11 +300,12 @@ window_prefill_kernel(WindowArgs a) {
                 if (r < NXR) DOT[r * WM + dl] = s;
                 else E[(r - NXR) * WM + dl] = s;
             }
-            __syncwarp();
-            // step size of every token of the block (lane t), and the weights
-            // of the residual-read recursion, M[t][j][j'] = x_{p-1-j'} . x_{p-j}
-            if (lane < nt) {
-                const int t = lane, rr = t + WM;   // row of pair p
+            bar_sync(kBarProd, NPT);
+            // step size of every token of the block (one in every four producer
+            // threads: eight per warp), and the weights of the residual-read
+            // recursion, M[t][j][j'] = x_{p-1-j'} . x_{p-j}
+            if ((pt & 3) == 0 && (pt >> 2) < nt) {
+                const int t = pt >> 2, rr = t + WM;   // row of pair p
                 float G[WM][WM];
                 int nb = 0;
 #pragma unroll
@@ -326,18 +337,18 @@ window_prefill_kernel(WindowArgs a) {
                         Mw[(t * WM + j) * WM + jp] = w;
                     }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full0 + 8 * b);
+            bar_sync(kBarProd, NPT);
+            if (pt == 0) mbar_arrive(full0 + 8 * b);
             if (kb == nblk - 1 && a.ox) {
                 // carried window out, keys: pair T-(W-1)+s sits in row T-(W-1)+s-p0+WM
-                for (int e = lane; e < (W - 1) * DK; e += 32) {
+                for (int e = pt; e < (W - 1) * DK; e += NPT) {
                     const int s = e / DK, i = e % DK;
                     const int r = (int)(T - (W - 1) + s - p0) + WM;
                     const bool held = VAL[r] != 0.f;
                     a.ox[chain * cs + e] = held ? X[r * LD + padded<RQ>(i)] : 0.f;
                     a.oy[chain * cs + e] = held ? V[r * DK + i] : 0.f;
                 }
-                if (lane == 0) {
+                if (pt == 0) {
                     int n = 0;
                     for (int s = 0; s < W - 1; ++s)
                         n += VAL[(int)(T - (W - 1) + s - p0) + WM] != 0.f;
@@ -566,7 +577,7 @@ cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)a.n_chains, WinLayout<DK, WM>::NCT + 32, bytes, s>>>(a);
+    kern<<<(unsigned)a.n_chains, WinLayout<DK, WM>::NCT + kProducers, bytes, s>>>(a);
     return cudaGetLastError();
 }
 
