@@ -53,6 +53,8 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 KERNEL_SOURCES = {
     "chunked prefill": ("fw_chunked.cu", "fw_sm100.cuh", "fw_internal.cuh"),
     "recurrent (SIMT)": ("fw_recurrent.cu", "fw_internal.cuh"),
+    "window prefill (SIMT)": ("fw_window_prefill.cu", "fw_window.cuh", "fw_sm100.cuh",
+                              "fw_internal.cuh"),
 }
 
 
@@ -102,6 +104,15 @@ def matmul_flops_prefill(w, C=64):
     if w.mode in ("falcon1", "falcon2"):
         return ht * (10 * C * w.d + 6 * w.d * w.d)
     return ht * (4 * C * w.d + 4 * w.d * w.d)
+
+
+def window_flops(w):
+    """Flops of the Falcon-3 / 3A write by its definition, per head-token:
+    W residual reads S^T x_j (Falcon-3 only), the rank-W write and the decay,
+    and the read S^T q -- (2W + 2) d^2 multiply-adds (3A: W + 2), 2 flops each.
+    The kernel forms the older pairs' reads by recursion, so it executes fewer."""
+    reads = 0 if w.mode == "falcon3a" else w.window
+    return w.B * w.H * w.T * 2 * (reads + w.window + 2) * w.d * w.d
 
 
 def recurrence_flops(w):
@@ -223,6 +234,63 @@ def bench_prefill(w, K, W, dev, fw, algo="auto", rbw=False, same_pair=False):
     if rbw or same_pair:
         res["flags"] = [f for f, on in (("rbw", rbw), ("same_pair", same_pair)) if on]
     return res, x
+
+
+def bench_window(w, K, W, dev, fw):
+    """Falcon-3 / 3A prefill through fw_window_prefill (window of w.window pairs)."""
+    x = I.prefill_inputs(w, device=dev)
+    o = torch.empty_like(x["q"])
+    S_T = torch.empty(w.B, w.H, w.d, w.d, device=dev)
+    win = fw.new_window(w.B, w.H, w.d, w.window, dev)
+    stream = torch.cuda.current_stream()
+
+    def fn():
+        fw.window_prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], w.window, x["S0"],
+                          mode=w.mode, phi=w.phi, eps=w.eps, o=o, S_T=S_T, win_out=win,
+                          stream=stream)
+
+    total, per = timed(fn, K, W, stream)
+    fw.check(stream)
+    kern_ms = statistics.mean(per)
+    tf = window_flops(w) / (kern_ms / 1e3) / 1e12
+    toks = w.B * w.T
+    return {"tokens_per_s": toks * K / (total / 1e3), "ms_per_step": total / K,
+            "kernel_ms": kern_ms, "window": w.window,
+            "hbm_gbs": algorithmic_bytes_prefill(w) / (kern_ms / 1e3) / 1e9,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS,
+                         "unit": "TFLOP/s", "frac": tf / ALU_FP32_TFLOPS,
+                         "kernel": "window prefill (SIMT)",
+                         "traffic": stored_traffic("window prefill (SIMT)", w.name),
+                         "flops": "(2W+2) d^2 multiply-adds per head-token (3A: W+2)"}}
+
+
+def bench_window_step(K_steps, W, dev, fw, window=4, mode="falcon3"):
+    """Falcon-3 / 3A decode steps on the decode workload's states, alternating
+    two carried windows."""
+    cfg = I.DECODE
+    Bn, H, d = cfg["batch"], cfg["H"], cfg["d"]
+    x = I.decode_inputs(K_steps, Bn, H, d, device=dev)
+    S = torch.zeros(Bn, H, d, d, device=dev)
+    o = torch.empty(Bn, H, d, device=dev, dtype=torch.bfloat16)
+    wins = [fw.new_window(Bn, H, d, window, dev), fw.new_window(Bn, H, d, window, dev)]
+    stream = torch.cuda.current_stream()
+    i = [0]
+
+    def fn():
+        s = i[0] % K_steps
+        fw.window_step(x["q"][s], x["k_prev"][s], x["v"][s], x["beta"][s], x["lam"][s], S,
+                       window, win_in=wins[i[0] & 1], win_out=wins[(i[0] + 1) & 1], mode=mode,
+                       eps=cfg["eps"], o=o, stream=stream)
+        i[0] += 1
+
+    total, per = timed(fn, K_steps, W, stream)
+    fw.check(stream)
+    kern_ms = statistics.mean(per)
+    # state read and written, carried window read and written, step vectors
+    nbytes = Bn * H * (2 * d * d * 4 + 2 * (window - 1) * 2 * d * 4 + 4 * d * 2 + 8 + 8)
+    return {"steps_per_s": K_steps / (total / 1e3), "tokens_per_s": Bn * K_steps / (total / 1e3),
+            "kernel_ms": kern_ms, "hbm_gbs": nbytes / (kern_ms / 1e3) / 1e9,
+            "bytes_per_step": nbytes, "steps": K_steps, "window": window, "mode": mode}
 
 
 def e2e_prefill(w, K, W, dev, fw, x_dev):
@@ -470,6 +538,13 @@ def main():
             dec = bench_decode(I.DECODE["steps"], 3, dev, fw)
             dec["hbm_frac"] = dec["hbm_gbs"] / peaks["hbm"]
             extra["decode"] = dec
+            # the window family (Falcon-3 / 3A, W = 4): prefill and decode step
+            for name in ("falcon3_bf16", "falcon3a_bf16"):
+                extra[name] = bench_window(I.WORKLOADS[name], 3, 3, dev, fw)
+            for mode in ("falcon3", "falcon3a"):
+                ds = bench_window_step(256, 3, dev, fw, window=4, mode=mode)
+                ds["hbm_frac"] = ds["hbm_gbs"] / peaks["hbm"]
+                extra["decode_%s_w4" % mode] = ds
             out["workloads"] = extra
         print(json.dumps(out), flush=True)
     if dist:

@@ -34,11 +34,16 @@ __device__ __forceinline__ float window_max_eig(float (&A)[WM][WM]) {
             for (int q = p + 1; q < WM; ++q) {
                 const float apq = A[p][q];
                 if (apq != 0.f) {
-                    const float tau = (A[q][q] - A[p][p]) / (2.f * apq);
-                    // tau * tau overflowing gives t = 0: a_pq is negligible
-                    const float t =
-                        copysignf(1.f, tau) / (fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f)));
-                    const float c = 1.f / sqrtf(fmaf(t, t, 1.f)), s = t * c;
+                    // fast reciprocal square root and division (a few ulp): the
+                    // rotations stay orthogonal to a few ulp, far inside the
+                    // eigenvalue accuracy the step needs
+                    const float tau = __fdividef(A[q][q] - A[p][p], 2.f * apq);
+                    const float at = fabsf(tau), r = fmaf(tau, tau, 1.f);
+                    // for |tau| beyond 1e18, t = 1 / (2 tau) to fp32 precision (and
+                    // tau * tau would overflow)
+                    const float t = at > 1e18f ? __fdividef(0.5f, tau)
+                                               : copysignf(__fdividef(1.f, at + r * rsqrtf(r)), tau);
+                    const float c = rsqrtf(fmaf(t, t, 1.f)), s = t * c;
 #pragma unroll
                     for (int k = 0; k < WM; ++k) {
                         if (k == p || k == q) continue;
