@@ -411,7 +411,9 @@ window_prefill_kernel(WindowArgs a) {
             // the first token has no previous reads: form S0^T x of the pairs
             // before it (rows WM-j), so that the recursion starts from them with
             // gamma = 1 and no previous write
-            for (int j = 1; j < W; ++j) {
+#pragma unroll
+            for (int j = 1; j < WM; ++j) {
+                if (j >= W) continue;   // (compile-time j keeps a_prev in registers)
                 const float *xj = X + (WM - j) * LD + rg * QS;
                 float2 acc[CPT];
 #pragma unroll
@@ -430,9 +432,7 @@ window_prefill_kernel(WindowArgs a) {
                     float r = acc[c].x + acc[c].y;
 #pragma unroll
                     for (int off = 1; off < RG; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-#pragma unroll
-                    for (int jj = 0; jj < WM; ++jj)
-                        if (jj == j - 1) a_prev[c][jj] = r;
+                    a_prev[c][j - 1] = r;
                 }
             }
         }

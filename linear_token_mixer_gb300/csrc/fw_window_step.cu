@@ -100,7 +100,22 @@ window_step_kernel(WindowArgs a) {
         }
     }
 
-    // reads of the old state: a_j = S^T x_j (partial over this thread's rows), c = S^T q
+    __syncthreads();   // Gram matrix complete
+    // mu, eta, gamma while the state's loads are still in flight
+    if (tid == 0) {
+        float A[WM][WM];
+#pragma unroll
+        for (int i = 0; i < WM; ++i)
+#pragma unroll
+            for (int j = 0; j < WM; ++j) A[i][j] = (i < W && j < W) ? G[i][j] : 0.f;
+        const int nb = cn + 1;   // the carried pairs held, and the new one
+        const float mu = window_max_eig<WM>(A) / (float)nb;
+        const float lt = a.lam[s];
+        const float eta = a.beta[s] / (mu + lt + a.eps);
+        scal[0] = 1.f - eta * lt;
+        scal[1] = eta / (float)nb;
+    }
+    // reads of the old state (the loads have landed by now)
     float4 pa[WM];
     float4 pc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -128,22 +143,8 @@ window_step_kernel(WindowArgs a) {
         for (int j = 0; j < WM; ++j)
             if (j < W) red[rg][j][cq] = pa[j];
     }
-    __syncthreads();   // Gram matrix and partial reads complete
+    __syncthreads();   // partial reads complete
 
-    if (tid == 0) {
-        float A[WM][WM];
-#pragma unroll
-        for (int i = 0; i < WM; ++i)
-#pragma unroll
-            for (int j = 0; j < WM; ++j) A[i][j] = (i < W && j < W) ? G[i][j] : 0.f;
-        const int nb = cn + 1;   // the carried pairs held, and the new one
-        const float mu = window_max_eig<WM>(A) / (float)nb;
-        const float lt = a.lam[s];
-        const float eta = a.beta[s] / (mu + lt + a.eps);
-        scal[0] = 1.f - eta * lt;
-        scal[1] = eta / (float)nb;
-    }
-    __syncthreads();
     const float gam = scal[0], cc = scal[1];
 
     float4 C = make_float4(0.f, 0.f, 0.f, 0.f);
