@@ -6,18 +6,29 @@
 
 namespace fw {
 
+// Round-robin ("circle") pairing of WM indices: in round r (0 .. WM-2) slot k
+// pairs jac_a(r, k) with jac_b(r, k); every round is a perfect matching and a
+// sweep of WM-1 rounds meets every pair once.
+__host__ __device__ constexpr int jac_a(int n, int r, int k) { return k == 0 ? r : (r + k) % (n - 1); }
+__host__ __device__ constexpr int jac_b(int n, int r, int k) {
+    return k == 0 ? n - 1 : (r - k + (n - 1)) % (n - 1);
+}
+
 // Largest eigenvalue of the symmetric WM x WM matrix A (destroyed), which is
-// zero outside the rows and columns of the pairs that exist.  Cyclic Jacobi:
-// each rotation J = [[c, s], [-s, c]] on rows / columns (p, q) is chosen so
-// that (J^T A J)_pq = 0 (Golub and Van Loan, the symmetric Schur
-// decomposition), t = tan(theta) being the smaller root of
-// t^2 + 2 tau t - 1 = 0 with tau = (a_qq - a_pp) / (2 a_pq); the two
-// diagonal entries move by -t a_pq and +t a_pq.  Sweeps stop once the
-// squared off-diagonal mass is below 1e-12 of the squared diagonal, or after
-// 12 (window matrices converge in at most five).  Indices are compile-time,
-// so A stays in registers.
+// zero outside the rows and columns of the pairs that exist.  Jacobi
+// rotations in the parallel (round-robin) ordering (Golub and Van Loan, the
+// symmetric Schur decomposition and its parallel orderings): each round
+// rotates WM/2 disjoint index pairs at once, J = [[c, s], [-s, c]] on (p, q)
+// chosen so that (J^T A J)_pq = 0, t = tan(theta) being the smaller root of
+// t^2 + 2 tau t - 1 = 0 with tau = (a_qq - a_pp) / (2 a_pq); the round's
+// rotations commute, so their angles come from the same A and the update is
+// A <- J^T A J with J their product.  Sweeps stop once the squared
+// off-diagonal mass is below 1e-12 of the squared diagonal, or after 12
+// (window matrices converge in at most four).  Indices are compile-time, so A
+// stays in registers, and the angles of a round are independent.
 template <int WM>
 __device__ __forceinline__ float window_max_eig(float (&A)[WM][WM]) {
+    static_assert(WM % 2 == 0, "an even number of slots");
     for (int sweep = 0; sweep < 12; ++sweep) {
         float off = 0.f, dg = 0.f;
 #pragma unroll
@@ -29,33 +40,56 @@ __device__ __forceinline__ float window_max_eig(float (&A)[WM][WM]) {
             }
         if (!(off > 1e-12f * dg)) break;
 #pragma unroll
-        for (int p = 0; p < WM - 1; ++p)
+        for (int r = 0; r < WM - 1; ++r) {
+            float cs[WM / 2], sn[WM / 2];
 #pragma unroll
-            for (int q = p + 1; q < WM; ++q) {
+            for (int k = 0; k < WM / 2; ++k) {
+                constexpr int n = WM;
+                const int a0 = jac_a(n, r, k), b0 = jac_b(n, r, k);
+                const int p = a0 < b0 ? a0 : b0, q = a0 < b0 ? b0 : a0;
                 const float apq = A[p][q];
+                float c = 1.f, s = 0.f;
                 if (apq != 0.f) {
                     // fast reciprocal square root and division (a few ulp): the
                     // rotations stay orthogonal to a few ulp, far inside the
                     // eigenvalue accuracy the step needs
                     const float tau = __fdividef(A[q][q] - A[p][p], 2.f * apq);
-                    const float at = fabsf(tau), r = fmaf(tau, tau, 1.f);
+                    const float at = fabsf(tau), r2 = fmaf(tau, tau, 1.f);
                     // for |tau| beyond 1e18, t = 1 / (2 tau) to fp32 precision (and
                     // tau * tau would overflow)
                     const float t = at > 1e18f ? __fdividef(0.5f, tau)
-                                               : copysignf(__fdividef(1.f, at + r * rsqrtf(r)), tau);
-                    const float c = rsqrtf(fmaf(t, t, 1.f)), s = t * c;
+                                               : copysignf(__fdividef(1.f, at + r2 * rsqrtf(r2)), tau);
+                    c = rsqrtf(fmaf(t, t, 1.f));
+                    s = t * c;
+                }
+                cs[k] = c;
+                sn[k] = s;
+            }
+            // A <- A J (columns p, q of every pair), then A <- J^T A (rows)
 #pragma unroll
-                    for (int k = 0; k < WM; ++k) {
-                        if (k == p || k == q) continue;
-                        const float akp = A[k][p], akq = A[k][q];
-                        A[k][p] = A[p][k] = c * akp - s * akq;
-                        A[k][q] = A[q][k] = s * akp + c * akq;
-                    }
-                    A[p][p] -= t * apq;
-                    A[q][q] += t * apq;
-                    A[p][q] = A[q][p] = 0.f;
+            for (int k = 0; k < WM / 2; ++k) {
+                const int a0 = jac_a(WM, r, k), b0 = jac_b(WM, r, k);
+                const int p = a0 < b0 ? a0 : b0, q = a0 < b0 ? b0 : a0;
+#pragma unroll
+                for (int i = 0; i < WM; ++i) {
+                    const float aip = A[i][p], aiq = A[i][q];
+                    A[i][p] = cs[k] * aip - sn[k] * aiq;
+                    A[i][q] = sn[k] * aip + cs[k] * aiq;
                 }
             }
+#pragma unroll
+            for (int k = 0; k < WM / 2; ++k) {
+                const int a0 = jac_a(WM, r, k), b0 = jac_b(WM, r, k);
+                const int p = a0 < b0 ? a0 : b0, q = a0 < b0 ? b0 : a0;
+#pragma unroll
+                for (int i = 0; i < WM; ++i) {
+                    const float api = A[p][i], aqi = A[q][i];
+                    A[p][i] = cs[k] * api - sn[k] * aqi;
+                    A[q][i] = sn[k] * api + cs[k] * aqi;
+                }
+                A[p][q] = A[q][p] = 0.f;
+            }
+        }
     }
     float m = A[0][0];
 #pragma unroll

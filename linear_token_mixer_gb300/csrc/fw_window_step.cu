@@ -38,11 +38,6 @@ window_step_kernel(WindowArgs a) {
     const int W = a.W;
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
 
-    float4 *Sp = reinterpret_cast<float4 *>(a.S_T + s * D * D);
-    float4 Sr[NP];
-#pragma unroll
-    for (int p = 0; p < NP; ++p) Sr[p] = __ldcs(&Sp[(p * RPP + rg) * TPR + cq]);
-
     __shared__ __align__(16) float xs[WM][D];
     __shared__ __align__(16) float ys[WM][D];
     __shared__ float qs[D];
@@ -52,23 +47,40 @@ window_step_kernel(WindowArgs a) {
     const int64_t cs = (int64_t)(W - 1) * D;
     int cn = a.cn ? a.cn[s] : 0;
     cn = cn < 0 ? 0 : (cn > W - 1 ? W - 1 : cn);
-    // window rows j = 0 .. W-2: carried slots (held if j >= W-1-cn); row W-1: the new pair
-    for (int e = tid; e < WM * D; e += kThreads) {
-        const int j = e / D, i = e % D;
-        float x = 0.f, y = 0.f;
+    // window rows j = 0 .. W-2: carried slots (held if j >= W-1-cn); row W-1:
+    // the new pair.  Their loads go out before the state's, so the window's
+    // Gram matrix and eigenvalue are formed while the state streams in.
+    constexpr int NE = WM * D / kThreads;   // window elements per thread
+    float xv[NE], yv[NE];
+#pragma unroll
+    for (int u = 0; u < NE; ++u) {
+        const int e = tid + u * kThreads, j = e / D, i = e % D;
+        xv[u] = 0.f;
+        yv[u] = 0.f;
         if (j < W - 1) {
             if (a.cx && j >= W - 1 - cn) {
-                x = a.cx[s * cs + e];
-                y = a.cy[s * cs + e];
+                xv[u] = a.cx[s * cs + e];
+                yv[u] = a.cy[s * cs + e];
             }
         } else if (j == W - 1) {
-            x = apply_phi(a.phi, to_f32(static_cast<const TIn *>(a.k)[s * D + i]));
-            y = to_f32(static_cast<const TIn *>(a.v)[s * D + i]);
+            xv[u] = to_f32(static_cast<const TIn *>(a.k)[s * D + i]);
+            yv[u] = to_f32(static_cast<const TIn *>(a.v)[s * D + i]);
         }
-        xs[j][i] = x;
-        ys[j][i] = y;
     }
-    for (int i = tid; i < D; i += kThreads) qs[i] = to_f32(static_cast<const TIn *>(a.q)[s * D + i]);
+    const float qv0 = tid < D ? to_f32(static_cast<const TIn *>(a.q)[s * D + tid]) : 0.f;
+
+    float4 *Sp = reinterpret_cast<float4 *>(a.S_T + s * D * D);
+    float4 Sr[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) Sr[p] = __ldcs(&Sp[(p * RPP + rg) * TPR + cq]);
+
+#pragma unroll
+    for (int u = 0; u < NE; ++u) {
+        const int e = tid + u * kThreads, j = e / D, i = e % D;
+        xs[j][i] = j == W - 1 ? apply_phi(a.phi, xv[u]) : xv[u];
+        ys[j][i] = yv[u];
+    }
+    if (tid < D) qs[tid] = qv0;
     __syncthreads();
 
     // Gram matrix of the window (upper triangle) and x_j . q, one warp each
