@@ -407,6 +407,23 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_sub(name, K, W, dev, fw, peaks):
+    """One sub-benchmark alone (the same calls the full run makes)."""
+    if name == "decode":
+        r = bench_decode(K, W, dev, fw)
+    elif name in ("decode_falcon3_w4", "decode_falcon3a_w4"):
+        r = bench_window_step(K, W, dev, fw, window=4, mode=name.split("_")[1])
+    elif name in I.WORKLOADS and I.WORKLOADS[name].mode in ("falcon3", "falcon3a"):
+        return dict(bench_window(I.WORKLOADS[name], K, W, dev, fw), workload=name)
+    elif name in I.WORKLOADS:
+        r, _ = bench_prefill(I.WORKLOADS[name], K, W, dev, fw)
+    else:
+        raise SystemExit("unknown sub-benchmark %r" % name)
+    r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
+    r["workload"] = name
+    return r
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -416,6 +433,10 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
+    ap.add_argument("--sub", default=None,
+                    help="run one sub-benchmark of the 'workloads' object alone (a prefill "
+                         "workload name, decode, decode_falcon3_w4 or decode_falcon3a_w4) and "
+                         "print its result; for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -439,6 +460,9 @@ def main():
     from linear_token_mixer_gb300 import fw
     fw.lib()
     peaks = _peaks()
+    if args.sub:
+        print(json.dumps(run_sub(args.sub, args.steps, args.warmup, dev, fw, peaks)), flush=True)
+        return
     w = I.WORKLOADS[args.workload]
 
     # ---- headline: timed region bracketed by barrier + synchronize

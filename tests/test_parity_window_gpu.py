@@ -198,3 +198,33 @@ def test_full_size_window_prefill_sampled_chains(name):
     eo, es = rel_l2(to64(of), ref[0]), rel_l2(to64(Sf), ref[1])
     assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], (eo, es)
     assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
+
+
+@pytest.mark.parametrize("W", [2, 4, 8])
+def test_window_prefill_degenerate_and_badly_scaled_windows(W):
+    # windows whose Gram matrix is singular (a key repeated over several
+    # tokens) or badly conditioned (keys scaled down by 1e-3 next to unit
+    # keys): the eigenvalue solve must still give the window's lambda_max
+    w, x = _inputs("falcon3", torch.float32, 64, T=90, W=W, key_norm="unit")
+    k = x["k"].clone()
+    k[:, :, 10:20] = k[:, :, 10:11]          # one key ten times in a row
+    k[:, :, 40:60:3] *= 1e-3                 # small keys among unit keys
+    k[:, :, 70:75] = 0.0                     # zero keys (pairs that exist, x = 0)
+    x["k"] = k
+    _assert_close(w, _gpu(w, x), _oracle(w, x))
+    # the same windows through the decode step, prefill of 8 tokens first
+    first = {kk: (t[:, :, :8].contiguous() if t is not None and kk != "S0" else t)
+             for kk, t in x.items()}
+    o1, S, win = _gpu(w.with_shape(T=8), first)
+    g = _dev(x)
+    spare = fw.new_window(w.B, w.H, w.d, W)
+    outs = [o1]
+    for t in range(8, w.T):
+        o, out = fw.window_step(g["q"][:, :, t].contiguous(), g["k"][:, :, t - 1].contiguous(),
+                                g["v"][:, :, t].contiguous(), g["beta"][:, :, t].contiguous(),
+                                g["lam"][:, :, t].contiguous(), S, W, win_in=win,
+                                win_out=spare, eps=w.eps)
+        spare, win = win, out
+        outs.append(o[:, :, None])
+    fw.check()
+    _assert_close(w, (torch.cat(outs, dim=2), S, win), _oracle(w, x))
