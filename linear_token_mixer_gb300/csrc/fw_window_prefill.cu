@@ -136,6 +136,7 @@ window_prefill_kernel(WindowArgs a) {
     constexpr int NB = L::NB, RQ = L::RQ, QS = L::QS, LD = L::LD, NXR = L::NXR;
     constexpr int CPT = L::CPT, RG = L::RG, NCT = L::NCT;
     constexpr int NCW = NCT / 32;        // compute warps
+    static_assert(2 * CPT == RG, "one reduced value per row-group lane");
     constexpr int NPT = kProducers;      // producer threads
     extern __shared__ __align__(16) float sm[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::BARS);
@@ -383,16 +384,14 @@ window_prefill_kernel(WindowArgs a) {
         for (int c = 0; c < CPT; ++c) S[c][m / 2] = f2(r0[c], r1[c]);
     }
 
-    // per column: the previous token's reads of its window's pairs and its
-    // write coefficients
-    float a_prev[CPT][WM], coef_prev[CPT][WM];
+    // lane rg < CPT of a column group keeps column c0 + rg's previous-token
+    // reads of its window's pairs and its write coefficients
+    float a_prev[WM], coef_prev[WM];
 #pragma unroll
-    for (int c = 0; c < CPT; ++c)
-#pragma unroll
-        for (int j = 0; j < WM; ++j) {
-            a_prev[c][j] = 0.f;
-            coef_prev[c][j] = 0.f;
-        }
+    for (int j = 0; j < WM; ++j) {
+        a_prev[j] = 0.f;
+        coef_prev[j] = 0.f;
+    }
     float gam_prev = 1.f;
 
     for (int64_t kb = 0; kb < nblk; ++kb) {
@@ -432,7 +431,7 @@ window_prefill_kernel(WindowArgs a) {
                     float r = acc[c].x + acc[c].y;
 #pragma unroll
                     for (int off = 1; off < RG; off <<= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
-                    a_prev[c][j - 1] = r;
+                    if (c == rg) a_prev[j - 1] = r;   // lane rg < CPT keeps column c0 + rg
                 }
             }
         }
@@ -461,66 +460,74 @@ window_prefill_kernel(WindowArgs a) {
                     pc[c] = __ffma2_rn(S[c][m / 2 + 1], f2(q4.z, q4.w), pc[c]);
                 }
             }
-            // reductions over the row groups: reads of the new pair (ra) and
-            // of the query (rc)
-            float ra[CPT], rc[CPT];
+            // reduce-scatter over the RG row-group lanes of the column group:
+            // values 0 .. CPT-1 are the new pair's reads of the CPT columns,
+            // CPT .. 2 CPT-1 the query's; lane rg ends with the whole of value rg
+            float v[2 * CPT];
 #pragma unroll
             for (int c = 0; c < CPT; ++c) {
-                ra[c] = pa[c].x + pa[c].y;
-                rc[c] = pc[c].x + pc[c].y;
+                v[c] = INNER ? 0.f : pa[c].x + pa[c].y;
+                v[CPT + c] = pc[c].x + pc[c].y;
             }
 #pragma unroll
-            for (int off = 1; off < RG; off <<= 1)
+            for (int h = RG / 2; h >= 1; h >>= 1) {
+                const bool up = (rg & h) != 0;
 #pragma unroll
-                for (int c = 0; c < CPT; ++c) {
-                    if constexpr (!INNER) ra[c] += __shfl_xor_sync(0xffffffffu, ra[c], off);
-                    rc[c] += __shfl_xor_sync(0xffffffffu, rc[c], off);
+                for (int i = 0; i < h; ++i) {
+                    const float send = up ? v[i] : v[i + h];
+                    const float keep = up ? v[i + h] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, h);
                 }
-
-            // per column: the reads of the older pairs by recursion (descending
-            // j, so that a_prev is replaced in place after its last use), the
-            // residuals and the write coefficients
-            float coef[CPT][WM];
-            {
+            }
+            // lane rg < CPT serves column c0 + rg; its query read sits on lane rg + CPT
+            const float rcv = __shfl_xor_sync(0xffffffffu, v[0], CPT);
+            float coef_m[WM];
+#pragma unroll
+            for (int j = 0; j < WM; ++j) coef_m[j] = 0.f;
+            if (rg < CPT) {
+                const int col = c0 + rg;
                 const float *mt = Mw + t * WM * WM;
+                // the reads of the older pairs by recursion (descending j, so
+                // that a_prev is replaced in place after its last use), the
+                // residuals and the write coefficients
 #pragma unroll
                 for (int j = WM - 1; j >= 0; --j) {
                     const bool in = j < W;   // slot j of the window (else coefficient 0)
-                    float y[CPT];            // targets of pair p - j in this thread's columns
-                    load_n<CPT>(V + (rr - j) * DK + c0, y);
+                    const float y = V[(rr - j) * DK + col];   // target of pair p - j
+                    float aj = 0.f;
+                    if constexpr (!INNER) {
+                        if (j == 0) {
+                            aj = v[0];
+                        } else {
+                            // M and the previous coefficients are 0 outside the window
+                            aj = gam_prev * a_prev[j - 1];
 #pragma unroll
-                    for (int c = 0; c < CPT; ++c) {
-                        float aj = 0.f;
-                        if constexpr (!INNER) {
-                            if (j == 0) {
-                                aj = ra[c];
-                            } else {
-                                // M and the previous coefficients are 0 outside the window
-                                aj = gam_prev * a_prev[c][j - 1];
-#pragma unroll
-                                for (int jp = 0; jp < WM; ++jp)
-                                    aj = fmaf(mt[j * WM + jp], coef_prev[c][jp], aj);
-                            }
-                            a_prev[c][j] = in ? aj : 0.f;
+                            for (int jp = 0; jp < WM; ++jp)
+                                aj = fmaf(mt[j * WM + jp], coef_prev[jp], aj);
                         }
-                        coef[c][j] = in ? cc * (y[c] - aj) : 0.f;
+                        a_prev[j] = in ? aj : 0.f;
                     }
+                    coef_m[j] = in ? cc * (y - aj) : 0.f;
                 }
-            }
-
-            if (rg == 0) {
-                float ov[CPT];
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) ov[c] = rc[c];   // read before the write
+                float ov = rcv;   // read before the write
                 if (!rbw) {
+                    ov *= gam;
 #pragma unroll
-                    for (int c = 0; c < CPT; ++c) {
-                        ov[c] *= gam;
-#pragma unroll
-                        for (int j = 0; j < WM; ++j) ov[c] = fmaf(coef[c][j], E[t * WM + j], ov[c]);
-                    }
+                    for (int j = 0; j < WM; ++j) ov = fmaf(coef_m[j], E[t * WM + j], ov);
                 }
-                store_n<CPT>(og + p * DK + c0, ov);
+                og[p * DK + col] = from_f32<TIn>(ov);
+#pragma unroll
+                for (int j = 0; j < WM; ++j) coef_prev[j] = coef_m[j];
+            }
+            // every lane of the group takes the coefficients of all CPT columns
+            float coef[CPT][WM];
+            {
+                const int gbase = lane & ~(RG - 1);
+#pragma unroll
+                for (int c = 0; c < CPT; ++c)
+#pragma unroll
+                    for (int j = 0; j < WM; ++j)
+                        coef[c][j] = __shfl_sync(0xffffffffu, coef_m[j], gbase + c);
             }
             // the write: S = gamma S + sum_j x_{p-j} coef_j
             {
@@ -545,10 +552,6 @@ window_prefill_kernel(WindowArgs a) {
                     }
                 }
             }
-#pragma unroll
-            for (int c = 0; c < CPT; ++c)
-#pragma unroll
-                for (int j = 0; j < WM; ++j) coef_prev[c][j] = coef[c][j];
             gam_prev = gam;
         }
         __syncwarp();
