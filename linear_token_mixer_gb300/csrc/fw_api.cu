@@ -182,8 +182,21 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     if (st != FW_OK) return st;
 
     cudaError_t e;
-    if (algo == FW_ALGO_RECURRENT || !chunk_ok) e = launch_recurrent(a, stream);
-    else e = launch_chunked(a, stream);
+    if (algo == FW_ALGO_AUTO && per_channel(mode)) {
+        // a step per value column: the staged per-token kernel of the window
+        // family with a window of one pair
+        WindowArgs w{};
+        w.q = q; w.k = k; w.v = v; w.beta = beta; w.lam = lambda; w.S0 = S0;
+        w.k_init = a.k_init;
+        w.o = o; w.S_T = S_T; w.n_chains = nc; w.T = shape->T; w.d = d; w.W = 1;
+        w.dtype = dtype; w.inner = (mode == FW_FALCON2A); w.chan = true; w.phi = phi;
+        w.eps = eps; w.flags = flags; w.err = a.err; w.wait_ns = a.wait_ns;
+        e = launch_window_prefill(w, stream);
+    } else if (algo == FW_ALGO_RECURRENT || !chunk_ok) {
+        e = launch_recurrent(a, stream);
+    } else {
+        e = launch_chunked(a, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return FW_OK;
 }
@@ -298,7 +311,7 @@ extern "C" int fw_window_prefill(const void *q, const void *k, const void *v, co
     a.oy = carry_out ? win_out->y : nullptr;
     a.on = carry_out ? win_out->n : nullptr;
     a.n_chains = nc; a.T = shape->T; a.d = d; a.W = window; a.dtype = dtype;
-    a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+    a.inner = (mode == FW_FALCON3A); a.chan = false; a.phi = phi; a.eps = eps; a.flags = flags;
     a.wait_ns = g_wait_us.load() * 1000LL;
 
     if ((st = device_setup(&a.err)) != FW_OK) return st;
@@ -356,7 +369,7 @@ extern "C" int fw_window_step(const void *q, const void *k_prev, const void *v,
     a.oy = carry_out ? win_out->y : nullptr;
     a.on = carry_out ? win_out->n : nullptr;
     a.n_chains = ns; a.T = 1; a.d = d; a.W = window; a.dtype = dtype;
-    a.inner = (mode == FW_FALCON3A); a.phi = phi; a.eps = eps; a.flags = flags;
+    a.inner = (mode == FW_FALCON3A); a.chan = false; a.phi = phi; a.eps = eps; a.flags = flags;
     a.wait_ns = g_wait_us.load() * 1000LL;
 
     if ((st = device_setup(&a.err)) != FW_OK) return st;

@@ -63,7 +63,8 @@ struct WindowArgs {
     int d;                        // d_k == d_v
     int W;                        // window, 1 .. FW_WINDOW_MAX
     fw_dtype dtype;
-    bool inner;                   // Falcon-3A
+    bool inner;                   // Falcon-3A (Falcon-2A with chan)
+    bool chan;                    // Falcon-2 / 2A: W = 1, beta [T][d_v] (a step per value column)
     fw_phi phi;
     float eps;
     unsigned flags;

@@ -48,7 +48,7 @@ constexpr int kNB = 32;          // tokens per staged block
 constexpr int kProducers = 128;  // producer threads (four warps, one per SM sub-partition)
 constexpr int kBarProd = 1;      // named barrier of the producer warps
 
-template <int DK, int WM>
+template <int DK, int WM, bool CHAN = false>
 struct WinLayout {
     static constexpr int NB = kNB;
     // compute threads: CPT value columns x RPT key rows each; the RG threads
@@ -73,7 +73,8 @@ struct WinLayout {
     static constexpr int GAM = M + NB * WM * WM;     // [NB] gamma_t
     static constexpr int CC = GAM + NB;              // [NB] c_t = eta_t / B_t
     static constexpr int VAL = CC + NB;              // [NXR] 1 if the pair exists
-    static constexpr int BUF = (VAL + NXR + 3) / 4 * 4;
+    static constexpr int BETA = (VAL + NXR + 3) / 4 * 4;   // per-column steps: [NB][DK]
+    static constexpr int BUF = BETA + (CHAN ? NB * DK : 0);
     // producer scratch and barriers after the two buffers
     static constexpr int DOT = 2 * BUF;              // [NXR][WM] x_r . x_{r-delta}
     static constexpr int BL = DOT + NXR * WM;        // [NB][2] beta, lambda
@@ -129,10 +130,10 @@ __device__ __forceinline__ void store_n(__nv_bfloat16 *p, const float (&v)[N]) {
     if constexpr (N == 4) q[1] = __floats2bfloat162_rn(v[2], v[3]);
 }
 
-template <int DK, int WM, typename TIn, bool INNER>
-__global__ void __launch_bounds__(WinLayout<DK, WM>::NCT + kProducers, 1)
+template <int DK, int WM, typename TIn, bool INNER, bool CHAN>
+__global__ void __launch_bounds__(WinLayout<DK, WM, CHAN>::NCT + kProducers, 1)
 window_prefill_kernel(WindowArgs a) {
-    using L = WinLayout<DK, WM>;
+    using L = WinLayout<DK, WM, CHAN>;
     constexpr int NB = L::NB, RQ = L::RQ, QS = L::QS, LD = L::LD, NXR = L::NXR;
     constexpr int CPT = L::CPT, RG = L::RG, NCT = L::NCT;
     constexpr int NCW = NCT / 32;        // compute warps
@@ -203,7 +204,7 @@ window_prefill_kernel(WindowArgs a) {
                   *CC = sm + b * L::BUF + L::CC, *VAL = sm + b * L::BUF + L::VAL;
             const int64_t p0 = kb * NB;
             const int nt = (int)(T - p0 < NB ? T - p0 : NB);
-            const float bt_l = pt < nt ? a.beta[chain * T + p0 + pt] : 0.f;
+            const float bt_l = !CHAN && pt < nt ? a.beta[chain * T + p0 + pt] : 0.f;
             const float lt_l = pt < nt ? a.lam[chain * T + p0 + pt] : 0.f;
             // this block's raw rows (then no copy is in flight), then its
             // buffer; the producer warps agree on the outcome before leaving
@@ -213,6 +214,17 @@ window_prefill_kernel(WindowArgs a) {
             if (bar_or(kBarProd, NPT, late)) {
                 if (pt == 0) atomicExch(a.err, kDevErrTimeout);
                 return;
+            }
+            if constexpr (CHAN) {
+                // per-column step sizes of the block's tokens, beta[p][j]
+                float *BT = sm + b * L::BUF + L::BETA;
+                const float *bg = a.beta + (chain * T + p0) * DK;
+#pragma unroll 8
+                for (int e = pt; e < NB * (DK / 4); e += NPT) {
+                    const int t = e / (DK / 4), i4 = (e % (DK / 4)) * 4;
+                    *reinterpret_cast<float4 *>(BT + t * DK + i4) =
+                        t < nt ? load4(bg + t * DK + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             // keys: row r holds pair m = p0 - WM + r, phi applied, 0 if it does not exist
 #pragma unroll 4
@@ -319,13 +331,21 @@ window_prefill_kernel(WindowArgs a) {
                     }
                 }
                 const float bt = BL[2 * t], lt = BL[2 * t + 1];
-                float eta = 0.f;
-                if (nb > 0) {
-                    const float mu = window_max_eig<WM>(G) / (float)nb;
-                    eta = bt / (mu + lt + a.eps);
+                if constexpr (CHAN) {
+                    // a step per value column (W = 1, mu = |x|^2): the compute
+                    // threads take eta_j = beta_j / (|x|^2 + lambda + eps) from
+                    // lambda and the reciprocal denominator
+                    GAM[t] = lt;
+                    CC[t] = nb > 0 ? 1.f / (G[0][0] + lt + a.eps) : 0.f;
+                } else {
+                    float eta = 0.f;
+                    if (nb > 0) {
+                        const float mu = window_max_eig<WM>(G) / (float)nb;
+                        eta = bt / (mu + lt + a.eps);
+                    }
+                    GAM[t] = 1.f - eta * lt;
+                    CC[t] = nb > 0 ? eta / (float)nb : 0.f;
                 }
-                GAM[t] = 1.f - eta * lt;
-                CC[t] = nb > 0 ? eta / (float)nb : 0.f;
 #pragma unroll
                 for (int j = 0; j < WM; ++j)
 #pragma unroll
@@ -484,9 +504,15 @@ window_prefill_kernel(WindowArgs a) {
             float coef_m[WM];
 #pragma unroll
             for (int j = 0; j < WM; ++j) coef_m[j] = 0.f;
+            float gcol = gam;   // this lane's column: decay, and write coefficient scale
             if (rg < CPT) {
                 const int col = c0 + rg;
                 const float *mt = Mw + t * WM * WM;
+                float ccol = cc;
+                if constexpr (CHAN) {   // GAM holds lambda, CC the reciprocal denominator
+                    ccol = sm[b * L::BUF + L::BETA + t * DK + col] * cc;
+                    gcol = 1.f - ccol * gam;
+                }
                 // the reads of the older pairs by recursion (descending j, so
                 // that a_prev is replaced in place after its last use), the
                 // residuals and the write coefficients
@@ -507,11 +533,11 @@ window_prefill_kernel(WindowArgs a) {
                         }
                         a_prev[j] = in ? aj : 0.f;
                     }
-                    coef_m[j] = in ? cc * (y - aj) : 0.f;
+                    coef_m[j] = in ? ccol * (y - aj) : 0.f;
                 }
                 float ov = rcv;   // read before the write
                 if (!rbw) {
-                    ov *= gam;
+                    ov *= gcol;
 #pragma unroll
                     for (int j = 0; j < WM; ++j) ov = fmaf(coef_m[j], E[t * WM + j], ov);
                 }
@@ -529,13 +555,16 @@ window_prefill_kernel(WindowArgs a) {
                     for (int j = 0; j < WM; ++j)
                         coef[c][j] = __shfl_sync(0xffffffffu, coef_m[j], gbase + c);
             }
-            // the write: S = gamma S + sum_j x_{p-j} coef_j
+            // the write: S = gamma S + sum_j x_{p-j} coef_j (gamma per column with CHAN)
             {
-                const float2 g2 = f2(gam, gam);
 #pragma unroll
-                for (int c = 0; c < CPT; ++c)
+                for (int c = 0; c < CPT; ++c) {
+                    const float gc = CHAN ? __shfl_sync(0xffffffffu, gcol, (lane & ~(RG - 1)) + c)
+                                          : gam;
+                    const float2 g2 = f2(gc, gc);
 #pragma unroll
                     for (int i = 0; i < RQ / 2; ++i) S[c][i] = __fmul2_rn(S[c][i], g2);
+                }
                 const float *x0 = X + rr * LD + rg * QS;
 #pragma unroll
                 for (int m = 0; m < RQ; m += 4) {
@@ -572,15 +601,15 @@ window_prefill_kernel(WindowArgs a) {
     }
 }
 
-template <int DK, int WM, typename TIn, bool INNER>
+template <int DK, int WM, typename TIn, bool INNER, bool CHAN = false>
 cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
-    auto kern = window_prefill_kernel<DK, WM, TIn, INNER>;
-    constexpr size_t bytes = WinLayout<DK, WM>::template bytes<TIn>();
+    auto kern = window_prefill_kernel<DK, WM, TIn, INNER, CHAN>;
+    constexpr size_t bytes = WinLayout<DK, WM, CHAN>::template bytes<TIn>();
     static_assert(bytes <= 227 * 1024, "shared memory of one CTA");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)a.n_chains, WinLayout<DK, WM>::NCT + kProducers, bytes, s>>>(a);
+    kern<<<(unsigned)a.n_chains, WinLayout<DK, WM, CHAN>::NCT + kProducers, bytes, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -589,7 +618,9 @@ cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
 template <int DK, typename TIn>
 cudaError_t launch_d(const WindowArgs &a, cudaStream_t s) {
     if (a.W <= 2)
-        return a.inner ? launch_t<DK, 2, TIn, true>(a, s) : launch_t<DK, 2, TIn, false>(a, s);
+        return a.chan ? (a.inner ? launch_t<DK, 2, TIn, true, true>(a, s)
+                                 : launch_t<DK, 2, TIn, false, true>(a, s))
+                      : (a.inner ? launch_t<DK, 2, TIn, true>(a, s) : launch_t<DK, 2, TIn, false>(a, s));
     if (a.W <= 4)
         return a.inner ? launch_t<DK, 4, TIn, true>(a, s) : launch_t<DK, 4, TIn, false>(a, s);
     return a.inner ? launch_t<DK, 8, TIn, true>(a, s) : launch_t<DK, 8, TIn, false>(a, s);

@@ -182,19 +182,27 @@ def _channel_betas(x, dv, seed=12):
     return torch.rand(lead + (dv,), generator=g) * 1.4 + 0.1   # U(0.1, 1.5) per channel
 
 
+@pytest.mark.parametrize("algo", ["auto", "recurrent"])
 @pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
-@pytest.mark.parametrize("rbw,same_pair", [(False, False), (True, True)])
-@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.bfloat16, 128)])
-def test_falcon2_prefill(mode, rbw, same_pair, dtype, d):
+@pytest.mark.parametrize("rbw,same_pair,kinit", [(False, False, False), (True, True, False),
+                                                 (True, False, True), (False, True, False)])
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 128),
+                                     (torch.bfloat16, 128)])
+def test_falcon2_prefill(mode, rbw, same_pair, kinit, dtype, d, algo):
+    # AUTO takes the staged per-token kernel (window of one pair, a step per
+    # column); RECURRENT the plain per-token kernel.  T spans several blocks.
     w, x = _inputs("falcon1", dtype, d, T=70)
     x["beta"] = _channel_betas(x, d)
+    k_init = torch.randn(x["k"].shape[:2] + (d,), generator=torch.Generator().manual_seed(3))
+    k_init = k_init.to(dtype) if kinit else None
     g = {k: (t.to(DEV) if t is not None else None) for k, t in x.items()}
     o, S = fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=mode,
-                      eps=w.eps, rbw=rbw, same_pair=same_pair)   # AUTO: the per-token kernel
+                      eps=w.eps, rbw=rbw, same_pair=same_pair, algo=algo,
+                      k_init=None if k_init is None else k_init.to(DEV))
     fw.check()
     c = {k: t.cpu() for k, t in x.items()}
     o_ref, S_ref = oracle.falcon2(c["q"], c["k"], c["v"], c["beta"], c["lam"], c["S0"],
-                                  eps=w.eps, inner=(mode == "falcon2a"), rbw=rbw,
+                                  k_init=k_init, eps=w.eps, inner=(mode == "falcon2a"), rbw=rbw,
                                   same_pair=same_pair)
     tol = TOL[dtype]
     eo, es = rel_l2(to64(o), o_ref), rel_l2(to64(S), S_ref)
@@ -220,3 +228,21 @@ def test_falcon2_decode(mode, dtype, rbw):
         assert rel_l2(to64(og), o_r) <= TOL[dtype]
     fw.check()
     assert rel_l2(to64(Sg), Sr) <= TOL[dtype]
+
+
+def test_falcon2_workload_full_size_sampled():
+    # B8 H16 T4096 d128 bf16 with a step per value channel, the launch the
+    # bench times (AUTO: the staged per-token kernel); 3 chains checked
+    w = I.WORKLOADS["falcon2_bf16"]
+    x = I.prefill_inputs(w, device=DEV)
+    o, S = fw.prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], x["S0"], mode=w.mode,
+                      eps=w.eps)
+    fw.check()
+    chains = [0, 77, 127]
+    xs = select_chains(x, chains)
+    o_ref, S_ref = oracle.falcon2(xs["q"], xs["k"], xs["v"], xs["beta"], xs["lam"], xs["S0"],
+                                  eps=w.eps)
+    og = to64(o.reshape(-1, w.T, w.d)[chains])[None]
+    Sg = to64(S.reshape(-1, w.d, w.d)[chains])[None]
+    eo, es = rel_l2(og, o_ref), rel_l2(Sg, S_ref)
+    assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], (eo, es)
