@@ -90,7 +90,8 @@ def algorithmic_bytes_prefill(w):
     given) and S_T written once."""
     esz = 2 if w.dtype == torch.bfloat16 else 4
     ht = w.B * w.H * w.T
-    gates = {"falcon1": 8, "falcon1a": 8, "falcon2": 4 * w.d + 4, "falcon2a": 4 * w.d + 4}
+    gates = {"falcon1": 8, "falcon1a": 8, "falcon3": 8, "falcon3a": 8,
+             "falcon2": 4 * w.d + 4, "falcon2a": 4 * w.d + 4}
     per_ht = 4 * w.d * esz + gates.get(w.mode, 0)
     state = w.B * w.H * w.d * w.d * 4
     return ht * per_ht + state * (2 if w.s0_std > 0 else 1)
