@@ -28,6 +28,9 @@ __host__ __device__ constexpr int jac_b(int n, int r, int k) {
 // stays in registers, and the angles of a round are independent.
 template <int WM>
 __device__ __forceinline__ float window_max_eig(float (&A)[WM][WM]) {
+    if constexpr (WM == 1) {
+        return A[0][0];   // a window of one pair: mu = |x|^2
+    } else {
     static_assert(WM % 2 == 0, "an even number of slots");
     for (int sweep = 0; sweep < 12; ++sweep) {
         float off = 0.f, dg = 0.f;
@@ -95,6 +98,7 @@ __device__ __forceinline__ float window_max_eig(float (&A)[WM][WM]) {
 #pragma unroll
     for (int p = 1; p < WM; ++p) m = fmaxf(m, A[p][p]);
     return m;
+    }
 }
 
 }  // namespace fw

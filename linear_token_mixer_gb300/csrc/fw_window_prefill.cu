@@ -613,14 +613,16 @@ cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// The window's slots are compile-time (WM = 2, 4 or 8 >= W); slots past W
+// The window's slots are compile-time (WM = 1, 2, 4 or 8 >= W); slots past W
 // carry zero coefficients.
 template <int DK, typename TIn>
 cudaError_t launch_d(const WindowArgs &a, cudaStream_t s) {
-    if (a.W <= 2)
-        return a.chan ? (a.inner ? launch_t<DK, 2, TIn, true, true>(a, s)
-                                 : launch_t<DK, 2, TIn, false, true>(a, s))
-                      : (a.inner ? launch_t<DK, 2, TIn, true>(a, s) : launch_t<DK, 2, TIn, false>(a, s));
+    if (a.W == 1)
+        return a.chan ? (a.inner ? launch_t<DK, 1, TIn, true, true>(a, s)
+                                 : launch_t<DK, 1, TIn, false, true>(a, s))
+                      : (a.inner ? launch_t<DK, 1, TIn, true>(a, s) : launch_t<DK, 1, TIn, false>(a, s));
+    if (a.W == 2)
+        return a.inner ? launch_t<DK, 2, TIn, true>(a, s) : launch_t<DK, 2, TIn, false>(a, s);
     if (a.W <= 4)
         return a.inner ? launch_t<DK, 4, TIn, true>(a, s) : launch_t<DK, 4, TIn, false>(a, s);
     return a.inner ? launch_t<DK, 8, TIn, true>(a, s) : launch_t<DK, 8, TIn, false>(a, s);
