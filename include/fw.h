@@ -109,8 +109,10 @@ typedef enum { FW_FLAG_RBW = 1, FW_FLAG_SAME_PAIR = 2 } fw_flag;
 typedef enum { FW_PHI_IDENTITY = 0, FW_PHI_ELU1 = 1 } fw_phi;
 
 /* Kernel choice for fw_prefill_ex.  FW_ALGO_AUTO picks the chunked
- * tensor-core kernel when it supports the call (bf16, d_k = d_v = 128) and the
- * per-token SIMT recurrence otherwise. */
+ * tensor-core kernel when it supports the call (bf16, d_k = d_v = 128), the
+ * staged per-token kernel of the window family for FW_FALCON2 / FW_FALCON2A,
+ * and the plain per-token SIMT recurrence otherwise; FW_ALGO_RECURRENT forces
+ * the plain per-token recurrence. */
 typedef enum { FW_ALGO_AUTO = 0, FW_ALGO_RECURRENT = 1, FW_ALGO_CHUNKED = 2 } fw_algo;
 
 typedef struct {

@@ -1,4 +1,5 @@
-// fw_window_prefill.cu -- Falcon-3 / 3A prefill, one token at a time (fp32).
+// fw_window_prefill.cu -- Falcon-3 / 3A (and Falcon-2 / 2A) prefill, one token
+// at a time (fp32).
 //
 // The write of "Fast Weight Attention for Continual Learning" paper reading
 // §4.2 (Falcon-3) and §4.3 (Falcon-3A): one gradient step on the average loss
@@ -12,16 +13,20 @@
 // counts the ones that do.
 //
 // Work split.  One CTA per chain.  The value columns are independent given
-// the window's keys and step sizes, so a compute thread holds two columns
-// over a quarter of the key rows (2 d_k compute threads) and the state never
-// leaves registers.  One more warp, the producer, works a
-// block of tokens ahead: it stages the block's keys (with the W pairs before
-// it), queries and targets (with the same W pairs) in shared memory and
-// forms everything that
-// depends on keys alone -- the dot products x_a . x_b of pairs up to W apart,
-// q_t . x_{t-j}, each token's window Gram matrix and its largest eigenvalue
-// (one lane per token), eta_t, gamma_t and c_t -- into the other of two
+// the window's keys and step sizes: a compute thread holds CPT value columns
+// over a slice of the key rows (4 columns x 16 rows at d = 128 for windows up
+// to 4 pairs), and the state never leaves registers.  Per token, the
+// row-slice lanes of a column group reduce-scatter their partial reads, one
+// lane per column runs that column's scalar work, and the write coefficients
+// are broadcast back for the rank-W write.  Four producer warps work a block
+// of 32 tokens ahead: they bulk-copy the block's keys (with the W pairs
+// before it), queries and targets, stage them in shared memory, and form
+// everything that depends on keys alone -- the dot products x_a . x_b of
+// pairs up to W apart, q_t . x_{t-j}, each token's window Gram matrix and its
+// largest eigenvalue, eta_t, gamma_t and c_t -- into the other of two
 // buffers.  Buffers change hands through mbarriers whose waits are bounded.
+// With a window of one pair and beta per value column (CHAN) the same kernel
+// serves Falcon-2 / 2A, the page's per-channel step (§4.2).
 //
 // Residual reads by recursion.  Of the W residual reads S_{t-1}^T x_{t-j}
 // only the newest pair's (j = 0) is a product with the state: for j >= 1 the
