@@ -181,6 +181,10 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
     b[1] = __float_as_uint(M[f32i(k0 + t + 4, n0 + g)]);
 }
 
+// GATED: eta, gamma and decays (not linear attention); FALCON: the residual
+// write (L, T, W).  Each mode is its own instantiation, so no role's loop
+// carries another mode's code.
+template <bool GATED, bool FALCON>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -194,8 +198,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const int64_t chain = blockIdx.x;
     const int64_t T = a.T;
     const int nch = (int)((T + C - 1) / C);
-    const bool gated = (a.mode != FW_LINATTN);                     // eta, gamma, decays
-    const bool falcon = (a.mode == FW_FALCON1);                    // residual: L, T, W
+    constexpr bool gated = GATED;                                  // eta, gamma, decays
+    constexpr bool falcon = FALCON;                                // residual: L, T, W
     const bool shifted = gated && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;                 // o_t = S_{t-1}^T q_t
     const bool elu = (a.phi == FW_PHI_ELU1);
@@ -1163,10 +1167,12 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
         !make_map(&tv, a.v, a.T, a.n_chains) ||
         !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunked_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = a.mode == FW_LINATTN ? chunked_kernel<false, false>
+              : a.mode == FW_FALCON1 ? chunked_kernel<true, true> : chunked_kernel<true, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    chunked_kernel<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
+    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
     return cudaGetLastError();
 }
 
