@@ -1066,8 +1066,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             {
                 const float *gv = reinterpret_cast<const float *>(sm + OFF_SGV);
                 __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RA) + srow;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {   // (a rolled loop: less code beside the key group's)
                     float o1[32], o2[32];
                     tmem_ld32x2(tmem + lane_base + COL_O1 + 32 * h, tmem + lane_base + COL_O2 + 32 * h, o1, o2);
                     if (srow == 0) TRACE(c, 26 + 2 * h);
