@@ -111,8 +111,9 @@ def window_flops(w):
     """Flops of the Falcon-3 / 3A write by its definition, per head-token:
     W residual reads S^T x_j (Falcon-3 only), the rank-W write and the decay,
     and the read S^T q -- (2W + 2) d^2 multiply-adds (3A: W + 2), 2 flops each.
-    The kernel forms the older pairs' reads by recursion, so it executes fewer."""
-    reads = 0 if w.mode == "falcon3a" else w.window
+    The kernel forms the older pairs' reads by recursion, so it executes fewer.
+    Falcon-2 / 2A (a step per value column) is the same count with W = 1."""
+    reads = 0 if w.mode in ("falcon3a", "falcon2a") else w.window
     return w.B * w.H * w.T * 2 * (reads + w.window + 2) * w.d * w.d
 
 
@@ -234,6 +235,14 @@ def bench_prefill(w, K, W, dev, fw, algo="auto", rbw=False, same_pair=False):
     }
     if rbw or same_pair:
         res["flags"] = [f for f, on in (("rbw", rbw), ("same_pair", same_pair)) if on]
+    if w.mode in ("falcon2", "falcon2a") and algo == "auto":
+        # per-channel steps run on the staged per-token kernel (window of one
+        # pair): bound by FP32 ALU work, not by memory
+        tf = window_flops(w) / (kern_ms / 1e3) / 1e12
+        res["roofline"] = {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS,
+                           "unit": "TFLOP/s", "frac": tf / ALU_FP32_TFLOPS,
+                           "kernel": "window prefill (SIMT)",
+                           "flops": "4 d^2 multiply-adds per head-token (2A: 3)"}
     return res, x
 
 

@@ -75,3 +75,16 @@ def test_stored_traffic_only_for_the_captured_sources(tmp_path, monkeypatch):
     # editing a kernel source invalidates the record
     (root / "linear_token_mixer_gb300" / "csrc" / "fw_sm100.cuh").write_text("// edited\n")
     assert bench.stored_traffic("chunked prefill", "falcon1_bf16") is None
+
+
+def test_alu_roofline_flop_counts_per_head_token():
+    # multiply-adds per head-token by the write's definition: residual reads
+    # S^T x_j (one per pair; none for the inner-product forms), the rank-W write,
+    # the decay of S and the read S^T q
+    from linear_token_mixer_gb300 import inputs as I
+    d = 128
+    per = lambda name, **kw: bench.window_flops(I.WORKLOADS[name].with_shape(B=1, H=1, T=1, **kw)) / (2 * d * d)
+    assert per("falcon3_bf16") == 4 + 4 + 2
+    assert per("falcon3a_bf16") == 4 + 2
+    assert per("falcon2_bf16") == 1 + 1 + 2     # a step per value column: W = 1
+    assert per("falcon2_bf16", mode="falcon2a") == 1 + 2
