@@ -228,3 +228,40 @@ def test_window_prefill_degenerate_and_badly_scaled_windows(W):
         outs.append(o[:, :, None])
     fw.check()
     _assert_close(w, (torch.cat(outs, dim=2), S, win), _oracle(w, x))
+
+
+@pytest.mark.parametrize("mode", ["falcon3", "falcon3a"])
+def test_window_step_full_size_sampled(mode):
+    # the decode configuration the bench times: 256 sequences x H=32 states, d=128,
+    # fp32 state (537 MB), bf16 step vectors, W=4, the two window buffers
+    # alternating; three steps from a random state, so the carried window holds
+    # 0, 1, 2 pairs.  Sampled states against the oracle's step, one by one.
+    cfg = I.DECODE
+    Bn, H, d, W, K = cfg["batch"], cfg["H"], cfg["d"], 4, 3
+    x = I.decode_inputs(K, Bn, H, d)
+    g = torch.Generator().manual_seed(41)
+    S0 = torch.randn(Bn, H, d, d, generator=g) * 0.05
+    S = S0.to(DEV)
+    wins = [fw.new_window(Bn, H, d, W, DEV), fw.new_window(Bn, H, d, W, DEV)]
+    outs = []
+    for s in range(K):
+        o, _ = fw.window_step(x["q"][s].to(DEV), x["k_prev"][s].to(DEV), x["v"][s].to(DEV),
+                              x["beta"][s].to(DEV), x["lam"][s].to(DEV), S, W,
+                              win_in=wins[s & 1] if s > 0 else None, win_out=wins[(s + 1) & 1],
+                              mode=mode, eps=cfg["eps"])
+        outs.append(o.cpu())
+    fw.check()
+    bi = torch.tensor([0, 17, 128, 255, 200, 64, 255])
+    hi = torch.tensor([0, 5, 31, 31, 3, 16, 0])
+    S_ref, win = S0[bi, hi], None
+    for s in range(K):
+        o_ref, S_ref, win = oracle.step3(x["q"][s][bi, hi], x["k_prev"][s][bi, hi],
+                                         x["v"][s][bi, hi], x["beta"][s][bi, hi],
+                                         x["lam"][s][bi, hi], S_ref, W, win=win,
+                                         eps=cfg["eps"], inner=(mode == "falcon3a"))
+        assert rel_l2(to64(outs[s][bi, hi]), o_ref) <= TOL[torch.bfloat16]
+    assert rel_l2(to64(S.cpu()[bi, hi]), S_ref) <= 1e-5
+    last = wins[K & 1]
+    np.testing.assert_array_equal(last[2].cpu()[bi, hi].numpy(), win[2])
+    np.testing.assert_allclose(to64(last[0].cpu()[bi, hi]), win[0], rtol=0, atol=1e-6)
+    np.testing.assert_allclose(to64(last[1].cpu()[bi, hi]), win[1], rtol=0, atol=1e-6)
