@@ -59,6 +59,7 @@ constexpr int KG_W0 = 4;     // first warp of the key group (lane quarters 0..3,
 constexpr int SG_W0 = 8;     // first warp of the state group
 constexpr int KG2_W0 = 12;   // key group, column half 1
 constexpr int BAR_KG = 1, BAR_SG = 2;   // named barriers of the two groups
+constexpr int BAR_PAIR0 = 3;            // and of the key group's two merge pairs (3, 4)
 constexpr int GROUP = 128, KGROUP = 256;
 
 constexpr uint32_t KB = 1024;
@@ -807,7 +808,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const int rr = (r < 16) ? r : 16 + r, cc4 = (r < 16) ? 16 + c4 : 48 + c4;
                 *reinterpret_cast<float4 *>(Tf + f64i(rr, cc4)) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            gsync();
+            // the first merge of pair p reads only the two diagonal blocks of the warps
+            // (kw = 2p, 2p+1) that do it; the zero blocks are read after the next sync
+            if (h == 0) {
+                if (kw < 2) bar_sync(BAR_PAIR0, 64);
+                else bar_sync(BAR_PAIR0 + 1, 64);
+            }
             if (kidx == 0) TRACE(c, 5);
             const int gq = lane >> 2, tq = lane & 3;
             float t2b[4];        // phase-2 tile
@@ -918,11 +924,13 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (c + 1 < nch && !lp(c + 1, Tf)) { ok = false; break; }   // T(c) fp32 is dead
 
             // ---- -W^T -> bf16 rows i, once W^T(c) is done and R(c-1) has read the old one
-            if (!gwait(bar(B_WUDONE), (uint32_t)c & 1u)) { ok = false; break; }
-            if (kidx == 0) TRACE(c, 7);
-            tc_fence_after();
-            if (c >= 1 && !gwait(bar(B_RDONE), (uint32_t)(c - 1) & 1u)) { ok = false; break; }
+            {
+                bool w = wait_bar(bar(B_WUDONE), (uint32_t)c & 1u, limit, s_abort);
+                w = w && (c < 1 || wait_bar(bar(B_RDONE), (uint32_t)(c - 1) & 1u, limit, s_abort));
+                if (bar_or(BAR_KG, KGROUP, !w)) { ok = false; break; }
+            }
             if (kidx == 0) TRACE(c, 8);
+            tc_fence_after();
             {
                 float w[32];
                 tmem_ld32(tmem + lane_base + COL_W + 32 * h, w);
@@ -990,8 +998,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
                 //      the output store of chunk c-1 has read the R^T buffer by then
                 if (srow == 0) { TRACE(c, 31); bulk_wait_read0(); }
-                if (!gwait(bar(B_RDONE), (uint32_t)c & 1u) ||
-                    !gwait(bar(B_GV0 + b), (uint32_t)(c / NST) & 1u)) { ok = false; break; }
+                {
+                    bool w = wait_bar(bar(B_RDONE), (uint32_t)c & 1u, limit, s_abort);
+                    w = w && wait_bar(bar(B_GV0 + b), (uint32_t)(c / NST) & 1u, limit, s_abort);
+                    if (bar_or(BAR_SG, GROUP, !w)) { ok = false; break; }
+                }
                 if (srow == 0) TRACE(c, 10);
                 tc_fence_after();
                 const float *wc = vec(b) + V_WC / 4;
@@ -1025,16 +1036,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             // ---- state carry (linear attention: the output store of chunk c-1 has read
             //      its staging tile before this chunk's is written)
             if (srow == 0) bulk_wait_read0();
-            if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
+            const bool last = (c + 1 == nch);
+            {
+                bool w = wait_bar(bar(B_SDONE), (uint32_t)c & 1u, limit, s_abort);
+                if (gated && !last)
+                    w = w && wait_bar(bar(B_GV0 + (c + 1) % NST), (uint32_t)((c + 1) / NST) & 1u,
+                                      limit, s_abort);
+                if (bar_or(BAR_SG, GROUP, !w)) { ok = false; break; }
+            }
             if (srow == 0) TRACE(c, 12);
             tc_fence_after();
-            const bool last = (c + 1 == nch);
-            float gC_next = 1.f;
-            if (gated && !last) {
-                const int b1 = (c + 1) % NST;
-                if (!gwait(bar(B_GV0 + b1), (uint32_t)((c + 1) / NST) & 1u)) { ok = false; break; }
-                gC_next = vec(b1)[V_GC / 4];
-            }
+            const float gC_next = (gated && !last) ? vec((c + 1) % NST)[V_GC / 4] : 1.f;
 #pragma unroll 1
             for (int q4 = 0; q4 < 2; ++q4) {   // i = 64 q4 .. 64 q4 + 63: one TMEM round trip
                 float v[64];
