@@ -221,7 +221,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     };
 
     if (tid == 0) {
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), 1);
+        // Falcon-1: T and -W^T are published by one arrival per key-group warp
+        for (int i = 0; i < B_COUNT; ++i)
+            mbar_init(bar(i), (falcon && (i == B_TRDY || i == B_WRDY)) ? KGROUP / 32 : 1);
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -918,9 +920,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     }
                 }
             }
+            // each warp publishes its part of T (the next phase's leading group
+            // agreement keeps L(c+1) from landing on the fp32 T before all have read it)
             fence_proxy_async();
-            gsync();
-            if (kidx == 0) { TRACE(c, 6); mbar_arrive(bar(B_TRDY)); }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_TRDY));
+            if (kidx == 0) TRACE(c, 6);
             if (c + 1 < nch && !lp(c + 1, Tf)) { ok = false; break; }   // T(c) fp32 is dead
 
             // ---- -W^T -> bf16 rows i, once W^T(c) is done and R(c-1) has read the old one
@@ -940,8 +945,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             tc_fence_before();
             fence_proxy_async();
-            gsync();
-            if (kidx == 0) { TRACE(c, 9); mbar_arrive(bar(B_WRDY)); }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_WRDY));   // each warp its rows of -W^T
+            if (kidx == 0) TRACE(c, 9);
         }
         if (!ok && kidx == 0) fail_now();
     } else if (warp >= SG_W0 && warp < KG2_W0) {
