@@ -221,9 +221,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     };
 
     if (tid == 0) {
-        // Falcon-1: T and -W^T are published by one arrival per key-group warp
-        for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(bar(i), (falcon && (i == B_TRDY || i == B_WRDY)) ? KGROUP / 32 : 1);
+        // Falcon-1: T, -W^T and the free Gram region are published by one arrival
+        // per key-group warp; R and the state copy by one per state-group warp
+        for (int i = 0; i < B_COUNT; ++i) {
+            uint32_t n = 1;
+            if (falcon && (i == B_TRDY || i == B_WRDY || i == B_GGO)) n = KGROUP / 32;
+            if (i == B_SRDY || i == B_RRDY || i == B_RFREE) n = GROUP / 32;
+            mbar_init(bar(i), n);
+        }
         fence_mbar_init();
         *s_abort = 0;
     }
@@ -671,7 +676,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (wrote) fence_proxy_async();
             }
             gsync();   // mapped tiles (and the k_init row) complete: the Gram MMA may start
-            if (kidx == 0) mbar_arrive(bar(B_GGO));
+            if (falcon ? lane == 0 : kidx == 0) mbar_arrive(bar(B_GGO));
             return true;
         };
         // Without a feature-map pass on the tiles (phi = identity), the Gram MMA of
@@ -737,9 +742,16 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 }
             tc_fence_before();
             fence_proxy_async();
-            gsync();
+            if constexpr (falcon) {
+                // each warp frees its rows of the Gram region; the phase that follows
+                // starts with a group agreement, which orders L and P for every reader
+                __syncwarp();
+                if (early && cc + 1 < nch && lane == 0) mbar_arrive(bar(B_GGO));
+            } else {
+                gsync();
+                if (early && cc + 1 < nch && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
+            }
             if (kidx == 0) TRACE(cc, 3);
-            if (early && cc + 1 < nch && kidx == 0) mbar_arrive(bar(B_GGO));   // the Gram region is free
             return true;
         };
         if (!falcon) {
@@ -771,7 +783,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         }
         // Falcon-1 (phi = identity): L/P of chunk c+1 runs while the W/U products of
         // chunk c are in flight
-        if (falcon && ok) ok = lp(0, reinterpret_cast<float *>(sm + lreg(0)));
+        if (falcon && ok) {
+            ok = lp(0, reinterpret_cast<float *>(sm + lreg(0)));
+            gsync();   // L(0) complete before the first solve reads it
+        }
 #pragma unroll 1
         for (int c = 0; falcon && c < nch && ok; ++c) {
             float *vb = vec(c % NST);        // gate block
@@ -992,8 +1007,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             }
             tmem_st_wait();
             tc_fence_before();
-            gsync();
-            if (srow == 0) mbar_arrive(bar(B_SRDY));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes of the state
         }
 
 #pragma unroll 1
@@ -1029,14 +1044,16 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         st_row8_bf16(sb + OFF_RB + sw128(srow, c16), w8);
                     }
                 }
+                // each warp publishes its rows of R (the state carry that follows
+                // starts with a group agreement)
                 tc_fence_before();
                 fence_proxy_async();
-                gsync();
-                if (srow == 0) {
-                    TRACE(c, 11);
+                __syncwarp();
+                if (lane == 0) {
                     mbar_arrive(bar(B_RRDY));
                     mbar_arrive(bar(B_RFREE));
                 }
+                if (srow == 0) TRACE(c, 11);
             }
 
             // ---- state carry (linear attention: the output store of chunk c-1 has read
@@ -1074,9 +1091,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tmem_st_wait();
             if (srow == 0) TRACE(c, 25);
             tc_fence_before();
-            gsync();
+            __syncwarp();
+            if (!last && lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
             if (srow == 0) TRACE(c, 13);
-            if (!last && srow == 0) mbar_arrive(bar(B_SRDY));
 
             // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t, staged as a [t][j] bf16 tile
             //      in the R^T buffer (free once S(c) and O2(c) are done: s_done),
