@@ -21,26 +21,29 @@
 // overlaps the state recurrence of chunk c:
 //   warp 0      TMA producer: X (keys shifted one token for Falcon-1; the row
 //               before the sequence reads as zero), Q, V tiles, 64 x 128 bf16,
-//               128-byte swizzle; X/Q double-buffered.
+//               128-byte swizzle; X/Q in a three-stage ring.
 //   warp 1      key-path MMA issuer:  G = [X;Q] X^T, W^T = X^T (T diag Gm)^T,
 //               U^T = Y^T T^T.
 //   warp 2      state-path MMA issuer: R^T = U^T - S^T W^T, O1^T = S^T Q^T,
 //               O2^T = R^T P^T, S += X^T (diag(w) R).
-//   warp 3      tensor-memory allocation.
+//   warp 3      tensor-memory allocation; in between, the gate warp (norms,
+//               eta, gamma and the decay products of each chunk).
 //   warps 4-7,  key group (two warps per tensor-memory lane quarter, each
-//   12-15       owning half the columns): feature map, gates and decay products,
-//               L and P from G, the triangular solve, -W^T staging.
+//   12-15       owning half the columns): feature map, L and P from G, the
+//               triangular solve, -W^T staging.
 //   warps 8-11  state group: R staging, state carry (fp32 in tensor memory,
-//               bf16 copy in shared memory as the MMA operand), outputs
-//               o_t = G_t O1_t + O2_t.
-// All products are tcgen05 MMAs with M = 128 (transposed forms keep d on the
-// M side), bf16 operands in shared memory and fp32 accumulators in tensor
-// memory.  The triangular solve runs on warp-level tf32 MMAs: each 16x16
-// diagonal block as the exact nilpotent product (I-L)(I+L^2)(I+L^4)(I+L^8),
-// then two levels of block merges T_ba = -T_bb L_ba T_aa.  Every
-// wait is bounded: on expiry the kernel records an error, the other roles
-// stop at their next wait, copies and MMAs in flight are drained, tensor
-// memory is freed and the kernel exits.
+//               with a bf16 copy in tensor memory as the A operand of R^T and
+//               O1^T), outputs o_t = G_t O1_t + O2_t.
+// All chunk products are tcgen05 MMAs with M = 128 (transposed forms keep d on
+// the M side), bf16 operands and fp32 accumulators in tensor memory.  The
+// triangular solve inverts the four 16x16 diagonal blocks by fp32 forward
+// substitution on the CUDA cores, then merges them in two levels,
+// T_ba = -T_bb L_ba T_aa, on warp-level tf32 MMAs.  With chains on few SMs
+// (SPLIT_CARRY) the state carry publishes the bf16 copy before it rescales
+// the fp32 state, taking the rescale off the state path's serial chain.
+// Every wait is bounded: on expiry the kernel records an error, the other
+// roles stop at their next wait, copies and MMAs in flight are drained,
+// tensor memory is freed and the kernel exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -93,7 +96,7 @@ static_assert(SMEM_ALLOC <= 227 * KB, "shared memory budget");
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + NST, B_FULLY = B_EMPTY0 + NST, B_YFREE, B_GGO, B_GDONE,
     B_TRDY, B_WUDONE, B_WRDY, B_GV0, B_PFREE0 = B_GV0 + NST, B_PFREE1, B_SRDY, B_RDONE, B_RRDY,
-    B_SDONE, B_OFREE, B_RFREE, B_KDRAIN, B_SDRAIN, B_NEVER, B_COUNT
+    B_SDONE, B_OFREE, B_RFREE, B_KDRAIN, B_SDRAIN, B_NEVER, B_SSCL, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -185,7 +188,7 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
 // GATED: eta, gamma and decays (not linear attention); FALCON: the residual
 // write (L, T, W).  Each mode is its own instantiation, so no role's loop
 // carries another mode's code.
-template <bool GATED, bool FALCON>
+template <bool GATED, bool FALCON, bool SPLIT_CARRY>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -226,7 +229,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t n = 1;
             if (falcon && (i == B_TRDY || i == B_WRDY || i == B_GGO)) n = KGROUP / 32;
-            if (i == B_SRDY || i == B_RRDY || i == B_RFREE) n = GROUP / 32;
+            if (i == B_SRDY || i == B_SSCL || i == B_RRDY || i == B_RFREE) n = GROUP / 32;
             mbar_init(bar(i), n);
         }
         fence_mbar_init();
@@ -417,7 +420,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                         mma_bf16_ta(tmem + COL_O1, sa + 8 * kk,
                                     dq + (((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4), id_mk, kk > 0);
                     TRACE(c, 17);
-                    if (!wait_fast(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                    if (!wait_fast(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort) ||
+                        (SPLIT_CARRY && !wait_fast(bar(B_SSCL), (uint32_t)c & 1u, limit, s_abort))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     // O2^T = R^T P^T;  S^T += (diag(w) R)^T X
                     const uint32_t id_kk = idesc_bf16(128, 64, false, false);
@@ -794,11 +801,12 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             float *Lf = reinterpret_cast<float *>(sm + tbo);
             float *Tf = reinterpret_cast<float *>(sm + lreg(c + 1));
             if (kidx == 0) TRACE(c, 4);
-            // ---- T = (I + L)^{-1} on the CUDA cores in fp32 (the warp-level tensor
-            //      MMAs would queue behind the chunk MMAs on the shared tensor pipe).
-            //      Blocks of 16: forward substitution on the diagonal blocks, then
-            //      T21 = -T22 L21 T11 at 16 -> 32 and 32 -> 64.  Tf's blocks above the
-            //      diagonal blocks stay zero, so every product runs over whole blocks.
+            // ---- T = (I + L)^{-1} in blocks of 16: fp32 forward substitution on the
+            //      CUDA cores for the diagonal blocks (a dependent chain of warp-level
+            //      tensor MMAs would queue behind the chunk MMAs on the shared tensor
+            //      pipe), then T21 = -T22 L21 T11 at 16 -> 32 and 32 -> 64 on
+            //      independent warp-level tf32 MMAs.  Tf's blocks above the diagonal
+            //      blocks stay zero, so every product runs over whole blocks.
             if (h == 0 && lane < 16) {
                 // diagonal block kw, column j: T[r][j] = [r == j] - sum_{s<r} L[r][s] T[s][j]
                 const int j = lane, B0 = 16 * kw;
@@ -1008,7 +1016,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes of the state
+            if (lane == 0) {   // each warp its lanes of the state (bf16 copy, scaled fp32)
+                mbar_arrive(bar(B_SRDY));
+                if (SPLIT_CARRY) mbar_arrive(bar(B_SSCL));
+            }
         }
 
 #pragma unroll 1
@@ -1070,30 +1081,73 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             if (srow == 0) TRACE(c, 12);
             tc_fence_after();
             const float gC_next = (gated && !last) ? vec((c + 1) % NST)[V_GC / 4] : 1.f;
+            if (last) {
 #pragma unroll 1
-            for (int q4 = 0; q4 < 2; ++q4) {   // i = 64 q4 .. 64 q4 + 63: one TMEM round trip
-                float v[64];
-                tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
-                if (srow == 0 && q4 == 0) TRACE(c, 23);
-                if (last) {   // S_T[i][j], consecutive j across the warp
+                for (int q4 = 0; q4 < 2; ++q4) {   // S_T[i][j], consecutive j across the warp
+                    float v[64];
+                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
 #pragma unroll
                     for (int e = 0; e < 64; ++e) a.S_T[(chain * D + 64 * q4 + e) * D + srow] = v[e];
-                } else {
+                }
+            } else if constexpr (SPLIT_CARRY) {
+                // (few chains: the state path's latency sets the period)
+                // the bf16 copy first: the next chunk's R^T and O1 wait only for it
+#pragma unroll 1
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    float v[64];
+                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+                    if (srow == 0 && q4 == 0) TRACE(c, 23);
                     put_sb(64 * q4, v);
                     put_sb(64 * q4 + 32, v + 32);
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) v[e] *= gC_next;
-#pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
+                if (srow == 0) TRACE(c, 13);
+                // then the fp32 state pre-scaled by the next chunk's total decay, which
+                // the next chunk's S update waits for (linear attention: no decay)
+                if (gated) {
+#pragma unroll 1
+                    for (int q4 = 0; q4 < 2; ++q4) {
+                        float v[64];
+                        tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) v[e] *= gC_next;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                }
+                if (lane == 0) mbar_arrive(bar(B_SSCL));
+            } else {
+                // (many chains: fewer TMEM round trips)
+                // one TMEM round trip per half: the bf16 copy and the fp32 state
+                // pre-scaled by the next chunk's total decay (linear attention: no decay)
+#pragma unroll 1
+                for (int q4 = 0; q4 < 2; ++q4) {
+                    float v[64];
+                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+                    if (srow == 0 && q4 == 0) TRACE(c, 23);
+                    put_sb(64 * q4, v);
+                    put_sb(64 * q4 + 32, v + 32);
+                    if (gated) {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) v[e] *= gC_next;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
+                if (srow == 0) TRACE(c, 13);
             }
-            if (srow == 0) TRACE(c, 24);
-            tmem_st_wait();
-            if (srow == 0) TRACE(c, 25);
-            tc_fence_before();
-            __syncwarp();
-            if (!last && lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
-            if (srow == 0) TRACE(c, 13);
 
             // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t, staged as a [t][j] bf16 tile
             //      in the R^T buffer (free once S(c) and O2(c) are done: s_done),
@@ -1202,11 +1256,23 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
         !make_map(&tv, a.v, a.T, a.n_chains) ||
         !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = a.mode == FW_LINATTN ? chunked_kernel<false, false>
-              : a.mode == FW_FALCON1 ? chunked_kernel<true, true> : chunked_kernel<true, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_ALLOC);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    // With chains on at most about 55 % of the SMs (a chain per SM), the state path's
+    // serial chain sets each chain's period, and the decay scaling of the state
+    // moves off it (measured crossover between 80 and 96 chains on 152 SMs).
+    const bool split = 20 * a.n_chains <= 11 * (int64_t)sms;
+    auto kern = a.mode == FW_LINATTN ? chunked_kernel<false, false, false>
+              : a.mode == FW_FALCON1 ? (split ? chunked_kernel<true, true, true>
+                                              : chunked_kernel<true, true, false>)
+                                     : (split ? chunked_kernel<true, false, true>
+                                              : chunked_kernel<true, false, false>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)SMEM_ALLOC)) != cudaSuccess)
+        return e;
     kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
     return cudaGetLastError();
 }
