@@ -418,13 +418,23 @@ def cpu_baseline(w, x=None, budget_s=10.0):
                       % (done, n_all, threads, w.T, w.d, dt)}
 
 
+def headline_config(w, world):
+    """The `config` object of the bench line, shared by both arms."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d,
+            "mode": w.mode, "state": "fp32", "global_batch": w.B * world,
+            "seq_len": w.T, "parallelism": "replicas x%d (independent chains)" % world,
+            "l2": "inputs larger than L2 (%.0f MB moved per step)"
+                  % (algorithmic_bytes_prefill(w) / 1e6)}
+
+
 def run_reference(args):
-    """Reference arm: the fp64 oracle as it stands, timed on the host cores."""
-    import oracle
-    oracle.build()
+    """Reference arm: the fp64 oracle as it stands, timed on the host cores
+    (rank 0 only; other ranks return without work)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle
+    oracle.build()
     w = I.WORKLOADS[args.workload]
     threads = oracle.default_threads()
     n = max(1, min(w.B * w.H, threads))
@@ -448,7 +458,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "mode": w.mode},
+        "config": headline_config(w, args.gpus),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -578,10 +588,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d_k": w.d, "d_v": w.d,
-                   "mode": w.mode, "state": "fp32", "global_batch": w.B * world,
-                   "seq_len": w.T, "parallelism": "replicas x%d (independent chains)" % world,
-                   "l2": "inputs larger than L2 (%.0f MB moved per step)" % (algo_bytes / 1e6)},
+        "config": headline_config(w, world),
         "roofline": roof,
         "tensor": {"matmul_tflops": mm_tf, "peak": peaks["bf16"],
                    "frac": mm_tf / peaks["bf16"], "chunk": 64,

@@ -88,3 +88,26 @@ def test_alu_roofline_flop_counts_per_head_token():
     assert per("falcon3a_bf16") == 4 + 2
     assert per("falcon2_bf16") == 1 + 1 + 2     # a step per value column: W = 1
     assert per("falcon2_bf16", mode="falcon2a") == 1 + 2
+
+
+def test_reference_arm_line(capsys, monkeypatch):
+    # the reference arm times the oracle on the host and prints one line with the
+    # GPU arm's metric, unit and config, an e2e object without host copies, and
+    # a cpu_baseline describing the run; ranks other than 0 print nothing
+    import argparse
+    args = argparse.Namespace(workload=bench.HEADLINE, gpus=1, steps=1, warmup=0)
+    monkeypatch.setenv("RANK", "1")
+    bench.run_reference(args)
+    assert capsys.readouterr().out == ""
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    from linear_token_mixer_gb300 import inputs as I
+    w = I.WORKLOADS[bench.HEADLINE]
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["config"] == bench.headline_config(w, 1)
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
