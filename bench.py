@@ -55,6 +55,7 @@ KERNEL_SOURCES = {
     "recurrent (SIMT)": ("fw_recurrent.cu", "fw_internal.cuh"),
     "window prefill (SIMT)": ("fw_window_prefill.cu", "fw_window.cuh", "fw_sm100.cuh",
                               "fw_internal.cuh"),
+    "decode step": ("fw_decode.cu",),
 }
 
 
@@ -97,14 +98,57 @@ def algorithmic_bytes_prefill(w):
     return ht * per_ht + state * (2 if w.s0_std > 0 else 1)
 
 
+def prefill_kernel(w, algo="auto"):
+    """The kernel fw_prefill picks for a workload, as the library dispatches it:
+    a step per value channel (Falcon-2 / 2A) on the staged per-token kernel,
+    then the chunked tensor-core kernel where it takes the call (bf16, d = 128;
+    Falcon-1 / 1A only with phi = identity), else the per-token kernel."""
+    if algo == "recurrent":
+        return "recurrent (SIMT)"
+    if w.mode in ("falcon2", "falcon2a"):
+        return "window prefill (SIMT)"
+    chunked = (w.dtype == torch.bfloat16 and w.d == 128 and
+               (w.mode == "linattn" or w.phi == "identity"))
+    return "chunked prefill" if chunked else "recurrent (SIMT)"
+
+
 def matmul_flops_prefill(w, C=64):
     """Dense matmul FLOPs of the chunked form per launch: Falcon-1
     10 C d + 6 d^2 per head-token; linear attention and Falcon-1A (no
-    residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y)."""
+    residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y).
+    None where the launch runs no tensor-core kernel."""
+    if prefill_kernel(w) != "chunked prefill":
+        return None
     ht = w.B * w.H * w.T
-    if w.mode in ("falcon1", "falcon2"):
+    if w.mode == "falcon1":
         return ht * (10 * C * w.d + 6 * w.d * w.d)
     return ht * (4 * C * w.d + 4 * w.d * w.d)
+
+
+# workloads the headline (fw_prefill) can run: the window family has its own call
+PREFILL_WORKLOADS = sorted(n for n, w in I.WORKLOADS.items()
+                           if w.mode not in ("falcon3", "falcon3a"))
+
+
+def oracle_run(oracle, w, x, threads):
+    """The fp64 oracle entry that computes workload w's mode, run on the input
+    dict x.  Returns the name of the entry that ran."""
+    if w.mode in ("falcon1", "falcon1a"):
+        oracle.falcon1(x["q"], x["k"], x["v"], x["beta"], x["lam"], S0=x["S0"], phi=w.phi,
+                       eps=w.eps, nthreads=threads, inner=(w.mode == "falcon1a"))
+        return w.mode
+    if w.mode in ("falcon2", "falcon2a"):
+        oracle.falcon2(x["q"], x["k"], x["v"], x["beta"], x["lam"], S0=x["S0"], phi=w.phi,
+                       eps=w.eps, nthreads=threads, inner=(w.mode == "falcon2a"))
+        return w.mode
+    if w.mode in ("falcon3", "falcon3a"):
+        oracle.falcon3(x["q"], x["k"], x["v"], x["beta"], x["lam"], w.window, S0=x["S0"],
+                       phi=w.phi, eps=w.eps, nthreads=threads, inner=(w.mode == "falcon3a"))
+        return w.mode
+    if w.mode == "linattn":
+        oracle.linattn(x["q"], x["k"], x["v"], S0=x["S0"], phi=w.phi, nthreads=threads)
+        return "linattn"
+    raise ValueError("no oracle entry for mode %r" % w.mode)
 
 
 def window_flops(w):
@@ -229,9 +273,11 @@ def bench_prefill(w, K, W, dev, fw, algo="auto", rbw=False, same_pair=False):
         "ms_per_step": total / K,
         "kernel_ms": kern_ms,
         "hbm_gbs": algorithmic_bytes_prefill(w) / (kern_ms / 1e3) / 1e9,
-        "matmul_tflops": matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12,
+        "matmul_tflops": (matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12
+                          if algo == "auto" and matmul_flops_prefill(w) else None),
         "recurrence_tflops": recurrence_flops(w) / (kern_ms / 1e3) / 1e12,
         "algo": algo,
+        "kernel": prefill_kernel(w, algo),
     }
     if rbw or same_pair:
         res["flags"] = [f for f, on in (("rbw", rbw), ("same_pair", same_pair)) if on]
@@ -378,9 +424,15 @@ def bench_decode(K_steps, W, dev, fw):
     fw.check(stream)
     kern_ms = statistics.mean(per)
     nbytes = Bn * H * (2 * d * d * 4 + 4 * d * 2 + 8)
-    return {"steps_per_s": K_steps / (total / 1e3), "tokens_per_s": Bn * K_steps / (total / 1e3),
-            "kernel_ms": kern_ms, "hbm_gbs": nbytes / (kern_ms / 1e3) / 1e9,
-            "bytes_per_step": nbytes, "steps": K_steps}
+    res = {"steps_per_s": K_steps / (total / 1e3), "tokens_per_s": Bn * K_steps / (total / 1e3),
+           "kernel_ms": kern_ms, "hbm_gbs": nbytes / (kern_ms / 1e3) / 1e9,
+           "bytes_per_step": nbytes, "steps": K_steps}
+    # the DRAM bytes ncu counted for one launch of this kernel (part of the state is
+    # still in L2 from the previous step), and the rate on those bytes
+    dram = stored_traffic("decode step", "decode")
+    res["dram_bytes_per_launch"] = dram
+    res["dram_gbs"] = dram / (kern_ms / 1e3) / 1e9 if dram else None
+    return res
 
 
 def cpu_baseline(w, x=None, budget_s=10.0):
@@ -398,22 +450,20 @@ def cpu_baseline(w, x=None, budget_s=10.0):
     flat = {k: (t.reshape((1, n_all) + tuple(t.shape[2:])) if t is not None else None)
             for k, t in x.items()}
     done, dt = 0, 0.0
+    ran = None
     while done < n_all and dt < budget_s:
         n = min(threads, n_all - done)
         sub = {k: (t[:, done:done + n].contiguous() if t is not None else None)
                for k, t in flat.items()}
         t0 = time.perf_counter()
-        if w.mode == "falcon1":
-            oracle.falcon1(sub["q"], sub["k"], sub["v"], sub["beta"], sub["lam"], S0=sub["S0"],
-                           eps=w.eps, nthreads=threads)
-        else:
-            oracle.linattn(sub["q"], sub["k"], sub["v"], phi=w.phi, nthreads=threads)
+        ran = oracle_run(oracle, w, sub, threads)
         dt += time.perf_counter() - t0
         done += n
     # tokens/s of the whole workload: chains are independent, so the sample's
     # head-token rate carries over; one token = H head-tokens.
     ht_rate = done * w.T / dt
     return {"value": ht_rate / w.H, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "oracle": ran,
             "sample": "%d of %d chains (B*H) in groups of %d, full T=%d, d=%d, fp64, %.2f s"
                       % (done, n_all, threads, w.T, w.d, dt)}
 
@@ -439,11 +489,10 @@ def run_reference(args):
     threads = oracle.default_threads()
     n = max(1, min(w.B * w.H, threads))
     sub = I.prefill_inputs(w.with_shape(B=1, H=n))
+    ran = []
 
     def fn():
-        oracle.falcon1(sub["q"], sub["k"], sub["v"], sub["beta"], sub["lam"], S0=sub["S0"],
-                       eps=w.eps, nthreads=threads) if w.mode == "falcon1" else \
-            oracle.linattn(sub["q"], sub["k"], sub["v"], phi=w.phi, nthreads=threads)
+        ran.append(oracle_run(oracle, w, sub, threads))
 
     for _ in range(args.warmup):
         fn()
@@ -460,7 +509,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": headline_config(w, args.gpus),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "oracle": ran[-1], "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -479,6 +528,8 @@ def run_sub(name, K, W, dev, fw, peaks):
     else:
         raise SystemExit("unknown sub-benchmark %r" % name)
     r["hbm_frac"] = r["hbm_gbs"] / peaks["hbm"]
+    if r.get("dram_gbs"):
+        r["dram_frac"] = r["dram_gbs"] / peaks["hbm"]
     r["workload"] = name
     return r
 
@@ -489,7 +540,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=PREFILL_WORKLOADS)
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
     ap.add_argument("--sub", default=None,
@@ -567,20 +618,22 @@ def main():
 
     algo_bytes = algorithmic_bytes_prefill(w)
     achieved_gbs = algo_bytes / (kern_ms / 1e3) / 1e9
-    chunked = w.dtype == torch.bfloat16 and w.d == 128
-    if chunked:
+    kname = prefill_kernel(w)
+    if kname == "chunked prefill":
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm"],
-                "traffic": stored_traffic("chunked prefill", w.name),
-                "kernel": "chunked prefill", "peak_source": peaks["src"],
+                "traffic": stored_traffic(kname, w.name),
+                "kernel": kname, "peak_source": peaks["src"],
                 "algorithmic_bytes_per_launch": algo_bytes}
     else:
-        tf = recurrence_flops(w) / (kern_ms / 1e3) / 1e12
+        flops = window_flops(w) if kname == "window prefill (SIMT)" else recurrence_flops(w)
+        tf = flops / (kern_ms / 1e3) / 1e12
         roof = {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
                 "frac": tf / ALU_FP32_TFLOPS,
-                "traffic": stored_traffic("recurrent (SIMT)", w.name), "kernel": "recurrent (SIMT)",
+                "traffic": stored_traffic(kname, w.name), "kernel": kname,
                 "peak_source": "152 SMs x 128 FP32 lanes x 2 x 2.07 GHz"}
-    mm_tf = matmul_flops_prefill(w) / (kern_ms / 1e3) / 1e12
+    mm = matmul_flops_prefill(w)
+    mm_tf = mm / (kern_ms / 1e3) / 1e12 if mm else None
 
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -590,9 +643,10 @@ def main():
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": headline_config(w, world),
         "roofline": roof,
-        "tensor": {"matmul_tflops": mm_tf, "peak": peaks["bf16"],
-                   "frac": mm_tf / peaks["bf16"], "chunk": 64,
-                   "note": "dense matmul FLOPs of the chunked form (10Cd+6d^2 per head-token)"},
+        "tensor": ({"matmul_tflops": mm_tf, "peak": peaks["bf16"],
+                    "frac": mm_tf / peaks["bf16"], "chunk": 64,
+                    "note": "dense matmul FLOPs of the chunked form (10Cd+6d^2 per head-token)"}
+                   if mm_tf else None),
         "gpu_launches": args.steps,
         "kernel_ms": kern_ms,
     }
@@ -617,6 +671,7 @@ def main():
             extra[w.name + "+rbw+same_pair"] = r
             dec = bench_decode(I.DECODE["steps"], 3, dev, fw)
             dec["hbm_frac"] = dec["hbm_gbs"] / peaks["hbm"]
+            dec["dram_frac"] = dec["dram_gbs"] / peaks["hbm"] if dec["dram_gbs"] else None
             extra["decode"] = dec
             # the window family (Falcon-3 / 3A, W = 4): prefill and decode step
             for name in ("falcon3_bf16", "falcon3a_bf16"):

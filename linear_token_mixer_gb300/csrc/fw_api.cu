@@ -163,6 +163,10 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     if (overlaps(S_T, ns, q, nx) || overlaps(S_T, ns, k, nx) || overlaps(S_T, ns, v, nx))
         return FW_ERR_ARG;
     if (S0 && S0 != S_T && overlaps(S_T, ns, S0, ns)) return FW_ERR_ARG;
+    // k_init is read while other chains' outputs are being written
+    const size_t nki = (size_t)nc * d * esz;
+    if (k_init && (overlaps(o, nx, k_init, nki) || overlaps(S_T, ns, k_init, nki)))
+        return FW_ERR_ARG;
 
     PrefillArgs a;
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.lam = lambda; a.S0 = S0;

@@ -17,6 +17,38 @@ def rel_l2(got, ref):
     return float(num / den)
 
 
+def per_chain(got, ref, lead=2):
+    """Relative L2 of every chain: the first `lead` axes ([B, H]) index the
+    chains, the rest is one chain's tensor.  Returns an array of B*H values."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    n = int(np.prod(ref.shape[:lead]))
+    g = got.reshape(n, -1)
+    r = ref.reshape(n, -1)
+    num = np.linalg.norm(g - r, axis=1)
+    den = np.linalg.norm(r, axis=1)
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+
+
+def gate(got, ref, tol, what="", lead=2):
+    """Gate the whole tensor and every chain on its own at `tol`; the message
+    names the worst chain (flat b*H + h index) and its relative L2."""
+    whole = rel_l2(got, ref)
+    pc = per_chain(got, ref, lead)
+    worst = int(np.argmax(pc)) if pc.size else -1
+    wv = float(pc[worst]) if pc.size else 0.0
+    assert whole <= tol and wv <= tol, (
+        "%s: rel-L2 whole %.3e, worst chain %d at %.3e (gate %.0e)" % (what, whole, worst, wv, tol))
+    return whole, wv
+
+
+def gate_prefill(o, o_ref, S, S_ref, tol):
+    """o [B,H,T,d] and S_T [B,H,d,d] against the oracle, whole and per chain."""
+    eo = gate(o, o_ref, tol, "o")
+    es = gate(S, S_ref, tol, "S_T")
+    return eo, es
+
+
 def to64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 

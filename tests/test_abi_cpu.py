@@ -78,6 +78,7 @@ def call_prefill(L, q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init
     (dict(k_init=P[8] + 2), -4), (dict(beta=P[3] + 4), -4),
     (dict(eps=-1.0), -9), (dict(eps=float("nan")), -9), (dict(o=P[0]), -9),
     (dict(S_T=P[1]), -9), (dict(S0=P[6] + 16), -9),
+    (dict(k_init=P[5] + 16), -9), (dict(k_init=P[6] + 64), -9),   # an output overlaps k_init
 ])
 def test_prefill_validation(L, kw, code):
     assert call_prefill(L, **kw) == code

@@ -111,3 +111,41 @@ def test_reference_arm_line(capsys, monkeypatch):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s",
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("name", ["falcon1_bf16", "falcon1a_bf16", "falcon2_bf16", "linattn_bf16"])
+def test_reference_arm_runs_the_oracle_of_the_workload_mode(capsys, monkeypatch, name):
+    # --impl reference with any headline workload times the oracle entry of that
+    # workload's own mode (not another mode's), and says which one ran
+    import argparse
+    import oracle
+    from linear_token_mixer_gb300 import inputs as I
+    calls = []
+    for fn in ("falcon1", "falcon2", "falcon3", "linattn"):
+        real = getattr(oracle, fn)
+        monkeypatch.setattr(oracle, fn, (lambda f, r: lambda *a, **k: (calls.append((f, k.get("inner", False))), r(*a, **k))[1])(fn, real))
+    w = I.WORKLOADS[name]
+    monkeypatch.setattr(I, "WORKLOADS", dict(I.WORKLOADS, **{name: w.with_shape(T=64)}))
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(argparse.Namespace(workload=name, gpus=1, steps=1, warmup=0))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["cpu_baseline"]["oracle"] == w.mode
+    fam = {"falcon1": "falcon1", "falcon1a": "falcon1", "falcon2": "falcon2",
+           "falcon2a": "falcon2", "linattn": "linattn"}[w.mode]
+    assert calls and all(c == (fam, w.mode.endswith("a")) for c in calls), calls
+    assert line["config"]["mode"] == w.mode
+
+
+def test_headline_kernel_labels_follow_the_dispatch():
+    from linear_token_mixer_gb300 import inputs as I
+    W = I.WORKLOADS
+    assert bench.prefill_kernel(W["falcon1_bf16"]) == "chunked prefill"
+    assert bench.prefill_kernel(W["linattn_bf16"]) == "chunked prefill"
+    assert bench.prefill_kernel(W["falcon1_fp32"]) == "recurrent (SIMT)"
+    assert bench.prefill_kernel(W["falcon1_bf16"].with_shape(phi="elu1")) == "recurrent (SIMT)"
+    assert bench.prefill_kernel(W["falcon2_bf16"]) == "window prefill (SIMT)"
+    # no tensor-core FLOPs are claimed for a launch that runs no tensor-core kernel
+    assert bench.matmul_flops_prefill(W["falcon2_bf16"]) is None
+    assert bench.matmul_flops_prefill(W["falcon1_fp32"]) is None
+    assert bench.matmul_flops_prefill(W["falcon1_bf16"]) > 0
+    assert "falcon3_bf16" not in bench.PREFILL_WORKLOADS

@@ -13,7 +13,7 @@ import torch
 import oracle
 from linear_token_mixer_gb300 import fw
 from linear_token_mixer_gb300 import inputs as I
-from tests.parity_util import TOL, rel_l2, select_chains, to64
+from tests.parity_util import TOL, gate_prefill, rel_l2, select_chains, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -63,8 +63,7 @@ def _assert_close(w, got, ref):
     tol = TOL[w.dtype]
     o, S, win = got
     o_ref, S_ref, win_ref = ref
-    eo, es = rel_l2(to64(o), o_ref), rel_l2(to64(S), S_ref)
-    assert eo <= tol and es <= tol, (eo, es)
+    eo, es = gate_prefill(to64(o), o_ref, to64(S), S_ref, tol)
     if w.window > 1:
         np.testing.assert_array_equal(win[2].cpu().numpy(), win_ref[2])
         ex, ey = rel_l2(to64(win[0]), win_ref[0]), rel_l2(to64(win[1]), win_ref[1])
@@ -195,8 +194,7 @@ def test_full_size_window_prefill_sampled_chains(name):
                          S0=sub["S0"], eps=w.eps, inner=(w.mode == "falcon3a"))
     of = o.reshape(-1, w.T, w.d)[idx].unsqueeze(0)
     Sf = S.reshape(-1, w.d, w.d)[idx].unsqueeze(0)
-    eo, es = rel_l2(to64(of), ref[0]), rel_l2(to64(Sf), ref[1])
-    assert eo <= TOL[w.dtype] and es <= TOL[w.dtype], (eo, es)
+    gate_prefill(to64(of), ref[0], to64(Sf), ref[1], TOL[w.dtype])
     assert torch.isfinite(o.float()).all() and torch.isfinite(S).all()
 
 
