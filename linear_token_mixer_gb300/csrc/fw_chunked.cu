@@ -111,11 +111,16 @@ constexpr uint64_t kDrainNs = 2000000000ull;
 // Optional phase timestamps of CTA 0 (instrumented builds only).
 #ifdef FW_TRACE
 constexpr int kTraceEv = 32, kTraceChunks = 64;
-__device__ unsigned long long g_trace[kTraceChunks * kTraceEv];
+// per-chunk phase stamps, then per-warp stamps of four publications (64 x 4 x 16)
+__device__ unsigned long long g_trace[kTraceChunks * kTraceEv + kTraceChunks * 64];
 #define TRACE(c, ev) \
     do { if (blockIdx.x == 0 && (c) < kTraceChunks) g_trace[(c) * kTraceEv + (ev)] = globaltimer(); } while (0)
+#define TRACEW(c, ev) \
+    do { if (blockIdx.x == 0 && (c) < kTraceChunks && (threadIdx.x & 31) == 0) \
+        g_trace[kTraceChunks * kTraceEv + ((c) * 4 + (ev)) * 16 + (threadIdx.x >> 5)] = globaltimer(); } while (0)
 #else
 #define TRACE(c, ev) do { } while (0)
+#define TRACEW(c, ev) do { } while (0)
 #endif
 
 // fp32 64x64 matrix with its 16-byte groups XOR-swizzled by row (conflict-free
@@ -138,12 +143,14 @@ __device__ __forceinline__ void unpack8(const uint4 u, float *f) {
     }
 }
 
-// Bounded wait for the single-thread roles (producer, MMA issuers): parked like
-// the group waits (a spinning warp would steal issue slots from the math warps
-// that share its scheduler).
-__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, uint64_t limit,
-                                          volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded waits.  The fast path (the phase is already complete) is inline; the
+// slow path is one out-of-line function shared by every call site, so that the
+// roles' per-chunk code stays short (each role's loop runs once per chunk and
+// competes with the other roles for the instruction caches).  A waiting thread is
+// parked (issuing nothing) between polls, and gives up on expiry or as soon as
+// another role has aborted.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit,
+                                       volatile int *abort_flag) {
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
@@ -152,17 +159,15 @@ __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit,
                                          volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        // parked until the phase completes (or ~100 us pass): no issue slots spent
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer() - t0 > limit) return false;
-    }
+    return wait_slow(bar, parity, limit, abort_flag);
+}
+
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, uint64_t limit,
+                                          volatile int *abort_flag) {
+    return wait_bar(bar, parity, limit, abort_flag);
 }
 
 // tf32 fragments of a 16x8 A tile / 8x8 B tile of a swizzled fp32 matrix.
@@ -194,8 +199,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
                const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-aligned base, derived from the shared array itself so that every
+    // pointer below stays in the shared address space (plain shared loads)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -253,36 +259,51 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const int shift = shifted ? 1 : 0;
             int nfill[NST] = {}, ny = 0;
             bool ok = true;
-            for (int c = 0; c < nch && ok; ++c) {
-                const int b = c % NST;
-                if (c >= NST && !wait_fast(bar(B_EMPTY0 + b), (uint32_t)((c / NST) - 1) & 1u, limit, s_abort)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t st = xq(b);
-                const int y = c * C;
-                const uint32_t full = bar(B_FULL0 + b);
-                mbar_expect_tx(full, gated ? 32 * KB : 48 * KB);
-                tma_load_3d(st + XQ_X0, &tmk, 0, y - shift, (int)chain, full);
-                tma_load_3d(st + XQ_X1, &tmk, 64, y - shift, (int)chain, full);
-                tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
-                tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
-                if (!gated) {
-                    const uint32_t yv = yv_of(b);
-                    tma_load_3d(yv, &tmv, 0, y, (int)chain, full);
-                    tma_load_3d(yv + 8 * KB, &tmv, 64, y, (int)chain, full);
-                }
-                ++nfill[b];
-                TRACE(c, 19);
-                if (gated) {
-                    if (c >= 1 && !wait_fast(bar(B_YFREE), (uint32_t)(c - 1) & 1u, limit, s_abort)) {
-                        ok = false;
-                        break;
+            // Falcon-1 / 1A: the single V tile of chunk cy can load once the U^T MMA of
+            // chunk cy-1 has read the previous one.  The X/Q ring and the V tile are
+            // polled independently, so a late V never holds back the ring.
+            int cx = 0, cy = 0;
+            uint64_t t_last = globaltimer();
+            while (cx < nch || (gated && cy < nch)) {
+                bool progressed = false;
+                if (cx < nch) {
+                    const int b = cx % NST;
+                    if (cx < NST || mbar_test(bar(B_EMPTY0 + b), (uint32_t)((cx / NST) - 1) & 1u)) {
+                        const uint32_t st = xq(b);
+                        const int y = cx * C;
+                        const uint32_t full = bar(B_FULL0 + b);
+                        mbar_expect_tx(full, gated ? 32 * KB : 48 * KB);
+                        tma_load_3d(st + XQ_X0, &tmk, 0, y - shift, (int)chain, full);
+                        tma_load_3d(st + XQ_X1, &tmk, 64, y - shift, (int)chain, full);
+                        tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
+                        tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
+                        if (!gated) {
+                            const uint32_t yv = yv_of(b);
+                            tma_load_3d(yv, &tmv, 0, y, (int)chain, full);
+                            tma_load_3d(yv + 8 * KB, &tmv, 64, y, (int)chain, full);
+                        }
+                        ++nfill[b];
+                        TRACE(cx, 19);
+                        ++cx;
+                        progressed = true;
                     }
+                }
+                if (gated && cy < nch && cy < cx &&
+                    (cy == 0 || mbar_test(bar(B_YFREE), (uint32_t)(cy - 1) & 1u))) {
+                    const int y = cy * C;
                     mbar_expect_tx(bar(B_FULLY), 16 * KB);
                     tma_load_3d(sb + OFF_Y0, &tmv, 0, y, (int)chain, bar(B_FULLY));
                     tma_load_3d(sb + OFF_Y0 + 8 * KB, &tmv, 64, y, (int)chain, bar(B_FULLY));
                     ++ny;
+                    ++cy;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = globaltimer();
+                } else {
+                    if (*s_abort) { ok = false; break; }
+                    if (globaltimer() - t_last > limit) { ok = false; break; }
+                    __nanosleep(100);
                 }
             }
             if (!ok) fail_now();
@@ -703,50 +724,54 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (bar_or(BAR_KG, KGROUP, !w)) return false;
             }
             tc_fence_after();
-            float g[32];   // row kt of G = [X;Q] X^T, columns 32h..32h+31
-            tmem_ld32(tmem + lane_base + COL_G + 32 * h, g);
-                // ---- L and P from G, columns 32h..32h+31 of row kt.  A half's running
-                //      product starts from prod_{i=32}^{u} gamma_i when its row reaches
-                //      past column 31 (division-free).
-                {
-                    const float4 *eta4 = reinterpret_cast<const float4 *>(vg + V_ETA / 4) + 8 * h;
-                    const float4 *gam4 = reinterpret_cast<const float4 *>(vg + V_GAM / 4) + 8 * h;
-                    const bool lrow = kt < C;
-                    if (lrow && !falcon) {
-                        // linear attention needs no L
-                    } else {
-                        const int t = lrow ? kt : kt - C;
-                        // last active column: L is strictly lower; P includes the
-                        // diagonal, except when the read comes before the write
-                        const int top = (lrow || rbw) ? t - 1 : t;
-                        float dz = 1.f;
-                        if (h == 0 && top >= 32) dz = vg[V_Q32 / 4 + top];
+            // ---- L and P from G, columns 32h..32h+31 of row kt, in two rolled 16-column
+            //      steps from the right.  A half's running product starts from
+            //      prod_{i=32}^{u} gamma_i when its row reaches past column 31
+            //      (division-free).
+            {
+                const bool lrow = kt < C;
+                if (lrow && !falcon) {
+                    // linear attention and Falcon-1A need no L
+                } else {
+                    const int t = lrow ? kt : kt - C;
+                    // last active column: L is strictly lower; P includes the
+                    // diagonal, except when the read comes before the write
+                    const int top = (lrow || rbw) ? t - 1 : t;
+                    float dz = 1.f;
+                    if (h == 0 && top >= 32) dz = vg[V_Q32 / 4 + top];
+                    const uint32_t pb = sb + ((cc & 1) ? OFF_PB1 : OFF_PB0);
+#pragma unroll 1
+                    for (int sub = 1; sub >= 0; --sub) {
+                        const int col0 = 32 * h + 16 * sub;
+                        float g[16];
+                        tmem_ld16(tmem + lane_base + COL_G + col0, g);
+                        const float4 *eta4 = reinterpret_cast<const float4 *>(vg + V_ETA / 4 + col0);
+                        const float4 *gam4 = reinterpret_cast<const float4 *>(vg + V_GAM / 4 + col0);
 #pragma unroll
-                        for (int q = 7; q >= 0; --q) {
+                        for (int q = 3; q >= 0; --q) {
                             const float4 e4 = eta4[q], y4 = gam4[q];
                             const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
                             const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
                             for (int e = 3; e >= 0; --e) {
-                                const int s2 = 4 * q + e;              // local column
-                                const bool act = (32 * h + s2) <= top;
+                                const int s2 = 4 * q + e;
+                                const bool act = (col0 + s2) <= top;
                                 g[s2] = act ? dz * ev[e] * g[s2] : 0.f;
                                 if (act) dz *= yv[e];
                             }
                         }
                         if (lrow) {
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                *reinterpret_cast<float4 *>(Lw + t * 64 + (((8 * h + q) ^ (t & 15)) << 2)) =
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<float4 *>(Lw + t * 64 + ((((col0 >> 2) + q) ^ (t & 15)) << 2)) =
                                     make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
                         } else {
-                            const uint32_t pb = sb + ((cc & 1) ? OFF_PB1 : OFF_PB0);
-#pragma unroll
-                            for (int c16 = 0; c16 < 4; ++c16)
-                                st_row8_bf16(pb + sw128(t, 4 * h + c16), g + 8 * c16);
+                            st_row8_bf16(pb + sw128((uint32_t)t, (uint32_t)(col0 >> 3)), g);
+                            st_row8_bf16(pb + sw128((uint32_t)t, (uint32_t)(col0 >> 3) + 1), g + 8);
                         }
                     }
                 }
+            }
             tc_fence_before();
             fence_proxy_async();
             if constexpr (falcon) {
@@ -790,12 +815,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         }
         // Falcon-1 (phi = identity): L/P of chunk c+1 runs while the W/U products of
         // chunk c are in flight
-        if (falcon && ok) {
-            ok = lp(0, reinterpret_cast<float *>(sm + lreg(0)));
-            gsync();   // L(0) complete before the first solve reads it
-        }
 #pragma unroll 1
-        for (int c = 0; falcon && c < nch && ok; ++c) {
+        for (int c = -1; falcon && c < nch && ok; ++c) {
+          // (c = -1 only forms L/P of chunk 0: the loop holds the one copy of lp)
+          if (c >= 0) {
             float *vb = vec(c % NST);        // gate block
             const uint32_t tbo = lreg(c);    // L(c), then the bf16 T and -T diag(Gm) of chunk c
             float *Lf = reinterpret_cast<float *>(sm + tbo);
@@ -808,25 +831,30 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             //      independent warp-level tf32 MMAs.  Tf's blocks above the diagonal
             //      blocks stay zero, so every product runs over whole blocks.
             if (h == 0 && lane < 16) {
-                // diagonal block kw, column j: T[r][j] = [r == j] - sum_{s<r} L[r][s] T[s][j]
-                const int j = lane, B0 = 16 * kw;
-                float tc[16];
+                // diagonal block kw, column j, right-looking (the row updates of a step
+                // are independent); the rows' 16-byte groups of L four columns at a time
+                const int B0 = 16 * kw, j = lane;
+                float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc = (r == j) ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-                    for (int s4 = 0; 4 * s4 < r; ++s4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(
-                            Lf + (B0 + r) * 64 + ((((B0 >> 2) + s4) ^ r) << 2));
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                for (int k = 0; k < 4; ++k) {
+                    float lk[16][4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (4 * s4 + e < r) acc = fmaf(-lv[e], tc[4 * s4 + e], acc);
+                    for (int r = 4 * k + 1; r < 16; ++r) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(
+                            Lf + (B0 + r) * 64 + ((((B0 >> 2) + k) ^ r) << 2));
+                        lk[r][0] = v4.x; lk[r][1] = v4.y; lk[r][2] = v4.z; lk[r][3] = v4.w;
                     }
-                    tc[r] = acc;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s2 = 4 * k + e;
+#pragma unroll
+                        for (int r = s2 + 1; r < 16; ++r) x[r] = fmaf(-lk[r][e], x[s2], x[r]);
+                    }
                 }
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Tf[f64i(B0 + r, B0 + j)] = tc[r];
+                for (int r = 0; r < 16; ++r) Tf[f64i(B0 + r, B0 + j)] = x[r];
             } else if (h == 1) {
                 // T[0:16, 16:32] and T[32:48, 48:64] are zero (the merges read them)
                 const int r = kt >> 2, c4 = 4 * (kt & 3);
@@ -949,7 +977,15 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_TRDY));
             if (kidx == 0) TRACE(c, 6);
-            if (c + 1 < nch && !lp(c + 1, Tf)) { ok = false; break; }   // T(c) fp32 is dead
+          }
+            if (c + 1 < nch && !lp(c + 1, reinterpret_cast<float *>(sm + lreg(c + 1)))) {
+                ok = false;   // (for c >= 0: T(c) fp32 is dead)
+                break;
+            }
+            if (c < 0) {
+                gsync();   // L(0) complete before the first solve reads it
+                continue;
+            }
 
             // ---- -W^T -> bf16 rows i, once W^T(c) is done and R(c-1) has read the old one
             {
@@ -1041,18 +1077,19 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (srow < C)   // the gate warp may recycle this gate block once S(c) is done
                     reinterpret_cast<float *>(sm + OFF_SGV)[srow] =
                         vec(b)[(rbw ? V_GM : V_G) / 4 + srow];   // G_{t-1} for a read before the write
-                {
-                    float r[64];
-                    tmem_ld64(tmem + lane_base + COL_R, r);
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {   // columns t = 16q .. 16q+15
+                    float r[16];
+                    tmem_ld16(tmem + lane_base + COL_R + 16 * q, r);
 #pragma unroll
-                    for (int c16 = 0; c16 < 8; ++c16) {
-                        const float4 w0 = *reinterpret_cast<const float4 *>(wc + 8 * c16);
-                        const float4 w1 = *reinterpret_cast<const float4 *>(wc + 8 * c16 + 4);
-                        const float *rr = r + 8 * c16;
+                    for (int c8 = 0; c8 < 2; ++c8) {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(wc + 16 * q + 8 * c8);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(wc + 16 * q + 8 * c8 + 4);
+                        const float *rr = r + 8 * c8;
                         const float w8[8] = {rr[0] * w0.x, rr[1] * w0.y, rr[2] * w0.z, rr[3] * w0.w,
                                              rr[4] * w1.x, rr[5] * w1.y, rr[6] * w1.z, rr[7] * w1.w};
-                        st_row8_bf16(sb + OFF_RA + sw128(srow, c16), rr);
-                        st_row8_bf16(sb + OFF_RB + sw128(srow, c16), w8);
+                        st_row8_bf16(sb + OFF_RA + sw128(srow, 2 * q + c8), rr);
+                        st_row8_bf16(sb + OFF_RB + sw128(srow, 2 * q + c8), w8);
                     }
                 }
                 // each warp publishes its rows of R (the state carry that follows
@@ -1083,40 +1120,39 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const float gC_next = (gated && !last) ? vec((c + 1) % NST)[V_GC / 4] : 1.f;
             if (last) {
 #pragma unroll 1
-                for (int q4 = 0; q4 < 2; ++q4) {   // S_T[i][j], consecutive j across the warp
-                    float v[64];
-                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+                for (int q = 0; q < 4; ++q) {   // S_T[i][j], consecutive j across the warp
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) a.S_T[(chain * D + 64 * q4 + e) * D + srow] = v[e];
+                    for (int e = 0; e < 32; ++e) a.S_T[(chain * D + 32 * q + e) * D + srow] = v[e];
                 }
             } else if constexpr (SPLIT_CARRY) {
                 // (few chains: the state path's latency sets the period)
                 // the bf16 copy first: the next chunk's R^T and O1 wait only for it
 #pragma unroll 1
-                for (int q4 = 0; q4 < 2; ++q4) {
-                    float v[64];
-                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
-                    if (srow == 0 && q4 == 0) TRACE(c, 23);
-                    put_sb(64 * q4, v);
-                    put_sb(64 * q4 + 32, v + 32);
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
+                    if (srow == 0 && q == 0) TRACE(c, 23);
+                    put_sb(32 * q, v);
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
+                TRACEW(c, 3);
                 if (srow == 0) TRACE(c, 13);
                 // then the fp32 state pre-scaled by the next chunk's total decay, which
                 // the next chunk's S update waits for (linear attention: no decay)
                 if (gated) {
 #pragma unroll 1
-                    for (int q4 = 0; q4 < 2; ++q4) {
-                        float v[64];
-                        tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
+                    for (int q = 0; q < 4; ++q) {
+                        float v[32];
+                        tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) v[e] *= gC_next;
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-                            tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
+                        for (int e = 0; e < 32; ++e) v[e] *= gC_next;
+                        tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+                        tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -1125,27 +1161,26 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (lane == 0) mbar_arrive(bar(B_SSCL));
             } else {
                 // (many chains: fewer TMEM round trips)
-                // one TMEM round trip per half: the bf16 copy and the fp32 state
+                // one TMEM round trip per 32 columns: the bf16 copy and the fp32 state
                 // pre-scaled by the next chunk's total decay (linear attention: no decay)
 #pragma unroll 1
-                for (int q4 = 0; q4 < 2; ++q4) {
-                    float v[64];
-                    tmem_ld64(tmem + lane_base + COL_S + 64 * q4, v);
-                    if (srow == 0 && q4 == 0) TRACE(c, 23);
-                    put_sb(64 * q4, v);
-                    put_sb(64 * q4 + 32, v + 32);
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
+                    if (srow == 0 && q == 0) TRACE(c, 23);
+                    put_sb(32 * q, v);
                     if (gated) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) v[e] *= gC_next;
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq)
-                            tmem_st16(tmem + lane_base + COL_S + 64 * q4 + 16 * qq, v + 16 * qq);
+                        for (int e = 0; e < 32; ++e) v[e] *= gC_next;
+                        tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+                        tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_SRDY));   // each warp its lanes
+                TRACEW(c, 3);
                 if (srow == 0) TRACE(c, 13);
             }
 
@@ -1156,22 +1191,21 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 const float *gv = reinterpret_cast<const float *>(sm + OFF_SGV);
                 __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RA) + srow;
 #pragma unroll 1
-                for (int h = 0; h < 2; ++h) {   // (a rolled loop: less code beside the key group's)
-                    float o1[32], o2[32];
-                    tmem_ld32x2(tmem + lane_base + COL_O1 + 32 * h, tmem + lane_base + COL_O2 + 32 * h, o1, o2);
-                    if (srow == 0) TRACE(c, 26 + 2 * h);
+                for (int h = 0; h < 4; ++h) {   // (a rolled loop: short code beside the other roles')
+                    float o1[16], o2[16];
+                    tmem_ld16(tmem + lane_base + COL_O1 + 16 * h, o1);
+                    tmem_ld16(tmem + lane_base + COL_O2 + 16 * h, o2);
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 g4 = gated ? *reinterpret_cast<const float4 *>(gv + 32 * h + 4 * e4)
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const float4 g4 = gated ? *reinterpret_cast<const float4 *>(gv + 16 * h + 4 * e4)
                                                  : make_float4(1.f, 1.f, 1.f, 1.f);
                         const float gg[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int t = 32 * h + 4 * e4 + e;
+                            const int t = 16 * h + 4 * e4 + e;
                             ot[t * D] = __float2bfloat16_rn(fmaf(gg[e], o1[4 * e4 + e], o2[4 * e4 + e]));
                         }
                     }
-                    if (srow == 0) TRACE(c, 27 + 2 * h);
                 }
             }
             fence_proxy_async();
@@ -1245,7 +1279,7 @@ bool chunked_supported(const PrefillArgs &a) {
 
 #ifdef FW_TRACE
 extern "C" int fw_debug_read_trace(unsigned long long *dst, int n) {
-    if (n > kTraceChunks * kTraceEv) n = kTraceChunks * kTraceEv;
+    if (n > kTraceChunks * (kTraceEv + 64)) n = kTraceChunks * (kTraceEv + 64);
     return (int)cudaMemcpyFromSymbol(dst, g_trace, sizeof(unsigned long long) * n);
 }
 #endif
