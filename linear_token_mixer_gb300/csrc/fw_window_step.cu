@@ -1,16 +1,20 @@
 // fw_window_step.cu -- Falcon-3 / 3A single-token decode step, one pass over
 // the state.
 //
-// One thread block (256 threads) per state, streaming S (d x d fp32, d_v
-// innermost) once through registers with 128-bit loads and stores, as the
-// Falcon-1 step does.  The window is the carried pairs plus the new pair
+// Two launches.  The window is the carried pairs plus the new pair
 // (phi(k_prev), v) ("Fast Weight Attention for Continual Learning" paper
-// reading §4.2, §4.3).  While the state's loads are in flight the block
-// stages the window, forms its Gram matrix x_a . x_b and the products
-// x_j . q (one warp per product), and one thread finds mu = lambda_max of the
-// window-average covariance by Jacobi rotations.  From the old state the
-// same pass forms the reads a_j = S^T x_j of every window pair and c = S^T q;
-// then, per value column,
+// reading §4.2, §4.3).
+//   1. window_prep_kernel: a warp per state forms the window's Gram matrix
+//      x_a . x_b and the products x_j . q (warp butterflies); then one lane per
+//      state finds mu = lambda_max of the window-average covariance by Jacobi
+//      rotations, and gamma = 1 - eta lambda and eta / B.  These 2 + W scalars are parked in
+//      the state's own output slot o[s] (at least 128 bytes), which the second
+//      launch reads before it writes the output there: no workspace.
+//   2. window_step_kernel, one thread block (256 threads) per state, streaming
+//      S (d x d fp32, d_v innermost) once through registers with 128-bit loads
+//      and stores, as the Falcon-1 step does, with no eigenvalue work on the
+//      state's critical path.  From the old state the pass forms the reads
+//      a_j = S^T x_j of every window pair and c = S^T q; then, per value column,
 //     r_j = y_j - a_j (3A: y_j),  coef_j = (eta / B) r_j,
 //     o = gamma c + sum_j coef_j (x_j . q)        (= S_new^T q; RBW: o = c),
 //     S <- gamma S + sum_j x_j coef_j^T,
@@ -25,6 +29,99 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Offset of the scalars parked in o[s]: gamma, eta / B, then x_j . q.
+template <typename TIn>
+__device__ __forceinline__ float *parked(const WindowArgs &a, int64_t s, int D) {
+    return reinterpret_cast<float *>(static_cast<TIn *>(a.o) + s * D);
+}
+
+// States per block of the prep launch: a warp per state forms the Gram matrix,
+// then one lane per state (a single warp) runs the rotations, so no two lanes
+// repeat the same eigenvalue work.
+template <int WM> constexpr int prep_states() { return WM <= 4 ? 32 : 16; }
+
+template <int D, int WM, typename TIn>
+__global__ void __launch_bounds__(prep_states<WM>() * 32, WM <= 4 ? 2 : 1)
+window_prep_kernel(WindowArgs a) {
+    constexpr int SPB = prep_states<WM>();
+    constexpr int PL = D / 32;   // elements of a row per lane
+    __shared__ float gram[SPB][WM * WM + WM + 1];   // window Gram matrix, x_j . q, pairs held
+    // the step launch may start now: it streams its state in before it waits for
+    // this grid's scalars
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int W = a.W;
+    {
+        const int64_t s = (int64_t)blockIdx.x * SPB + w;
+        if (s < a.n_chains) {
+            const int64_t cs = (int64_t)(W - 1) * D;
+            int cn = a.cn ? a.cn[s] : 0;
+            cn = cn < 0 ? 0 : (cn > W - 1 ? W - 1 : cn);
+            // window rows j = 0 .. W-2: carried slots (held if j >= W-1-cn); row W-1:
+            // the new pair's key, phi applied; rows past W are zero
+            float x[WM][PL], qv[PL];
+#pragma unroll
+            for (int j = 0; j < WM; ++j)
+#pragma unroll
+                for (int e = 0; e < PL; ++e) {
+                    const int i = lane + 32 * e;
+                    float v = 0.f;
+                    if (j < W - 1) {
+                        if (a.cx && j >= W - 1 - cn) v = a.cx[s * cs + (int64_t)j * D + i];
+                    } else if (j == W - 1) {
+                        v = apply_phi(a.phi, to_f32(static_cast<const TIn *>(a.k)[s * D + i]));
+                    }
+                    x[j][e] = v;
+                }
+#pragma unroll
+            for (int e = 0; e < PL; ++e)
+                qv[e] = to_f32(static_cast<const TIn *>(a.q)[s * D + lane + 32 * e]);
+            auto wsum = [&](float v) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                return v;
+            };
+#pragma unroll
+            for (int i = 0; i < WM; ++i) {
+#pragma unroll
+                for (int j = i; j < WM; ++j) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int e = 0; e < PL; ++e) v = fmaf(x[i][e], x[j][e], v);
+                    v = wsum(v);
+                    if (lane == 0) { gram[w][i * WM + j] = v; gram[w][j * WM + i] = v; }
+                }
+                float v = 0.f;
+#pragma unroll
+                for (int e = 0; e < PL; ++e) v = fmaf(x[i][e], qv[e], v);
+                v = wsum(v);
+                if (lane == 0) gram[w][WM * WM + i] = v;
+            }
+            if (lane == 0) gram[w][WM * WM + WM] = (float)(cn + 1);   // the carried pairs held, and the new one
+        }
+    }
+    __syncthreads();
+    if (w == 0 && lane < SPB) {
+        const int64_t s = (int64_t)blockIdx.x * SPB + lane;
+        if (s < a.n_chains) {
+            float A[WM][WM];
+#pragma unroll
+            for (int i = 0; i < WM; ++i)
+#pragma unroll
+                for (int j = 0; j < WM; ++j) A[i][j] = gram[lane][i * WM + j];
+            const float nb = gram[lane][WM * WM + WM];
+            const float mu = window_max_eig<WM>(A) / nb;
+            const float lt = a.lam[s];
+            const float eta = a.beta[s] / (mu + lt + a.eps);
+            float *sc = parked<TIn>(a, s, D);
+            sc[0] = 1.f - eta * lt;
+            sc[1] = eta / nb;
+#pragma unroll
+            for (int j = 0; j < WM; ++j) sc[2 + j] = gram[lane][WM * WM + j];
+        }
+    }
+}
+
 template <int D, int WM, typename TIn, bool INNER>
 __global__ void __launch_bounds__(kThreads)
 window_step_kernel(WindowArgs a) {
@@ -32,7 +129,7 @@ window_step_kernel(WindowArgs a) {
     constexpr int RPP = kThreads / TPR;    // rows per pass
     constexpr int NP = D / RPP;            // passes
     constexpr int NR = INNER ? 1 : WM + 1; // reads reduced per column group
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int cq = tid % TPR, rg = tid / TPR;
     const int64_t s = blockIdx.x;
     const int W = a.W;
@@ -41,15 +138,15 @@ window_step_kernel(WindowArgs a) {
     __shared__ __align__(16) float xs[WM][D];
     __shared__ __align__(16) float ys[WM][D];
     __shared__ float qs[D];
-    __shared__ float G[WM][WM], Eq[WM], scal[2];
+    __shared__ float Eq[WM], scal[2];
     __shared__ float4 red[RPP][NR][TPR];
+    __shared__ float4 fin[NR][TPR];
 
     const int64_t cs = (int64_t)(W - 1) * D;
     int cn = a.cn ? a.cn[s] : 0;
     cn = cn < 0 ? 0 : (cn > W - 1 ? W - 1 : cn);
     // window rows j = 0 .. W-2: carried slots (held if j >= W-1-cn); row W-1:
-    // the new pair.  Their loads go out before the state's, so the window's
-    // Gram matrix and eigenvalue are formed while the state streams in.
+    // the new pair.  Their loads go out before the state's.
     constexpr int NE = WM * D / kThreads;   // window elements per thread
     float xv[NE], yv[NE];
 #pragma unroll
@@ -73,6 +170,12 @@ window_step_kernel(WindowArgs a) {
     float4 Sr[NP];
 #pragma unroll
     for (int p = 0; p < NP; ++p) Sr[p] = __ldcs(&Sp[(p * RPP + rg) * TPR + cq]);
+    // gamma, eta / B and x_j . q from the prep launch, parked in o[s] (read before
+    // this block writes the output there).  Launched as its dependent, this grid
+    // may start while the prep grid runs: the loads above need nothing from it,
+    // and the wait returns once its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float scv = tid < 2 + WM ? parked<TIn>(a, s, D)[tid] : 0.f;
 
 #pragma unroll
     for (int u = 0; u < NE; ++u) {
@@ -81,52 +184,10 @@ window_step_kernel(WindowArgs a) {
         ys[j][i] = yv[u];
     }
     if (tid < D) qs[tid] = qv0;
+    if (tid < 2) scal[tid] = scv;
+    else if (tid < 2 + WM) Eq[tid - 2] = scv;
     __syncthreads();
 
-    // Gram matrix of the window (upper triangle) and x_j . q, one warp each
-    {
-        const int ng = W * (W + 1) / 2;
-        for (int it = warp; it < ng + W; it += kThreads / 32) {
-            const float *u, *w;
-            int ia = 0, ib = 0;
-            if (it < ng) {
-                int r = it;
-                while (r >= W - ia) { r -= W - ia; ++ia; }
-                ib = ia + r;
-                u = xs[ia];
-                w = xs[ib];
-            } else {
-                ia = it - ng;
-                u = xs[ia];
-                w = qs;
-            }
-            float acc = 0.f;
-#pragma unroll
-            for (int i = lane; i < D; i += 32) acc = fmaf(u[i], w[i], acc);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (lane == 0) {
-                if (it < ng) { G[ia][ib] = acc; G[ib][ia] = acc; }
-                else Eq[ia] = acc;
-            }
-        }
-    }
-
-    __syncthreads();   // Gram matrix complete
-    // mu, eta, gamma while the state's loads are still in flight
-    if (tid == 0) {
-        float A[WM][WM];
-#pragma unroll
-        for (int i = 0; i < WM; ++i)
-#pragma unroll
-            for (int j = 0; j < WM; ++j) A[i][j] = (i < W && j < W) ? G[i][j] : 0.f;
-        const int nb = cn + 1;   // the carried pairs held, and the new one
-        const float mu = window_max_eig<WM>(A) / (float)nb;
-        const float lt = a.lam[s];
-        const float eta = a.beta[s] / (mu + lt + a.eps);
-        scal[0] = 1.f - eta * lt;
-        scal[1] = eta / (float)nb;
-    }
     // reads of the old state (the loads have landed by now)
     float4 pa[WM];
     float4 pc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -156,15 +217,22 @@ window_step_kernel(WindowArgs a) {
             if (j < W) red[rg][j][cq] = pa[j];
     }
     __syncthreads();   // partial reads complete
+    // each read's RPP partials are summed once, by the row group whose index it
+    // carries, then every thread takes the sums of its column quad
+#pragma unroll
+    for (int j = rg; j < NR; j += RPP) {
+        float4 t = red[0][j][cq];
+#pragma unroll
+        for (int g = 1; g < RPP; ++g) {
+            const float4 u = red[g][j][cq];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        fin[j][cq] = t;
+    }
+    __syncthreads();   // sums complete
 
     const float gam = scal[0], cc = scal[1];
-
-    float4 C = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int g = 0; g < RPP; ++g) {
-        const float4 u = red[g][NR - 1][cq];
-        C.x += u.x; C.y += u.y; C.z += u.z; C.w += u.w;
-    }
+    const float4 C = fin[NR - 1][cq];
     float4 coef[WM];
 #pragma unroll
     for (int j = 0; j < WM; ++j) {
@@ -172,12 +240,7 @@ window_step_kernel(WindowArgs a) {
         if (j < W) {
             float4 r = *reinterpret_cast<const float4 *>(&ys[j][cq * 4]);
             if constexpr (!INNER) {
-                float4 A4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int g = 0; g < RPP; ++g) {
-                    const float4 u = red[g][j][cq];
-                    A4.x += u.x; A4.y += u.y; A4.z += u.z; A4.w += u.w;
-                }
+                const float4 A4 = fin[j][cq];
                 r.x -= A4.x; r.y -= A4.y; r.z -= A4.z; r.w -= A4.w;
             }
             coef[j] = make_float4(cc * r.x, cc * r.y, cc * r.z, cc * r.w);
@@ -230,8 +293,23 @@ window_step_kernel(WindowArgs a) {
 
 template <int D, int WM, typename TIn, bool INNER>
 cudaError_t launch_t(const WindowArgs &a, cudaStream_t s) {
-    window_step_kernel<D, WM, TIn, INNER><<<(unsigned)a.n_chains, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    constexpr int SPB = prep_states<WM>();
+    const unsigned nprep = (unsigned)((a.n_chains + SPB - 1) / SPB);
+    window_prep_kernel<D, WM, TIn><<<nprep, SPB * 32, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the step grid is the prep grid's programmatic dependent (it waits in-kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_chains);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, window_step_kernel<D, WM, TIn, INNER>, a);
 }
 
 template <int D, typename TIn>
