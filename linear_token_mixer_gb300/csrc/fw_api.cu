@@ -179,14 +179,17 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     a.wait_ns = g_wait_us.load() * 1000LL;
     a.force_timeout = g_force_timeout.load();
 
-    const bool chunk_ok = chunked_supported(a);
+    const bool chunk_ok = per_channel(mode) ? chunked_chan_supported(a) : chunked_supported(a);
     if (algo == FW_ALGO_CHUNKED && !chunk_ok) return FW_ERR_UNSUPPORTED;
 
     st = device_setup(&a.err);
     if (st != FW_OK) return st;
 
     cudaError_t e;
-    if (algo == FW_ALGO_AUTO && per_channel(mode)) {
+    if (algo != FW_ALGO_RECURRENT && per_channel(mode) && chunk_ok) {
+        // a step per value channel on the chunked tensor-core kernel
+        e = launch_chunked_chan(a, stream);
+    } else if (algo == FW_ALGO_AUTO && per_channel(mode)) {
         // a step per value column: the staged per-token kernel of the window
         // family with a window of one pair
         WindowArgs w{};

@@ -1,0 +1,647 @@
+// fw_chunked_chan.cu -- chunked prefill of the per-channel step (Falcon-2 /
+// Falcon-2A) for bf16 inputs, d_k = d_v = 128.
+//
+// "Fast Weight Attention for Continual Learning" paper reading, §4.2: the
+// squared error is separable by value dimension, so value channel j takes its
+// own step eta_{t,j} = beta_{t,j} / (|x_t|^2 + lambda_t + eps), sharing the
+// residual's feature x_t; §4.4: the chunk's Gram matrix is shared by every
+// channel, and only the triangular system is modulated per channel.  Our chunk
+// form, for one chunk (C = 64 tokens, chunk-local t, s) from state S0, channel j,
+// with gamma_t = 1 - eta_t lambda_t, D[t,s] = prod_{i=s+1..t} gamma_i,
+// G_t = prod_{i<=t} gamma_i, Gm_t = G_{t-1}, A = X X^T, B = Q X^T, U = X S0[:, j],
+// V = Q S0[:, j]:
+//   r_t = y_t - Gm_t U_t - sum_{s<t} D[t-1,s] eta_s A[t,s] r_s   (2A: r_t = y_t)
+//   o_t = G_t V_t + sum_{s<=t} D[t,s] eta_s B[t,s] r_s
+//         (read before the write: Gm_t V_t + sum_{s<t} D[t-1,s] eta_s B[t,s] r_s)
+//   S_C[:, j] = G_{C-1} S0[:, j] + X^T (D[C-1, .] eta r).
+// The shared matrix products run on tcgen05 (the Gram [X;Q] X^T; U^T = S^T X^T
+// and V^T = S^T Q^T with the state transposed in tensor memory, one lane per
+// value channel; the state update S^T += Rw^T X).  Each channel's recurrence
+// over the chunk is one thread: the sums over earlier tokens are block-factored
+// over blocks of NB tokens, D[t-1, s] = P[t-1] (block totals between) Suf[s] for
+// s in an earlier block, so a running vector zhat (rescaled by each finished
+// block's total) turns every cross-block sum into a dot product with a row of
+// A or B; inside a block a direct product runs over at most NB - 1 tokens.  The
+// final zhat is D[C-1, s] eta_s r_s, the state update's weights.  No decay
+// product is ever divided (gamma may be zero or negative).
+//
+// One CTA per chain:
+//   warp 0      TMA producer: X (keys shifted one token unless the same-step
+//               pair; the row before the sequence reads as zero) and Q tiles,
+//               64 x 128 bf16, 128-byte swizzle, in a two-stage ring; the V
+//               tile; the chunk's beta rows (64 x 128 fp32, one bulk copy).
+//   warp 1      MMA issuer: Gram, U^T / V^T, state update.
+//   warp 2      tensor-memory allocation.
+//   warps 4-7   staging group: the Gram tile from tensor memory to fp32 A and B
+//               in shared memory, and 1 / (|x_t|^2 + lambda_t + eps).
+//   warps 8-11  channel group (thread j = value channel j = tensor-memory lane
+//               j): gates, the recurrence above, the outputs, the state carry.
+// Every wait is bounded: on expiry the kernel records an error, the other roles
+// stop at their next wait, copies and MMAs in flight are drained, tensor memory
+// is freed and the kernel exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fw_internal.cuh"
+#include "fw_sm100.cuh"
+
+namespace fw {
+namespace {
+using namespace sm100;
+
+constexpr int C = 64;          // chunk length
+constexpr int D = 128;         // d_k = d_v
+constexpr int NB = 8;          // block of the decay factorisation
+constexpr int NTHREADS = 384;
+constexpr int SG_W0 = 4, CG_W0 = 8;
+constexpr int BAR_SGRP = 1, BAR_CGRP = 2;   // named barriers of the two groups
+constexpr int GROUP = 128;
+constexpr uint32_t KB = 1024;
+constexpr int NST = 2;         // depth of the key/query tile ring
+
+// shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t OFF_XQ = 0;             // NST stages of X0 Q0 X1 Q1 (8 KB each)
+constexpr uint32_t XQ_X0 = 0, XQ_Q0 = 8 * KB, XQ_X1 = 16 * KB, XQ_Q1 = 24 * KB;
+constexpr uint32_t OFF_Y = 64 * KB;        // V tile, two 64-column halves (128-byte swizzle)
+constexpr uint32_t OFF_BETA = 80 * KB;     // beta rows of the chunk, fp32 [t][j]
+constexpr uint32_t OFF_A = 112 * KB;       // X X^T, fp32 [t][s]
+constexpr uint32_t OFF_B = 128 * KB;       // Q X^T, fp32 [t][s]
+constexpr uint32_t OFF_RT = 144 * KB;      // (weights * r)^T, bf16 rows j (K-major A operand)
+constexpr uint32_t OFF_OUT = 160 * KB;     // output tile, bf16 [t][j]
+constexpr uint32_t OFF_Z = 176 * KB;       // zhat per channel, fp32 rows j of ZROW floats
+constexpr int ZROW = 68;                   // 64 + 4 (16-byte groups spread over the banks)
+constexpr uint32_t OFF_VEC = OFF_Z + (uint32_t)D * ZROW * 4;   // inv[64], lambda[64]
+constexpr uint32_t OFF_BAR = OFF_VEC + 512;
+constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
+static_assert(SMEM_ALLOC <= 227 * KB, "shared memory budget");
+static_assert(OFF_VEC % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+
+enum {
+    B_FULL0 = 0, B_EMPTY0 = B_FULL0 + NST, B_FULLY = B_EMPTY0 + NST, B_YFREE, B_FULLB, B_BFREE,
+    B_GDONE, B_GFREE, B_ABRDY, B_ABFREE, B_SRDY, B_UVDONE, B_RRDY, B_SDONE, B_MDRAIN, B_NEVER,
+    B_PATCH, B_COUNT
+};
+static_assert(B_COUNT <= 32, "barrier area");
+
+// tensor-memory columns (128 lanes x 32 bit); the state is held transposed
+// (lane j), with a bf16 copy (two i per column), the A operand of U^T and V^T
+constexpr uint32_t COL_G = 0, COL_U = 64, COL_V = 128, COL_SB = 192, COL_S = 256;
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+__device__ __noinline__ bool cwait_slow(uint32_t bar, uint32_t parity, uint64_t limit,
+                                        volatile int *abort_flag) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) return false;
+    }
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool cwait(uint32_t bar, uint32_t parity, uint64_t limit,
+                                      volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return cwait_slow(bar, parity, limit, abort_flag);
+}
+
+__device__ __forceinline__ void st_row8(uint32_t addr, const float *v) {
+    st_shared_v4(addr, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                 pack_bf16(v[6], v[7]));
+}
+
+// Eight consecutive columns of one lane, loaded and waited for.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool INNER>
+__global__ void __launch_bounds__(NTHREADS, 1)
+chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+            const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-aligned base, derived from the shared array itself (shared-space loads)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t chain = blockIdx.x;
+    const int64_t T = a.T;
+    const int nch = (int)((T + C - 1) / C);
+    const bool shifted = !(a.flags & FW_FLAG_SAME_PAIR);   // x_t = phi(k_{t-1})
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;          // o_t = S_{t-1}^T q_t
+    const uint64_t limit = (uint64_t)a.wait_ns;
+
+    volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_MISC);
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(sm + OFF_MISC + 4);
+    auto bar = [&](int i) -> uint32_t { return sb + OFF_BAR + 8u * (uint32_t)i; };
+    auto xq = [&](int st) -> uint32_t { return sb + OFF_XQ + (uint32_t)st * 32u * KB; };
+    float *inv = reinterpret_cast<float *>(sm + OFF_VEC);
+    float *lamv = inv + 64;
+    auto fail_now = [&]() {
+        *s_abort = 1;
+        atomicExch(a.err, kDevErrTimeout);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < B_COUNT; ++i) {
+            uint32_t n = 1;
+            if (i == B_YFREE || i == B_BFREE || i == B_GFREE || i == B_ABRDY || i == B_ABFREE ||
+                i == B_SRDY || i == B_RRDY)
+                n = 4;   // one arrival per warp of the publishing group
+            mbar_init(bar(i), n);
+        }
+        fence_mbar_init();
+        *s_abort = 0;
+    }
+    if (warp == 2) tmem_alloc(sb + OFF_MISC + 4, TMEM_COLS);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmo);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0) {
+            const int shift = shifted ? 1 : 0;
+            int nfill[NST] = {}, ny = 0, nb = 0;
+            bool ok = true;
+            int cx = 0, cy = 0, cb = 0;
+            uint64_t t_last = globaltimer();
+            while (cx < nch || cy < nch || cb < nch) {
+                bool progressed = false;
+                if (cx < nch) {
+                    const int b = cx % NST;
+                    if (cx < NST || mbar_test(bar(B_EMPTY0 + b), (uint32_t)((cx / NST) - 1) & 1u)) {
+                        const uint32_t st = xq(b);
+                        const int y = cx * C;
+                        const uint32_t full = bar(B_FULL0 + b);
+                        mbar_expect_tx(full, 32 * KB);
+                        tma_load_3d(st + XQ_X0, &tmk, 0, y - shift, (int)chain, full);
+                        tma_load_3d(st + XQ_X1, &tmk, 64, y - shift, (int)chain, full);
+                        tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
+                        tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
+                        ++nfill[b];
+                        ++cx;
+                        progressed = true;
+                    }
+                }
+                if (cy < nch && cy < cx && (cy == 0 || mbar_test(bar(B_YFREE), (uint32_t)(cy - 1) & 1u))) {
+                    const int y = cy * C;
+                    mbar_expect_tx(bar(B_FULLY), 16 * KB);
+                    tma_load_3d(sb + OFF_Y, &tmv, 0, y, (int)chain, bar(B_FULLY));
+                    tma_load_3d(sb + OFF_Y + 8 * KB, &tmv, 64, y, (int)chain, bar(B_FULLY));
+                    ++ny;
+                    ++cy;
+                    progressed = true;
+                }
+                if (cb < nch && cb < cx && (cb == 0 || mbar_test(bar(B_BFREE), (uint32_t)(cb - 1) & 1u))) {
+                    // the chunk's beta rows: contiguous [t][j] fp32, 512 B per token,
+                    // clipped at the chain's end (rows past T are never read)
+                    const int64_t t0 = (int64_t)cb * C;
+                    const int rows = (int)((T - t0) < C ? (T - t0) : C);
+                    const uint32_t bytes = (uint32_t)rows * (uint32_t)D * 4u;
+                    mbar_expect_tx(bar(B_FULLB), bytes);
+                    bulk_g2s(sb + OFF_BETA, a.beta + (chain * T + t0) * D, bytes, bar(B_FULLB));
+                    ++nb;
+                    ++cb;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = globaltimer();
+                } else {
+                    if (*s_abort) { ok = false; break; }
+                    if (globaltimer() - t_last > limit) { ok = false; break; }
+                    __nanosleep(200);
+                }
+            }
+            if (!ok) fail_now();
+            // never leave a copy in flight into this CTA's shared memory
+            for (int b = 0; b < NST; ++b)
+                if (nfill[b]) mbar_wait(bar(B_FULL0 + b), (uint32_t)(nfill[b] - 1) & 1u, kDrainNs);
+            if (ny) mbar_wait(bar(B_FULLY), (uint32_t)(ny - 1) & 1u, kDrainNs);
+            if (nb) mbar_wait(bar(B_FULLB), (uint32_t)(nb - 1) & 1u, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            auto issue_g = [&](int cc) -> bool {   // G = [X; Q] X^T of chunk cc
+                if (!cwait(bar(B_FULL0 + cc % NST), (uint32_t)(cc / NST) & 1u, limit, s_abort) ||
+                    (cc >= 1 && !cwait(bar(B_GFREE), (uint32_t)(cc - 1) & 1u, limit, s_abort)) ||
+                    (cc == 0 && a.k_init && !cwait(bar(B_PATCH), 0u, limit, s_abort)))
+                    return false;
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+                const uint64_t dx = sdesc_sw128(xq(cc % NST) + XQ_X0, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                    mma_bf16(tmem + COL_G, dx + off, dx + off, id, kk > 0);
+                }
+                mma_commit(bar(B_GDONE));
+                return true;
+            };
+            if (nch > 0) ok = issue_g(0);
+            for (int c = 0; c < nch && ok; ++c) {
+                const uint32_t st = xq(c % NST);
+                // U^T = S^T X^T (not for the additive write), V^T = S^T Q^T from the
+                // bf16 state copy of chunk c's start
+                if (!cwait(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    const uint32_t id = idesc_bf16(128, 64, false, false);
+                    const uint32_t sa = tmem + COL_SB;
+                    const uint64_t dxk = sdesc_sw128(st + XQ_X0, 16, 1024);
+                    const uint64_t dqk = sdesc_sw128(st + XQ_Q0, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                        if (!INNER) mma_bf16_ta(tmem + COL_U, sa + 8 * kk, dxk + off, id, kk > 0);
+                        mma_bf16_ta(tmem + COL_V, sa + 8 * kk, dqk + off, id, kk > 0);
+                    }
+                    mma_commit(bar(B_UVDONE));
+                }
+                // the next chunk's Gram while this chunk's channels run
+                if (c + 1 < nch && !issue_g(c + 1)) { ok = false; break; }
+                // S^T += Rw^T X
+                if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                tc_fence_after();
+                {
+                    const uint32_t id_s = idesc_bf16(128, 128, false, true);
+                    const uint64_t dr = sdesc_sw128(sb + OFF_RT, 16, 1024);
+                    const uint64_t dx = sdesc_sw128(st + XQ_X0, 16384, 1024);   // X as MN-major B (N = i)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + COL_S, dr + kk * 2, dx + kk * 128, id_s, 1);
+                    mma_commit(bar(B_SDONE));
+                    mma_commit(bar(B_EMPTY0 + c % NST));
+                }
+            }
+            if (!ok) fail_now();
+            mma_commit(bar(B_MDRAIN));
+            mbar_wait(bar(B_MDRAIN), 0, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp >= SG_W0 && warp < CG_W0) {
+        // ================================================================ staging group
+        const int r = tid - SG_W0 * 32;   // == TMEM lane: row r of [X; Q] X^T
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        bool ok = true;
+        if (a.force_timeout) {   // testing hook: a wait on a barrier nothing arrives on
+            const bool w = cwait(bar(B_NEVER), 0, limit, s_abort);
+            if (bar_or(BAR_SGRP, GROUP, !w)) ok = false;
+        }
+        // chunk 0's first key row is phi(k_init) when one is given (the row before
+        // the sequence reads as zero otherwise)
+        if (ok && a.k_init && nch > 0) {
+            const bool w = cwait(bar(B_FULL0), 0u, limit, s_abort);
+            if (bar_or(BAR_SGRP, GROUP, !w)) {
+                ok = false;
+            } else {
+                if (r < 16) {
+                    const int hb = r >> 3, c16 = r & 7;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(
+                        static_cast<const __nv_bfloat16 *>(a.k_init) + chain * D + hb * 64 + c16 * 8);
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 p2 = unpack_bf16(w4[e]);
+                        f[2 * e] = apply_phi(a.phi, p2.x);
+                        f[2 * e + 1] = apply_phi(a.phi, p2.y);
+                    }
+                    st_row8(xq(0) + (hb ? XQ_X1 : XQ_X0) + (uint32_t)c16 * 16u, f);
+                    fence_proxy_async();
+                }
+                bar_sync(BAR_SGRP, GROUP);
+                if (r == 0) mbar_arrive(bar(B_PATCH));
+            }
+        }
+        float *Am = reinterpret_cast<float *>(sm + (r < C ? OFF_A : OFF_B));
+        const int t = r & (C - 1);
+#pragma unroll 1
+        for (int c = 0; c < nch && ok; ++c) {
+            {
+                bool w = cwait(bar(B_GDONE), (uint32_t)c & 1u, limit, s_abort);
+                w = w && (c < 1 || cwait(bar(B_ABFREE), (uint32_t)(c - 1) & 1u, limit, s_abort));
+                if (bar_or(BAR_SGRP, GROUP, !w)) { ok = false; break; }
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {   // 16 columns s at a time
+                float g[16];
+                tmem_ld16(tmem + lane_base + COL_G + 16 * q, g);
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4)
+                    *reinterpret_cast<float4 *>(Am + t * C + 16 * q + 4 * e4) =
+                        make_float4(g[4 * e4], g[4 * e4 + 1], g[4 * e4 + 2], g[4 * e4 + 3]);
+                if (r < C && (t >> 4) == q) {   // the diagonal: |x_t|^2
+                    const int64_t tok = (int64_t)c * C + t;
+                    const float lt = tok < T ? a.lam[chain * T + tok] : 0.f;
+                    float n = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) n = (e == (t & 15)) ? g[e] : n;
+                    inv[t] = 1.f / (n + lt + a.eps);
+                    lamv[t] = lt;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_GFREE));   // this warp's rows of the Gram region are read
+                mbar_arrive(bar(B_ABRDY));   // and its rows of A or B are staged
+            }
+        }
+        if (!ok && r == 0) fail_now();
+    } else if (warp >= CG_W0) {
+        // ================================================================ channel group
+        const int j = tid - CG_W0 * 32;   // value channel == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        auto gsync = [&]() { bar_sync(BAR_CGRP, GROUP); };
+        auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
+            const bool w = cwait(bb, parity, limit, s_abort);
+            return !bar_or(BAR_CGRP, GROUP, !w);
+        };
+        const float *Am = reinterpret_cast<const float *>(sm + OFF_A);
+        const float *Bm = reinterpret_cast<const float *>(sm + OFF_B);
+        const float *betam = reinterpret_cast<const float *>(sm + OFF_BETA);
+        float *zrow = reinterpret_cast<float *>(sm + OFF_Z) + j * ZROW;
+        __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OUT) + j;
+        // V tile element (t, j): 128-byte swizzled rows, two 64-column halves
+        const uint32_t yhalf = sb + OFF_Y + (j >= 64 ? 8 * KB : 0);
+        const uint32_t ych = (uint32_t)((j & 63) >> 3), yin = (uint32_t)(j & 7) * 2u;
+        bool ok = true;
+
+        // initial state, transposed (thread j holds column j of S): fp32 and bf16
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {   // i = 32q .. 32q+31
+            float v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = a.S0 ? a.S0[(chain * D + 32 * q + e) * D + j] : 0.f;
+            tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+            tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
+            float pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(v[2 * e], v[2 * e + 1]));
+            tmem_st16(tmem + lane_base + COL_SB + 16 * q, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SRDY));
+
+#pragma unroll 1
+        for (int c = 0; c < nch && ok; ++c) {
+            const int64_t tok0 = (int64_t)c * C;
+            // the previous output store has read the output tile
+            if (j == 0) bulk_wait_read0();
+            {
+                bool w = cwait(bar(B_ABRDY), (uint32_t)c & 1u, limit, s_abort);
+                w = w && cwait(bar(B_UVDONE), (uint32_t)c & 1u, limit, s_abort);
+                w = w && cwait(bar(B_FULLY), (uint32_t)c & 1u, limit, s_abort);
+                w = w && cwait(bar(B_FULLB), (uint32_t)c & 1u, limit, s_abort);
+                if (bar_or(BAR_CGRP, GROUP, !w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            float gacc = 1.f;   // G of the last token done (running chunk prefix)
+#pragma unroll 1
+            for (int tb = 0; tb < C / NB; ++tb) {
+                const int b0 = NB * tb;
+                // gates of the block's tokens: eta = beta inv (0 where no pair exists or
+                // past the chain's end), gamma = 1 - eta lambda
+                float eta[NB], gam[NB], yv[NB], uv[NB], vv[NB], pre[NB];
+#pragma unroll
+                for (int e = 0; e < NB; ++e) {
+                    const int64_t tok = tok0 + b0 + e;
+                    const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
+                    eta[e] = pair ? betam[(b0 + e) * D + j] * inv[b0 + e] : 0.f;
+                    gam[e] = 1.f - eta[e] * lamv[b0 + e];
+                    const uint32_t t = (uint32_t)(b0 + e);
+                    const uint32_t ya = yhalf + sw128(t, ych) + yin;
+                    uint16_t yb;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(yb) : "r"(ya));
+                    yv[e] = __uint_as_float((uint32_t)yb << 16);
+                    pre[e] = (e == 0 ? 1.f : pre[e - 1]) * gam[e];
+                }
+                if (!INNER) tmem_ld8(tmem + lane_base + COL_U + b0, uv);
+                tmem_ld8(tmem + lane_base + COL_V + b0, vv);
+                // cross-block sums: H_A(t) = sum_{s < b0} A[t,s] zhat_s, H_B likewise
+                float ha[NB], hb[NB];
+#pragma unroll
+                for (int e = 0; e < NB; ++e) { ha[e] = 0.f; hb[e] = 0.f; }
+#pragma unroll 1
+                for (int s4 = 0; s4 < b0; s4 += 4) {
+                    const float4 z4 = *reinterpret_cast<const float4 *>(zrow + s4);
+#pragma unroll
+                    for (int e = 0; e < NB; ++e) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + (b0 + e) * C + s4);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + (b0 + e) * C + s4);
+                        if (!INNER) {
+                            ha[e] = fmaf(a4.x, z4.x, ha[e]); ha[e] = fmaf(a4.y, z4.y, ha[e]);
+                            ha[e] = fmaf(a4.z, z4.z, ha[e]); ha[e] = fmaf(a4.w, z4.w, ha[e]);
+                        }
+                        hb[e] = fmaf(b4.x, z4.x, hb[e]); hb[e] = fmaf(b4.y, z4.y, hb[e]);
+                        hb[e] = fmaf(b4.z, z4.z, hb[e]); hb[e] = fmaf(b4.w, z4.w, hb[e]);
+                    }
+                }
+                // the block's tokens in order
+                float rr[NB];
+#pragma unroll
+                for (int tl = 0; tl < NB; ++tl) {
+                    const int t = b0 + tl;
+                    const float gm = gacc;          // G_{t-1}
+                    gacc *= gam[tl];                // G_t
+                    const float ct = tl >= 1 ? pre[tl - 1] : 1.f;
+                    float ina = 0.f, inb = 0.f, dd = 1.f;
+                    float arow[NB], brow[NB];
+#pragma unroll
+                    for (int e4 = 0; e4 < NB; e4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * C + b0 + e4);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + t * C + b0 + e4);
+                        arow[e4] = a4.x; arow[e4 + 1] = a4.y; arow[e4 + 2] = a4.z; arow[e4 + 3] = a4.w;
+                        brow[e4] = b4.x; brow[e4 + 1] = b4.y; brow[e4 + 2] = b4.z; brow[e4 + 3] = b4.w;
+                    }
+#pragma unroll
+                    for (int sl = tl - 1; sl >= 0; --sl) {   // D[t-1, s] directly
+                        const float zs = dd * eta[sl] * rr[sl];
+                        if (!INNER) ina = fmaf(arow[sl], zs, ina);
+                        inb = fmaf(brow[sl], zs, inb);
+                        dd *= gam[sl];
+                    }
+                    if (INNER) rr[tl] = yv[tl];
+                    else rr[tl] = yv[tl] - gm * uv[tl] - ct * ha[tl] - ina;
+                    float o;
+                    if (rbw) o = gm * vv[tl] + ct * hb[tl] + inb;
+                    else o = gacc * vv[tl] + gam[tl] * (ct * hb[tl] + inb) + eta[tl] * brow[tl] * rr[tl];
+                    ot[t * D] = __float2bfloat16_rn(o);
+                }
+                // the block is done: earlier weights take its total decay, its own
+                // tokens the suffix products to its end
+                const float tot = pre[NB - 1];
+#pragma unroll 1
+                for (int s4 = 0; s4 < b0; s4 += 4) {
+                    float4 z4 = *reinterpret_cast<const float4 *>(zrow + s4);
+                    z4.x *= tot; z4.y *= tot; z4.z *= tot; z4.w *= tot;
+                    *reinterpret_cast<float4 *>(zrow + s4) = z4;
+                }
+                float zb[NB], suf = 1.f;
+#pragma unroll
+                for (int e = NB - 1; e >= 0; --e) {
+                    zb[e] = suf * eta[e] * rr[e];
+                    suf *= gam[e];
+                }
+#pragma unroll
+                for (int e4 = 0; e4 < NB; e4 += 4)
+                    *reinterpret_cast<float4 *>(zrow + b0 + e4) = make_float4(zb[e4], zb[e4 + 1], zb[e4 + 2], zb[e4 + 3]);
+            }
+            // A, B, inv, V and beta of this chunk are read
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(B_ABFREE));
+                mbar_arrive(bar(B_YFREE));
+                mbar_arrive(bar(B_BFREE));
+            }
+            // fp32 state pre-scaled by this chunk's total decay (per channel), and the
+            // weights-times-residuals row as the state update's bf16 A operand
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float v[32];
+                tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= gacc;
+                tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+                tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const float4 z0 = *reinterpret_cast<const float4 *>(zrow + 8 * c8);
+                const float4 z1 = *reinterpret_cast<const float4 *>(zrow + 8 * c8 + 4);
+                const float z8[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+                st_row8(sb + OFF_RT + sw128((uint32_t)j, (uint32_t)c8), z8);
+            }
+            tmem_st_wait();
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_RRDY));
+            // the chunk's outputs: one tensor store (rows past T are not written)
+            fence_proxy_async();
+            gsync();
+            if (j == 0) {
+                tma_store_3d(&tmo, sb + OFF_OUT, 0, (int)tok0, (int)chain);
+                bulk_commit();
+            }
+            // state carry: once the update is done, the bf16 copy for the next chunk
+            // (the last chunk writes S_T)
+            if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
+            tc_fence_after();
+            const bool last = (c + 1 == nch);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float v[32];
+                tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
+                if (last) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a.S_T[(chain * D + 32 * q + e) * D + j] = v[e];
+                } else {
+                    float pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(v[2 * e], v[2 * e + 1]));
+                    tmem_st16(tmem + lane_base + COL_SB + 16 * q, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && !last) mbar_arrive(bar(B_SRDY));
+        }
+        if (!ok && j == 0) fail_now();
+        if (j == 0) bulk_wait0();   // no output store in flight at exit
+    }
+
+    // every role meets here; tensor memory is released last
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [n_chains][T][128] bf16 viewed as (d, T, chain): 64 x 64 boxes with the 128-byte
+// swizzle for the tile loads, 128 x 64 plain for the output store.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t box_d = 64,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)nc};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+    cuuint32_t box[3] = {box_d, (cuuint32_t)C, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Falcon-2 / 2A with bf16 inputs, d = 128, phi = identity (phi = elu+1 would round
+// phi(k) ~ 1 + k to a bf16 operand and lose the key's varying part).
+bool chunked_chan_supported(const PrefillArgs &a) {
+    return (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A) && a.phi == FW_PHI_IDENTITY &&
+           a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
+           a.n_chains <= (int64_t)INT32_MAX;
+}
+
+cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s) {
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
+        !make_map(&tv, a.v, a.T, a.n_chains) ||
+        !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = a.mode == FW_FALCON2A ? chan_kernel<true> : chan_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
+    return cudaGetLastError();
+}
+
+}  // namespace fw

@@ -80,6 +80,9 @@ cudaError_t launch_decode(const StepArgs &a, cudaStream_t s);
 // Chunked tensor-core prefill.  supported() tells whether it takes the call.
 bool chunked_supported(const PrefillArgs &a);
 cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s);
+// Chunked tensor-core prefill of the per-channel step (Falcon-2 / 2A).
+bool chunked_chan_supported(const PrefillArgs &a);
+cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s);
 
 // ---- small device helpers ------------------------------------------------
 

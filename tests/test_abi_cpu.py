@@ -106,9 +106,13 @@ def test_chunked_unsupported_shapes(L):
         assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), flags=flags,
                             algo=2) in (-6, -10)
     assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=2, algo=2) in (-6, -10)
-    # a step per value channel stays on the per-token kernel
+    # a step per value channel is taken for bf16, d = 128, phi = identity (the
+    # call then fails only at the device query); fp32, d = 64 and elu+1 are not
     for mode in (3, 4):
-        assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=mode, algo=2) == -8
+        assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=mode, algo=2) in (-6, -10)
+        assert call_prefill(L, dtype=0, shape=(1, 1, 8, 128, 128), mode=mode, algo=2) == -8
+        assert call_prefill(L, dtype=1, shape=(1, 1, 8, 64, 64), mode=mode, algo=2) == -8
+        assert call_prefill(L, dtype=1, shape=(1, 1, 8, 128, 128), mode=mode, phi=1, algo=2) == -8
 
 
 @no_gpu
