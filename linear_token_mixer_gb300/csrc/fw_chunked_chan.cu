@@ -65,24 +65,27 @@ constexpr uint32_t OFF_XQ = 0;             // NST stages of X0 Q0 X1 Q1 (8 KB ea
 constexpr uint32_t XQ_X0 = 0, XQ_Q0 = 8 * KB, XQ_X1 = 16 * KB, XQ_Q1 = 24 * KB;
 constexpr uint32_t OFF_Y = 64 * KB;        // V tile, two 64-column halves (128-byte swizzle)
 constexpr uint32_t OFF_BETA = 80 * KB;     // beta rows of the chunk, fp32 [t][j]
+constexpr int ABROW = 68;                  // row stride of A and B (64 + 4: conflict-free columns)
 constexpr uint32_t OFF_A = 112 * KB;       // X X^T, fp32 [t][s]
-constexpr uint32_t OFF_B = 128 * KB;       // Q X^T, fp32 [t][s]
-constexpr uint32_t OFF_RT = 144 * KB;      // (weights * r)^T, bf16 rows j (K-major A operand)
-constexpr uint32_t OFF_OUT = 160 * KB;     // output tile, bf16 [t][j]
-constexpr uint32_t OFF_Z = 176 * KB;       // zhat per channel, fp32 rows j of ZROW floats
+constexpr uint32_t OFF_B = OFF_A + (uint32_t)C * ABROW * 4;   // Q X^T, fp32 [t][s]
+constexpr uint32_t OFF_RT = 147 * KB;      // (weights * r)^T, bf16 rows j (K-major A operand)
+constexpr uint32_t OFF_OUT = OFF_RT + 16 * KB;   // output tile, bf16 [t][j]
+constexpr uint32_t OFF_Z = OFF_OUT + 16 * KB;    // zhat per channel, fp32 rows j of ZROW floats
 constexpr int ZROW = 68;                   // 64 + 4 (16-byte groups spread over the banks)
-constexpr uint32_t OFF_VEC = OFF_Z + (uint32_t)D * ZROW * 4;   // inv[64], lambda[64]
+constexpr uint32_t OFF_HT = OFF_Z + (uint32_t)D * ZROW * 4;    // per channel warp: H_A, H_B [8][32]
+constexpr uint32_t OFF_VEC = OFF_HT + 4 * 2 * NB * 32 * 4;       // inv[64], lambda[64]
 constexpr uint32_t OFF_BAR = OFF_VEC + 512;
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
 static_assert(SMEM_ALLOC <= 227 * KB, "shared memory budget");
-static_assert(OFF_VEC % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+static_assert(OFF_VEC % 16 == 0 && OFF_BAR % 8 == 0 && OFF_B + (uint32_t)C * ABROW * 4 <= OFF_RT,
+              "alignment and layout");
 
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + NST, B_FULLY = B_EMPTY0 + NST, B_YFREE, B_FULLB, B_BFREE,
     B_GDONE, B_GFREE, B_ABRDY, B_ABFREE, B_SRDY, B_UVDONE, B_RRDY, B_SDONE, B_MDRAIN, B_NEVER,
-    B_PATCH, B_COUNT
+    B_PATCH, B_SSCL, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
@@ -92,6 +95,16 @@ constexpr uint32_t COL_G = 0, COL_U = 64, COL_V = 128, COL_SB = 192, COL_S = 256
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint64_t kDrainNs = 2000000000ull;
+
+// Optional phase timestamps of CTA 0 (instrumented builds only).
+#ifdef FW_TRACE
+constexpr int kCTraceEv = 32, kCTraceChunks = 64;
+__device__ unsigned long long g_ctrace[kCTraceChunks * kCTraceEv];
+#define CTRACE(c, ev) \
+    do { if (blockIdx.x == 0 && (c) < kCTraceChunks) g_ctrace[(c) * kCTraceEv + (ev)] = globaltimer(); } while (0)
+#else
+#define CTRACE(c, ev) do { } while (0)
+#endif
 
 __device__ __noinline__ bool cwait_slow(uint32_t bar, uint32_t parity, uint64_t limit,
                                         volatile int *abort_flag) {
@@ -161,9 +174,10 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t n = 1;
-            if (i == B_YFREE || i == B_BFREE || i == B_GFREE || i == B_ABRDY || i == B_ABFREE ||
-                i == B_SRDY || i == B_RRDY)
+            if (i == B_YFREE || i == B_GFREE || i == B_ABRDY || i == B_ABFREE || i == B_SRDY ||
+                i == B_RRDY || i == B_SSCL)
                 n = 4;   // one arrival per warp of the publishing group
+            if (i == B_BFREE) n = 8;   // the beta rows are read by both groups
             mbar_init(bar(i), n);
         }
         fence_mbar_init();
@@ -283,11 +297,13 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                         mma_bf16_ta(tmem + COL_V, sa + 8 * kk, dqk + off, id, kk > 0);
                     }
                     mma_commit(bar(B_UVDONE));
+                    CTRACE(c, 6);
                 }
                 // the next chunk's Gram while this chunk's channels run
                 if (c + 1 < nch && !issue_g(c + 1)) { ok = false; break; }
-                // S^T += Rw^T X
-                if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                // S^T += Rw^T X, onto the state pre-scaled by the chunk's decay
+                if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort) ||
+                    !cwait(bar(B_SSCL), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
                 tc_fence_after();
                 {
                     const uint32_t id_s = idesc_bf16(128, 128, false, true);
@@ -297,6 +313,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     for (int kk = 0; kk < 4; ++kk) mma_bf16(tmem + COL_S, dr + kk * 2, dx + kk * 128, id_s, 1);
                     mma_commit(bar(B_SDONE));
                     mma_commit(bar(B_EMPTY0 + c % NST));
+                    CTRACE(c, 7);
                 }
             }
             if (!ok) fail_now();
@@ -355,7 +372,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 tmem_ld16(tmem + lane_base + COL_G + 16 * q, g);
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4)
-                    *reinterpret_cast<float4 *>(Am + t * C + 16 * q + 4 * e4) =
+                    *reinterpret_cast<float4 *>(Am + t * ABROW + 16 * q + 4 * e4) =
                         make_float4(g[4 * e4], g[4 * e4 + 1], g[4 * e4 + 2], g[4 * e4 + 3]);
                 if (r < C && (t >> 4) == q) {   // the diagonal: |x_t|^2
                     const int64_t tok = (int64_t)c * C + t;
@@ -373,6 +390,42 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 mbar_arrive(bar(B_GFREE));   // this warp's rows of the Gram region are read
                 mbar_arrive(bar(B_ABRDY));   // and its rows of A or B are staged
             }
+            if (r == 0) CTRACE(c, 8);
+            // this chunk's total decay of channel r, and the fp32 state (lane r) pre-scaled
+            // by it, once the state carry of the previous chunk has read the state
+            {
+                bool w = cwait(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort);
+                w = w && cwait(bar(B_FULLB), (uint32_t)c & 1u, limit, s_abort);
+                if (bar_or(BAR_SGRP, GROUP, !w)) { ok = false; break; }
+            }
+            {
+                const float *betam = reinterpret_cast<const float *>(sm + OFF_BETA);
+                float gtot = 1.f;
+#pragma unroll 4
+                for (int tt = 0; tt < C; ++tt) {
+                    const int64_t tok = (int64_t)c * C + tt;
+                    const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
+                    const float eta = pair ? betam[tt * D + r] * inv[tt] : 0.f;
+                    gtot *= 1.f - eta * lamv[tt];
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= gtot;
+                    tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
+                    tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(B_SSCL));
+                    mbar_arrive(bar(B_BFREE));
+                }
+            }
         }
         if (!ok && r == 0) fail_now();
     } else if (warp >= CG_W0) {
@@ -388,6 +441,8 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         const float *Bm = reinterpret_cast<const float *>(sm + OFF_B);
         const float *betam = reinterpret_cast<const float *>(sm + OFF_BETA);
         float *zrow = reinterpret_cast<float *>(sm + OFF_Z) + j * ZROW;
+        const int jw0 = j & ~31;   // first channel of this warp
+        float *hts = reinterpret_cast<float *>(sm + OFF_HT) + (j >> 5) * (2 * NB * 32);
         __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OUT) + j;
         // V tile element (t, j): 128-byte swizzled rows, two 64-column halves
         const uint32_t yhalf = sb + OFF_Y + (j >= 64 ? 8 * KB : 0);
@@ -424,6 +479,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 w = w && cwait(bar(B_FULLB), (uint32_t)c & 1u, limit, s_abort);
                 if (bar_or(BAR_CGRP, GROUP, !w)) { ok = false; break; }
             }
+            if (j == 0) CTRACE(c, 0);
             tc_fence_after();
             float gacc = 1.f;   // G of the last token done (running chunk prefix)
 #pragma unroll 1
@@ -447,25 +503,62 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 }
                 if (!INNER) tmem_ld8(tmem + lane_base + COL_U + b0, uv);
                 tmem_ld8(tmem + lane_base + COL_V + b0, vv);
-                // cross-block sums: H_A(t) = sum_{s < b0} A[t,s] zhat_s, H_B likewise
+                if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 10 : 13);
+                // cross-block sums H_A(t) = sum_{s < b0} A[t,s] zhat_s (and H_B with B) for
+                // the block's eight rows and this warp's 32 channels: a small product
+                // (t x s) (s x j) on the warp's tf32 MMAs (rows 8..15 of the 16-row
+                // tile are zero), then through shared memory to one thread per channel
                 float ha[NB], hb[NB];
+                {
+                    const int g = lane >> 2, t4 = lane & 3;
+                    float ca[4][4], cb[4][4];
 #pragma unroll
-                for (int e = 0; e < NB; ++e) { ha[e] = 0.f; hb[e] = 0.f; }
+                    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) { ca[nt][e] = 0.f; cb[nt][e] = 0.f; }
+                    const float *arow = Am + (b0 + g) * ABROW + t4;
+                    const float *brow = Bm + (b0 + g) * ABROW + t4;
+                    const float *zcol = reinterpret_cast<const float *>(sm + OFF_Z) + (jw0 + g) * ZROW + t4;
 #pragma unroll 1
-                for (int s4 = 0; s4 < b0; s4 += 4) {
-                    const float4 z4 = *reinterpret_cast<const float4 *>(zrow + s4);
+                    for (int k0 = 0; k0 < b0; k0 += 8) {
+                        uint32_t fa[4], fb[4];
+                        fa[0] = __float_as_uint(arow[k0]);
+                        fa[1] = 0u;
+                        fa[2] = __float_as_uint(arow[k0 + 4]);
+                        fa[3] = 0u;
+                        fb[0] = __float_as_uint(brow[k0]);
+                        fb[1] = 0u;
+                        fb[2] = __float_as_uint(brow[k0 + 4]);
+                        fb[3] = 0u;
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+                            uint32_t fz[2];
+                            fz[0] = __float_as_uint(zcol[nt * 8 * ZROW + k0]);
+                            fz[1] = __float_as_uint(zcol[nt * 8 * ZROW + k0 + 4]);
+                            if (!INNER) mma_tf32_16x8x8(ca[nt], fa, fz);
+                            mma_tf32_16x8x8(cb[nt], fb, fz);
+                        }
+                    }
+                    // rows g (< 8) of the tiles: channel 8 nt + 2 t4 (+1) of this warp
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        const int jl = 8 * nt + 2 * t4;
+                        if (!INNER) {
+                            hts[(0 * NB + g) * 32 + jl] = ca[nt][0];
+                            hts[(0 * NB + g) * 32 + jl + 1] = ca[nt][1];
+                        }
+                        hts[(1 * NB + g) * 32 + jl] = cb[nt][0];
+                        hts[(1 * NB + g) * 32 + jl + 1] = cb[nt][1];
+                    }
+                    __syncwarp();
 #pragma unroll
                     for (int e = 0; e < NB; ++e) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + (b0 + e) * C + s4);
-                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + (b0 + e) * C + s4);
-                        if (!INNER) {
-                            ha[e] = fmaf(a4.x, z4.x, ha[e]); ha[e] = fmaf(a4.y, z4.y, ha[e]);
-                            ha[e] = fmaf(a4.z, z4.z, ha[e]); ha[e] = fmaf(a4.w, z4.w, ha[e]);
-                        }
-                        hb[e] = fmaf(b4.x, z4.x, hb[e]); hb[e] = fmaf(b4.y, z4.y, hb[e]);
-                        hb[e] = fmaf(b4.z, z4.z, hb[e]); hb[e] = fmaf(b4.w, z4.w, hb[e]);
+                        ha[e] = INNER ? 0.f : hts[(0 * NB + e) * 32 + lane];
+                        hb[e] = hts[(1 * NB + e) * 32 + lane];
                     }
+                    __syncwarp();
                 }
+                if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 11 : 14);
                 // the block's tokens in order
                 float rr[NB];
 #pragma unroll
@@ -478,8 +571,8 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     float arow[NB], brow[NB];
 #pragma unroll
                     for (int e4 = 0; e4 < NB; e4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * C + b0 + e4);
-                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + t * C + b0 + e4);
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * ABROW + b0 + e4);
+                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + t * ABROW + b0 + e4);
                         arow[e4] = a4.x; arow[e4 + 1] = a4.y; arow[e4 + 2] = a4.z; arow[e4 + 3] = a4.w;
                         brow[e4] = b4.x; brow[e4 + 1] = b4.y; brow[e4 + 2] = b4.z; brow[e4 + 3] = b4.w;
                     }
@@ -497,6 +590,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     else o = gacc * vv[tl] + gam[tl] * (ct * hb[tl] + inb) + eta[tl] * brow[tl] * rr[tl];
                     ot[t * D] = __float2bfloat16_rn(o);
                 }
+                if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 12 : 15);
                 // the block is done: earlier weights take its total decay, its own
                 // tokens the suffix products to its end
                 const float tot = pre[NB - 1];
@@ -516,6 +610,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 for (int e4 = 0; e4 < NB; e4 += 4)
                     *reinterpret_cast<float4 *>(zrow + b0 + e4) = make_float4(zb[e4], zb[e4 + 1], zb[e4 + 2], zb[e4 + 3]);
             }
+            if (j == 0) CTRACE(c, 1);
             // A, B, inv, V and beta of this chunk are read
             tc_fence_before();
             __syncwarp();
@@ -524,17 +619,8 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 mbar_arrive(bar(B_YFREE));
                 mbar_arrive(bar(B_BFREE));
             }
-            // fp32 state pre-scaled by this chunk's total decay (per channel), and the
-            // weights-times-residuals row as the state update's bf16 A operand
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] *= gacc;
-                tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
-                tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
-            }
+            // the weights-times-residuals row as the state update's bf16 A operand
+            // (the staging group pre-scales the fp32 state by the chunk's decay)
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
                 const float4 z0 = *reinterpret_cast<const float4 *>(zrow + 8 * c8);
@@ -542,11 +628,10 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 const float z8[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
                 st_row8(sb + OFF_RT + sw128((uint32_t)j, (uint32_t)c8), z8);
             }
-            tmem_st_wait();
             fence_proxy_async();
-            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_RRDY));
+            if (j == 0) CTRACE(c, 2);
             // the chunk's outputs: one tensor store (rows past T are not written)
             fence_proxy_async();
             gsync();
@@ -557,6 +642,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             // state carry: once the update is done, the bf16 copy for the next chunk
             // (the last chunk writes S_T)
             if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
+            if (j == 0) CTRACE(c, 3);
             tc_fence_after();
             const bool last = (c + 1 == nch);
 #pragma unroll 1
@@ -577,6 +663,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && !last) mbar_arrive(bar(B_SRDY));
+            if (j == 0) CTRACE(c, 4);
         }
         if (!ok && j == 0) fail_now();
         if (j == 0) bulk_wait0();   // no output store in flight at exit
@@ -629,6 +716,13 @@ bool chunked_chan_supported(const PrefillArgs &a) {
            a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
            a.n_chains <= (int64_t)INT32_MAX;
 }
+
+#ifdef FW_TRACE
+extern "C" int fw_debug_read_chan_trace(unsigned long long *dst, int n) {
+    if (n > kCTraceChunks * kCTraceEv) n = kCTraceChunks * kCTraceEv;
+    return (int)cudaMemcpyFromSymbol(dst, g_ctrace, sizeof(unsigned long long) * n);
+}
+#endif
 
 cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tv, to;
