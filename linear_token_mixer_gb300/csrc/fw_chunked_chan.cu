@@ -72,8 +72,9 @@ constexpr uint32_t OFF_RT = 147 * KB;      // (weights * r)^T, bf16 rows j (K-ma
 constexpr uint32_t OFF_OUT = OFF_RT + 16 * KB;   // output tile, bf16 [t][j]
 constexpr uint32_t OFF_Z = OFF_OUT + 16 * KB;    // zhat per channel, fp32 rows j of ZROW floats
 constexpr int ZROW = 68;                   // 64 + 4 (16-byte groups spread over the banks)
-constexpr uint32_t OFF_HT = OFF_Z + (uint32_t)D * ZROW * 4;    // per channel warp: H_A, H_B [8][32]
-constexpr uint32_t OFF_VEC = OFF_HT + 4 * 2 * NB * 32 * 4;       // inv[64], lambda[64]
+constexpr int HTP = 36;                    // row stride of the H transposes (8 HTP = 8 mod 32: no conflicts)
+constexpr uint32_t OFF_HT = OFF_Z + (uint32_t)D * ZROW * 4;    // per channel warp: H_A, H_B [8][HTP]
+constexpr uint32_t OFF_VEC = OFF_HT + 4 * 2 * NB * HTP * 4;      // inv[64], lambda[64]
 constexpr uint32_t OFF_BAR = OFF_VEC + 512;
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64;
@@ -129,6 +130,24 @@ __device__ __forceinline__ void st_row8(uint32_t addr, const float *v) {
 }
 
 // Eight consecutive columns of one lane, loaded and waited for.
+// two 8-column loads, one wait (no memory clobber: tensor memory only)
+__device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float *va, float *vb) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(ta), "r"(tb));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[8 + i]);
+    }
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
     uint32_t r[8];
     asm volatile(
@@ -442,7 +461,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         const float *betam = reinterpret_cast<const float *>(sm + OFF_BETA);
         float *zrow = reinterpret_cast<float *>(sm + OFF_Z) + j * ZROW;
         const int jw0 = j & ~31;   // first channel of this warp
-        float *hts = reinterpret_cast<float *>(sm + OFF_HT) + (j >> 5) * (2 * NB * 32);
+        float *hts = reinterpret_cast<float *>(sm + OFF_HT) + (j >> 5) * (2 * NB * HTP);
         __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OUT) + j;
         // V tile element (t, j): 128-byte swizzled rows, two 64-column halves
         const uint32_t yhalf = sb + OFF_Y + (j >= 64 ? 8 * KB : 0);
@@ -482,6 +501,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             if (j == 0) CTRACE(c, 0);
             tc_fence_after();
             float gacc = 1.f;   // G of the last token done (running chunk prefix)
+            float totp = 1.f;   // total decay of the previous block (this channel)
 #pragma unroll 1
             for (int tb = 0; tb < C / NB; ++tb) {
                 const int b0 = NB * tb;
@@ -501,73 +521,91 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     yv[e] = __uint_as_float((uint32_t)yb << 16);
                     pre[e] = (e == 0 ? 1.f : pre[e - 1]) * gam[e];
                 }
-                if (!INNER) tmem_ld8(tmem + lane_base + COL_U + b0, uv);
-                tmem_ld8(tmem + lane_base + COL_V + b0, vv);
+                if (INNER) tmem_ld8(tmem + lane_base + COL_V + b0, vv);
+                else tmem_ld8x2(tmem + lane_base + COL_U + b0, tmem + lane_base + COL_V + b0, uv, vv);
                 if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 10 : 13);
                 // cross-block sums H_A(t) = sum_{s < b0} A[t,s] zhat_s (and H_B with B) for
-                // the block's eight rows and this warp's 32 channels: a small product
-                // (t x s) (s x j) on the warp's tf32 MMAs (rows 8..15 of the 16-row
-                // tile are zero), then through shared memory to one thread per channel
+                // the block's eight rows and this warp's 32 channels, as the transposed
+                // product (j x s) (s x t) on the warp's tf32 MMAs: two 16-channel tiles,
+                // n = the block's eight tokens, the k steps alternating between two
+                // accumulator sets; then through shared memory to one thread per channel.
+                // Weights of blocks before the previous one still lack the previous
+                // block's decay: they take it on the way in and are stored back.
                 float ha[NB], hb[NB];
                 {
                     const int g = lane >> 2, t4 = lane & 3;
-                    float ca[4][4], cb[4][4];
+                    float sc[4];   // decay of channels g + 8 q of this warp
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
+                    for (int q = 0; q < 4; ++q) sc[q] = __shfl_sync(0xffffffffu, totp, g + 8 * q);
+                    __syncwarp();   // the previous block's weights are in shared memory
+                    float xa[2][2][4], xb[2][2][4];   // [k-step parity][channel tile][fragment]
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) { ca[nt][e] = 0.f; cb[nt][e] = 0.f; }
+                    for (int p = 0; p < 2; ++p)
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) { xa[p][mt][e] = 0.f; xb[p][mt][e] = 0.f; }
                     const float *arow = Am + (b0 + g) * ABROW + t4;
                     const float *brow = Bm + (b0 + g) * ABROW + t4;
-                    const float *zcol = reinterpret_cast<const float *>(sm + OFF_Z) + (jw0 + g) * ZROW + t4;
+                    float *zr = reinterpret_cast<float *>(sm + OFF_Z) + (jw0 + g) * ZROW + t4;
+                    auto kstep = [&](float (&ya)[2][4], float (&yb)[2][4], int k0, bool stale) {
+                        const uint32_t fa[2] = {__float_as_uint(arow[k0]), __float_as_uint(arow[k0 + 4])};
+                        const uint32_t fb[2] = {__float_as_uint(brow[k0]), __float_as_uint(brow[k0 + 4])};
+#pragma unroll
+                        for (int mt = 0; mt < 2; ++mt) {
+                            float *zp = zr + 16 * mt * ZROW + k0;
+                            // fragment rows g and g + 8 (channels), columns t4 and t4 + 4 (s)
+                            float z00 = zp[0], z10 = zp[8 * ZROW], z01 = zp[4], z11 = zp[8 * ZROW + 4];
+                            if (stale) {
+                                z00 *= sc[2 * mt];
+                                z01 *= sc[2 * mt];
+                                z10 *= sc[2 * mt + 1];
+                                z11 *= sc[2 * mt + 1];
+                                zp[0] = z00;
+                                zp[4] = z01;
+                                zp[8 * ZROW] = z10;
+                                zp[8 * ZROW + 4] = z11;
+                            }
+                            const uint32_t fz[4] = {__float_as_uint(z00), __float_as_uint(z10),
+                                                    __float_as_uint(z01), __float_as_uint(z11)};
+                            if (!INNER) mma_tf32_16x8x8(ya[mt], fz, fa);
+                            mma_tf32_16x8x8(yb[mt], fz, fb);
+                        }
+                    };
+                    int k0 = 0;
 #pragma unroll 1
-                    for (int k0 = 0; k0 < b0; k0 += 8) {
-                        uint32_t fa[4], fb[4];
-                        fa[0] = __float_as_uint(arow[k0]);
-                        fa[1] = 0u;
-                        fa[2] = __float_as_uint(arow[k0 + 4]);
-                        fa[3] = 0u;
-                        fb[0] = __float_as_uint(brow[k0]);
-                        fb[1] = 0u;
-                        fb[2] = __float_as_uint(brow[k0 + 4]);
-                        fb[3] = 0u;
-#pragma unroll
-                        for (int nt = 0; nt < 4; ++nt) {
-                            uint32_t fz[2];
-                            fz[0] = __float_as_uint(zcol[nt * 8 * ZROW + k0]);
-                            fz[1] = __float_as_uint(zcol[nt * 8 * ZROW + k0 + 4]);
-                            if (!INNER) mma_tf32_16x8x8(ca[nt], fa, fz);
-                            mma_tf32_16x8x8(cb[nt], fb, fz);
-                        }
+                    for (; k0 + 16 <= b0; k0 += 16) {
+                        kstep(xa[0], xb[0], k0, true);
+                        kstep(xa[1], xb[1], k0 + 8, k0 + 16 < b0);
                     }
-                    // rows g (< 8) of the tiles: channel 8 nt + 2 t4 (+1) of this warp
+                    if (k0 < b0) kstep(xa[0], xb[0], k0, false);
+                    // fragment (channel 16 mt + g + 8 h, token 2 t4 + u) to [token][channel]
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        const int jl = 8 * nt + 2 * t4;
-                        if (!INNER) {
-                            hts[(0 * NB + g) * 32 + jl] = ca[nt][0];
-                            hts[(0 * NB + g) * 32 + jl + 1] = ca[nt][1];
+                    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int idx = (2 * t4 + (e & 1)) * HTP + 16 * mt + g + 8 * (e >> 1);
+                            if (!INNER) hts[idx] = xa[0][mt][e] + xa[1][mt][e];
+                            hts[NB * HTP + idx] = xb[0][mt][e] + xb[1][mt][e];
                         }
-                        hts[(1 * NB + g) * 32 + jl] = cb[nt][0];
-                        hts[(1 * NB + g) * 32 + jl + 1] = cb[nt][1];
-                    }
                     __syncwarp();
 #pragma unroll
                     for (int e = 0; e < NB; ++e) {
-                        ha[e] = INNER ? 0.f : hts[(0 * NB + e) * 32 + lane];
-                        hb[e] = hts[(1 * NB + e) * 32 + lane];
+                        ha[e] = INNER ? 0.f : hts[e * HTP + lane];
+                        hb[e] = hts[(NB + e) * HTP + lane];
                     }
                     __syncwarp();
                 }
                 if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 11 : 14);
-                // the block's tokens in order
-                float rr[NB];
+                // the block's tokens in order; w_s = eta_s r_s
+                float rr[NB], wv[NB];
 #pragma unroll
                 for (int tl = 0; tl < NB; ++tl) {
                     const int t = b0 + tl;
                     const float gm = gacc;          // G_{t-1}
                     gacc *= gam[tl];                // G_t
                     const float ct = tl >= 1 ? pre[tl - 1] : 1.f;
-                    float ina = 0.f, inb = 0.f, dd = 1.f;
+                    float ina = 0.f, inb = 0.f;
                     float arow[NB], brow[NB];
 #pragma unroll
                     for (int e4 = 0; e4 < NB; e4 += 4) {
@@ -576,34 +614,38 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                         arow[e4] = a4.x; arow[e4 + 1] = a4.y; arow[e4 + 2] = a4.z; arow[e4 + 3] = a4.w;
                         brow[e4] = b4.x; brow[e4 + 1] = b4.y; brow[e4 + 2] = b4.z; brow[e4 + 3] = b4.w;
                     }
+                    // D[t-1, s] = gam_{s+1} ... gam_{t-1} directly (no residual in it)
+                    float dd[NB];
+                    {
+                        float p = 1.f;
 #pragma unroll
-                    for (int sl = tl - 1; sl >= 0; --sl) {   // D[t-1, s] directly
-                        const float zs = dd * eta[sl] * rr[sl];
+                        for (int sl = tl - 1; sl >= 0; --sl) {
+                            dd[sl] = p;
+                            p *= gam[sl];
+                        }
+                    }
+#pragma unroll
+                    for (int sl = 0; sl < tl; ++sl) {   // oldest first: the newest residual enters last
+                        const float zs = dd[sl] * wv[sl];
                         if (!INNER) ina = fmaf(arow[sl], zs, ina);
                         inb = fmaf(brow[sl], zs, inb);
-                        dd *= gam[sl];
                     }
                     if (INNER) rr[tl] = yv[tl];
                     else rr[tl] = yv[tl] - gm * uv[tl] - ct * ha[tl] - ina;
+                    wv[tl] = eta[tl] * rr[tl];
                     float o;
                     if (rbw) o = gm * vv[tl] + ct * hb[tl] + inb;
-                    else o = gacc * vv[tl] + gam[tl] * (ct * hb[tl] + inb) + eta[tl] * brow[tl] * rr[tl];
+                    else o = gacc * vv[tl] + gam[tl] * (ct * hb[tl] + inb) + brow[tl] * wv[tl];
                     ot[t * D] = __float2bfloat16_rn(o);
                 }
                 if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 12 : 15);
-                // the block is done: earlier weights take its total decay, its own
-                // tokens the suffix products to its end
-                const float tot = pre[NB - 1];
-#pragma unroll 1
-                for (int s4 = 0; s4 < b0; s4 += 4) {
-                    float4 z4 = *reinterpret_cast<const float4 *>(zrow + s4);
-                    z4.x *= tot; z4.y *= tot; z4.z *= tot; z4.w *= tot;
-                    *reinterpret_cast<float4 *>(zrow + s4) = z4;
-                }
+                // the block is done: its own tokens take the suffix products to its
+                // end (earlier weights take its total decay in the next block's sums)
+                totp = pre[NB - 1];
                 float zb[NB], suf = 1.f;
 #pragma unroll
                 for (int e = NB - 1; e >= 0; --e) {
-                    zb[e] = suf * eta[e] * rr[e];
+                    zb[e] = suf * wv[e];
                     suf *= gam[e];
                 }
 #pragma unroll
@@ -619,13 +661,16 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 mbar_arrive(bar(B_YFREE));
                 mbar_arrive(bar(B_BFREE));
             }
-            // the weights-times-residuals row as the state update's bf16 A operand
-            // (the staging group pre-scales the fp32 state by the chunk's decay)
+            // the weights-times-residuals row as the state update's bf16 A operand,
+            // the last block's decay applied to the blocks before it (the staging
+            // group pre-scales the fp32 state by the chunk's decay)
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
+                const float f = 8 * c8 < C - NB ? totp : 1.f;
                 const float4 z0 = *reinterpret_cast<const float4 *>(zrow + 8 * c8);
                 const float4 z1 = *reinterpret_cast<const float4 *>(zrow + 8 * c8 + 4);
-                const float z8[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+                const float z8[8] = {z0.x * f, z0.y * f, z0.z * f, z0.w * f,
+                                     z1.x * f, z1.y * f, z1.z * f, z1.w * f};
                 st_row8(sb + OFF_RT + sw128((uint32_t)j, (uint32_t)c8), z8);
             }
             fence_proxy_async();
