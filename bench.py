@@ -52,6 +52,7 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 KERNEL_SOURCES = {
     "chunked prefill": ("fw_chunked.cu", "fw_sm100.cuh", "fw_internal.cuh"),
+    "chunked prefill (per channel)": ("fw_chunked_chan.cu", "fw_sm100.cuh", "fw_internal.cuh"),
     "recurrent (SIMT)": ("fw_recurrent.cu", "fw_internal.cuh"),
     "window prefill (SIMT)": ("fw_window_prefill.cu", "fw_window.cuh", "fw_sm100.cuh",
                               "fw_internal.cuh"),
@@ -100,29 +101,43 @@ def algorithmic_bytes_prefill(w):
 
 def prefill_kernel(w, algo="auto"):
     """The kernel fw_prefill picks for a workload, as the library dispatches it:
-    a step per value channel (Falcon-2 / 2A) on the staged per-token kernel,
-    then the chunked tensor-core kernel where it takes the call (bf16, d = 128;
-    Falcon-1 / 1A only with phi = identity), else the per-token kernel."""
+    a step per value channel (Falcon-2 / 2A) on the per-channel chunked kernel
+    where it takes the call (bf16, d = 128, phi = identity), else on the staged
+    per-token kernel; the other modes on the chunked tensor-core kernel where it
+    takes the call (bf16, d = 128; Falcon-1 / 1A only with phi = identity), else
+    on the per-token kernel."""
     if algo == "recurrent":
         return "recurrent (SIMT)"
+    tc = w.dtype == torch.bfloat16 and w.d == 128
     if w.mode in ("falcon2", "falcon2a"):
+        if tc and w.phi == "identity":
+            return "chunked prefill (per channel)"
         return "window prefill (SIMT)"
-    chunked = (w.dtype == torch.bfloat16 and w.d == 128 and
-               (w.mode == "linattn" or w.phi == "identity"))
+    chunked = tc and (w.mode == "linattn" or w.phi == "identity")
     return "chunked prefill" if chunked else "recurrent (SIMT)"
 
 
 def matmul_flops_prefill(w, C=64):
-    """Dense matmul FLOPs of the chunked form per launch: Falcon-1
+    """Dense matmul FLOPs of the chunked forms per launch, on tcgen05: Falcon-1
     10 C d + 6 d^2 per head-token; linear attention and Falcon-1A (no
-    residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y).
-    None where the launch runs no tensor-core kernel."""
-    if prefill_kernel(w) != "chunked prefill":
-        return None
+    residual, so no W, U or solve) 4 C d + 4 d^2 (Q X^T, P Y, Q S0, X^T Y);
+    the per-channel kernel (Falcon-2) 4 C d + 6 d^2 (the Gram [X; Q] X^T,
+    X S0, Q S0 and the state update; Falcon-2A 4 C d + 4 d^2, no X S0).  The
+    per-channel kernel's cross-block sums on the warps' tf32 MMAs (112 d per
+    head-token) are not counted.  None where the launch runs no tensor-core
+    kernel."""
+    k = prefill_kernel(w)
     ht = w.B * w.H * w.T
+    if k == "chunked prefill (per channel)":
+        return ht * (4 * C * w.d + (6 if w.mode == "falcon2" else 4) * w.d * w.d)
+    if k != "chunked prefill":
+        return None
     if w.mode == "falcon1":
         return ht * (10 * C * w.d + 6 * w.d * w.d)
     return ht * (4 * C * w.d + 4 * w.d * w.d)
+
+
+MATMUL_NOTE = {"falcon1": "10Cd+6d^2", "falcon2": "4Cd+6d^2", "falcon2a": "4Cd+4d^2"}
 
 
 # workloads the headline (fw_prefill) can run: the window family has its own call
@@ -281,9 +296,13 @@ def bench_prefill(w, K, W, dev, fw, algo="auto", rbw=False, same_pair=False):
     }
     if rbw or same_pair:
         res["flags"] = [f for f, on in (("rbw", rbw), ("same_pair", same_pair)) if on]
-    if w.mode in ("falcon2", "falcon2a") and algo == "auto":
-        # per-channel steps run on the staged per-token kernel (window of one
-        # pair): bound by FP32 ALU work, not by memory
+    elif algo == "auto" and res["kernel"] != "recurrent (SIMT)":
+        # DRAM bytes of one launch from the committed ncu summary (None once the
+        # kernel's sources changed since the capture)
+        res["dram_bytes_per_launch"] = stored_traffic(res["kernel"], w.name)
+    if res["kernel"] == "window prefill (SIMT)":
+        # per-channel steps on the staged per-token kernel (window of one pair):
+        # bound by FP32 ALU work, not by memory
         tf = window_flops(w) / (kern_ms / 1e3) / 1e12
         res["roofline"] = {"bound": "alu", "achieved": tf, "peak": ALU_FP32_TFLOPS,
                            "unit": "TFLOP/s", "frac": tf / ALU_FP32_TFLOPS,
@@ -619,7 +638,7 @@ def main():
     algo_bytes = algorithmic_bytes_prefill(w)
     achieved_gbs = algo_bytes / (kern_ms / 1e3) / 1e9
     kname = prefill_kernel(w)
-    if kname == "chunked prefill":
+    if kname in ("chunked prefill", "chunked prefill (per channel)"):
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm"],
                 "traffic": stored_traffic(kname, w.name),
@@ -645,7 +664,8 @@ def main():
         "roofline": roof,
         "tensor": ({"matmul_tflops": mm_tf, "peak": peaks["bf16"],
                     "frac": mm_tf / peaks["bf16"], "chunk": 64,
-                    "note": "dense matmul FLOPs of the chunked form (10Cd+6d^2 per head-token)"}
+                    "note": "dense matmul FLOPs of the chunked form (%s per head-token)"
+                            % MATMUL_NOTE.get(w.mode, "4Cd+4d^2")}
                    if mm_tf else None),
         "gpu_launches": args.steps,
         "kernel_ms": kern_ms,

@@ -143,9 +143,16 @@ def test_headline_kernel_labels_follow_the_dispatch():
     assert bench.prefill_kernel(W["linattn_bf16"]) == "chunked prefill"
     assert bench.prefill_kernel(W["falcon1_fp32"]) == "recurrent (SIMT)"
     assert bench.prefill_kernel(W["falcon1_bf16"].with_shape(phi="elu1")) == "recurrent (SIMT)"
-    assert bench.prefill_kernel(W["falcon2_bf16"]) == "window prefill (SIMT)"
+    f2 = W["falcon2_bf16"]
+    assert bench.prefill_kernel(f2) == "chunked prefill (per channel)"
+    assert bench.prefill_kernel(f2.with_shape(phi="elu1")) == "window prefill (SIMT)"
+    assert bench.prefill_kernel(f2.with_shape(dtype=torch.float32)) == "window prefill (SIMT)"
+    # the per-channel kernel's tcgen05 products: Gram, X S0, Q S0, state update
+    ht = f2.B * f2.H * f2.T
+    assert bench.matmul_flops_prefill(f2) == ht * (4 * 64 * 128 + 6 * 128 * 128)
+    assert bench.matmul_flops_prefill(f2.with_shape(mode="falcon2a")) == ht * (4 * 64 * 128 + 4 * 128 * 128)
     # no tensor-core FLOPs are claimed for a launch that runs no tensor-core kernel
-    assert bench.matmul_flops_prefill(W["falcon2_bf16"]) is None
+    assert bench.matmul_flops_prefill(f2.with_shape(phi="elu1")) is None
     assert bench.matmul_flops_prefill(W["falcon1_fp32"]) is None
     assert bench.matmul_flops_prefill(W["falcon1_bf16"]) > 0
     assert "falcon3_bf16" not in bench.PREFILL_WORKLOADS
