@@ -19,11 +19,14 @@
 // value channel; the state update S^T += Rw^T X).  Each channel's recurrence
 // over the chunk is one thread: the sums over earlier tokens are block-factored
 // over blocks of NB tokens, D[t-1, s] = P[t-1] (block totals between) Suf[s] for
-// s in an earlier block, so a running vector zhat (rescaled by each finished
-// block's total) turns every cross-block sum into a dot product with a row of
-// A or B; inside a block a direct product runs over at most NB - 1 tokens.  The
-// final zhat is D[C-1, s] eta_s r_s, the state update's weights.  No decay
-// product is ever divided (gamma may be zero or negative).
+// s in an earlier block, so with the weights zhat_s = eta_s r_s brought to the
+// end of the last finished block, every cross-block sum is a row of A or B
+// against zhat.  Those sums, for a block's eight rows and a warp's 32 channels,
+// are one small product (channels x s)(s x tokens) on the warp's tf32 MMAs; the
+// older blocks' weights take the previous block's decay on the way into it.
+// Inside a block a direct product runs over at most NB - 1 tokens.  At the
+// chunk's end zhat is D[C-1, s] eta_s r_s, the state update's weights.  No
+// decay product is ever divided (gamma may be zero or negative).
 //
 // One CTA per chain:
 //   warp 0      TMA producer: X (keys shifted one token unless the same-step
@@ -33,7 +36,8 @@
 //   warp 1      MMA issuer: Gram, U^T / V^T, state update.
 //   warp 2      tensor-memory allocation.
 //   warps 4-7   staging group: the Gram tile from tensor memory to fp32 A and B
-//               in shared memory, and 1 / (|x_t|^2 + lambda_t + eps).
+//               in shared memory, 1 / (|x_t|^2 + lambda_t + eps), and the fp32
+//               state pre-scaled by each channel's chunk decay.
 //   warps 8-11  channel group (thread j = value channel j = tensor-memory lane
 //               j): gates, the recurrence above, the outputs, the state carry.
 // Every wait is bounded: on expiry the kernel records an error, the other roles
