@@ -225,18 +225,19 @@ def test_falcon2_decode(mode, dtype, rbw):
     assert rel_l2(to64(Sg), Sr) <= TOL[dtype]
 
 
-def test_falcon2_workload_full_size_sampled():
+@pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
+def test_falcon2_workload_full_size_sampled(mode):
     # B8 H16 T4096 d128 bf16 with a step per value channel, the launch the
-    # bench times (AUTO: the staged per-token kernel); 3 chains checked
-    w = I.WORKLOADS["falcon2_bf16"]
+    # bench times (AUTO: the per-channel chunked kernel); 4 chains checked
+    w = I.WORKLOADS["falcon2_bf16"].with_shape(mode=mode)
     x = I.prefill_inputs(w, device=DEV)
     o, S = fw.prefill(x["q"], x["k"], x["v"], x["beta"], x["lam"], x["S0"], mode=w.mode,
                       eps=w.eps)
     fw.check()
-    chains = [0, 77, 127]
+    chains = [0, 31, 77, 127]
     xs = select_chains(x, chains)
     o_ref, S_ref = oracle.falcon2(xs["q"], xs["k"], xs["v"], xs["beta"], xs["lam"], xs["S0"],
-                                  eps=w.eps)
+                                  eps=w.eps, inner=(mode == "falcon2a"))
     og = to64(o.reshape(-1, w.T, w.d)[chains])[None]
     Sg = to64(S.reshape(-1, w.d, w.d)[chains])[None]
     gate_prefill(og, o_ref, Sg, S_ref, TOL[w.dtype])
