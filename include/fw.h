@@ -108,11 +108,14 @@ typedef enum { FW_FLAG_RBW = 1, FW_FLAG_SAME_PAIR = 2 } fw_flag;
  * FW_PHI_ELU1: elu(z) + 1 = z + 1 for z > 0, exp(z) for z <= 0. */
 typedef enum { FW_PHI_IDENTITY = 0, FW_PHI_ELU1 = 1 } fw_phi;
 
-/* Kernel choice for fw_prefill_ex.  FW_ALGO_AUTO picks the chunked
- * tensor-core kernel when it supports the call (bf16, d_k = d_v = 128), the
- * staged per-token kernel of the window family for FW_FALCON2 / FW_FALCON2A,
- * and the plain per-token SIMT recurrence otherwise; FW_ALGO_RECURRENT forces
- * the plain per-token recurrence. */
+/* Kernel choice for fw_prefill_ex.  FW_ALGO_AUTO picks a chunked tensor-core
+ * kernel when one supports the call (bf16, d_k = d_v = 128; for FW_FALCON1,
+ * FW_FALCON1A, FW_FALCON2 and FW_FALCON2A only with FW_PHI_IDENTITY): the
+ * per-channel one for FW_FALCON2 / FW_FALCON2A, the shared-step one for the
+ * other modes.  Otherwise FW_FALCON2 / FW_FALCON2A run on the staged per-token
+ * kernel of the window family and the other modes on the plain per-token SIMT
+ * recurrence.  FW_ALGO_CHUNKED insists on a chunked kernel; FW_ALGO_RECURRENT
+ * forces the plain per-token recurrence. */
 typedef enum { FW_ALGO_AUTO = 0, FW_ALGO_RECURRENT = 1, FW_ALGO_CHUNKED = 2 } fw_algo;
 
 typedef struct {
