@@ -107,3 +107,25 @@ def test_chan_chunked_matches_per_token_kernel():
         orr, Sr = _run(w, x, "recurrent")
         assert rel_l2(to64(oc), to64(orr)) <= 1e-2
         assert rel_l2(to64(Sc), to64(Sr)) <= 1e-2
+
+
+def test_chan_chunked_timeout_path_reports_and_recovers():
+    """A bounded wait on a barrier nothing arrives on runs out in the
+    per-channel kernel too: FW_ERR_TIMEOUT through fw_check, resources freed,
+    and the next call on the same context is correct."""
+    L = fw.lib()
+    w, x = _inputs(200, seed=7)
+    g = {k: (t.to(DEV) if t is not None else None) for k, t in x.items()}
+    L.fw_set_wait_limit_us(2000)
+    L.fw_debug_force_timeout(1)
+    try:
+        fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=w.mode,
+                   eps=w.eps, algo="chunked")
+        with pytest.raises(fw.FwError) as ei:
+            fw.check()
+        assert ei.value.status == -7
+    finally:
+        L.fw_debug_force_timeout(0)
+        L.fw_set_wait_limit_us(0)
+    fw.check()  # the error word was cleared
+    _check(w, x)
