@@ -403,7 +403,10 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     float n = 0.f;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) n = (e == (t & 15)) ? g[e] : n;
-                    inv[t] = 1.f / (n + lt + a.eps);
+                    // 0 where the token has no pair (past the chain's end, or the first
+                    // token of a shifted pairing without k_init): its eta is 0
+                    const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
+                    inv[t] = pair ? 1.f / (n + lt + a.eps) : 0.f;
                     lamv[t] = lt;
                 }
             }
@@ -426,9 +429,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 float gtot = 1.f;
 #pragma unroll 4
                 for (int tt = 0; tt < C; ++tt) {
-                    const int64_t tok = (int64_t)c * C + tt;
-                    const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
-                    const float eta = pair ? betam[tt * D + r] * inv[tt] : 0.f;
+                    const float eta = betam[tt * D + r] * inv[tt];   // 0 where no pair exists
                     gtot *= 1.f - eta * lamv[tt];
                 }
                 tc_fence_after();
@@ -468,7 +469,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         float *hts = reinterpret_cast<float *>(sm + OFF_HT) + (j >> 5) * (2 * NB * HTP);
         __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OUT) + j;
         // V tile element (t, j): 128-byte swizzled rows, two 64-column halves
-        const uint32_t yhalf = sb + OFF_Y + (j >= 64 ? 8 * KB : 0);
+        const uint16_t *ysm = reinterpret_cast<const uint16_t *>(sm + OFF_Y + (j >= 64 ? 8 * KB : 0));
         const uint32_t ych = (uint32_t)((j & 63) >> 3), yin = (uint32_t)(j & 7) * 2u;
         bool ok = true;
 
@@ -509,20 +510,16 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
 #pragma unroll 1
             for (int tb = 0; tb < C / NB; ++tb) {
                 const int b0 = NB * tb;
-                // gates of the block's tokens: eta = beta inv (0 where no pair exists or
-                // past the chain's end), gamma = 1 - eta lambda
+                // gates of the block's tokens: eta = beta inv (inv is 0 where no pair
+                // exists or past the chain's end), gamma = 1 - eta lambda
                 float eta[NB], gam[NB], yv[NB], uv[NB], vv[NB], pre[NB];
+                const uint16_t *yrow = ysm + (uint32_t)tb * 512u;   // rows b0 .. b0+7 (1 KB atom)
 #pragma unroll
                 for (int e = 0; e < NB; ++e) {
-                    const int64_t tok = tok0 + b0 + e;
-                    const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
-                    eta[e] = pair ? betam[(b0 + e) * D + j] * inv[b0 + e] : 0.f;
+                    eta[e] = betam[(b0 + e) * D + j] * inv[b0 + e];
                     gam[e] = 1.f - eta[e] * lamv[b0 + e];
-                    const uint32_t t = (uint32_t)(b0 + e);
-                    const uint32_t ya = yhalf + sw128(t, ych) + yin;
-                    uint16_t yb;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(yb) : "r"(ya));
-                    yv[e] = __uint_as_float((uint32_t)yb << 16);
+                    // row b0 + e of the swizzled V tile: 128-byte row e of the block's atom
+                    yv[e] = __uint_as_float((uint32_t)yrow[(e * 128 + ((ych ^ (uint32_t)e) << 4) + yin) >> 1] << 16);
                     pre[e] = (e == 0 ? 1.f : pre[e - 1]) * gam[e];
                 }
                 if (INNER) tmem_ld8(tmem + lane_base + COL_V + b0, vv);
@@ -602,7 +599,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 }
                 if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 11 : 14);
                 // the block's tokens in order; w_s = eta_s r_s
-                float rr[NB], wv[NB];
+                float rr[NB], wv[NB], wr[NB];
 #pragma unroll
                 for (int tl = 0; tl < NB; ++tl) {
                     const int t = b0 + tl;
@@ -610,29 +607,30 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     gacc *= gam[tl];                // G_t
                     const float ct = tl >= 1 ? pre[tl - 1] : 1.f;
                     float ina = 0.f, inb = 0.f;
+                    // row t's columns of the block: the strictly lower part and (for the
+                    // write-then-read output) the diagonal; the second group of four only
+                    // once the row reaches it
                     float arow[NB], brow[NB];
 #pragma unroll
                     for (int e4 = 0; e4 < NB; e4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * ABROW + b0 + e4);
-                        const float4 b4 = *reinterpret_cast<const float4 *>(Bm + t * ABROW + b0 + e4);
-                        arow[e4] = a4.x; arow[e4 + 1] = a4.y; arow[e4 + 2] = a4.z; arow[e4 + 3] = a4.w;
-                        brow[e4] = b4.x; brow[e4 + 1] = b4.y; brow[e4 + 2] = b4.z; brow[e4 + 3] = b4.w;
-                    }
-                    // D[t-1, s] = gam_{s+1} ... gam_{t-1} directly (no residual in it)
-                    float dd[NB];
-                    {
-                        float p = 1.f;
-#pragma unroll
-                        for (int sl = tl - 1; sl >= 0; --sl) {
-                            dd[sl] = p;
-                            p *= gam[sl];
+                        if (e4 <= tl) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(Am + t * ABROW + b0 + e4);
+                            const float4 b4 = *reinterpret_cast<const float4 *>(Bm + t * ABROW + b0 + e4);
+                            arow[e4] = a4.x; arow[e4 + 1] = a4.y; arow[e4 + 2] = a4.z; arow[e4 + 3] = a4.w;
+                            brow[e4] = b4.x; brow[e4 + 1] = b4.y; brow[e4 + 2] = b4.z; brow[e4 + 3] = b4.w;
                         }
+                    }
+                    // wr[s] = D[t-1, s] w_s, carried from the previous token: the older
+                    // weights take gamma_{t-1}, the newest enters as w_{t-1}
+                    if (tl >= 1) {
+#pragma unroll
+                        for (int sl = 0; sl < tl - 1; ++sl) wr[sl] *= gam[tl - 1];
+                        wr[tl - 1] = wv[tl - 1];
                     }
 #pragma unroll
                     for (int sl = 0; sl < tl; ++sl) {   // oldest first: the newest residual enters last
-                        const float zs = dd[sl] * wv[sl];
-                        if (!INNER) ina = fmaf(arow[sl], zs, ina);
-                        inb = fmaf(brow[sl], zs, inb);
+                        if (!INNER) ina = fmaf(arow[sl], wr[sl], ina);
+                        inb = fmaf(brow[sl], wr[sl], inb);
                     }
                     if (INNER) rr[tl] = yv[tl];
                     else rr[tl] = yv[tl] - gm * uv[tl] - ct * ha[tl] - ina;
