@@ -165,7 +165,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <bool INNER>
+template <bool INNER, bool RBW>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
             const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
@@ -180,7 +180,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
     const int64_t T = a.T;
     const int nch = (int)((T + C - 1) / C);
     const bool shifted = !(a.flags & FW_FLAG_SAME_PAIR);   // x_t = phi(k_{t-1})
-    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;          // o_t = S_{t-1}^T q_t
+    constexpr bool rbw = RBW;                               // o_t = S_{t-1}^T q_t
     const uint64_t limit = (uint64_t)a.wait_ns;
 
     volatile int *s_abort = reinterpret_cast<volatile int *>(sm + OFF_MISC);
@@ -514,10 +514,18 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 // exists or past the chain's end), gamma = 1 - eta lambda
                 float eta[NB], gam[NB], yv[NB], uv[NB], vv[NB], pre[NB];
                 const uint16_t *yrow = ysm + (uint32_t)tb * 512u;   // rows b0 .. b0+7 (1 KB atom)
+                float iv[NB], lv[NB];   // the block's shared scalars, two 16-byte loads each
+#pragma unroll
+                for (int e4 = 0; e4 < NB; e4 += 4) {
+                    const float4 i4 = *reinterpret_cast<const float4 *>(inv + b0 + e4);
+                    const float4 l4 = *reinterpret_cast<const float4 *>(lamv + b0 + e4);
+                    iv[e4] = i4.x; iv[e4 + 1] = i4.y; iv[e4 + 2] = i4.z; iv[e4 + 3] = i4.w;
+                    lv[e4] = l4.x; lv[e4 + 1] = l4.y; lv[e4 + 2] = l4.z; lv[e4 + 3] = l4.w;
+                }
 #pragma unroll
                 for (int e = 0; e < NB; ++e) {
-                    eta[e] = betam[(b0 + e) * D + j] * inv[b0 + e];
-                    gam[e] = 1.f - eta[e] * lamv[b0 + e];
+                    eta[e] = betam[(b0 + e) * D + j] * iv[e];
+                    gam[e] = 1.f - eta[e] * lv[e];
                     // row b0 + e of the swizzled V tile: 128-byte row e of the block's atom
                     yv[e] = __uint_as_float((uint32_t)yrow[(e * 128 + ((ych ^ (uint32_t)e) << 4) + yin) >> 1] << 16);
                     pre[e] = (e == 0 ? 1.f : pre[e - 1]) * gam[e];
@@ -777,7 +785,9 @@ cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s) {
         !make_map(&tv, a.v, a.T, a.n_chains) ||
         !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = a.mode == FW_FALCON2A ? chan_kernel<true> : chan_kernel<false>;
+    const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
+    auto kern = a.mode == FW_FALCON2A ? (rbw ? chan_kernel<true, true> : chan_kernel<true, false>)
+                                      : (rbw ? chan_kernel<false, true> : chan_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
