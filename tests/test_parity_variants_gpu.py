@@ -186,8 +186,9 @@ def _channel_betas(x, dv, seed=12):
 @pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 128),
                                      (torch.bfloat16, 128)])
 def test_falcon2_prefill(mode, rbw, same_pair, kinit, dtype, d, algo):
-    # AUTO takes the staged per-token kernel (window of one pair, a step per
-    # column); RECURRENT the plain per-token kernel.  T spans several blocks.
+    # AUTO takes the per-channel chunked kernel for bf16 with d = 128 and the
+    # staged per-token kernel (window of one pair, a step per column) for the
+    # other shapes; RECURRENT the plain per-token kernel.  T spans several blocks.
     w, x = _inputs("falcon1", dtype, d, T=70)
     x["beta"] = _channel_betas(x, d)
     k_init = torch.randn(x["k"].shape[:2] + (d,), generator=torch.Generator().manual_seed(3))
@@ -202,6 +203,26 @@ def test_falcon2_prefill(mode, rbw, same_pair, kinit, dtype, d, algo):
                                   k_init=k_init, eps=w.eps, inner=(mode == "falcon2a"), rbw=rbw,
                                   same_pair=same_pair)
     gate_prefill(to64(o), o_ref, to64(S), S_ref, TOL[dtype])
+
+
+@pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
+def test_falcon2_elu1_bf16_takes_the_per_token_kernel(mode):
+    # phi = elu+1 with bf16 d = 128: the chunked kernel declines it (its bf16
+    # Gram operands would round phi(k) ~ 1 + k), AUTO serves it on the staged
+    # per-token kernel within the bf16 gate
+    w, x = _inputs("falcon1", torch.bfloat16, 128, T=90, phi="elu1")
+    x["beta"] = _channel_betas(x, 128)
+    g = {k: (t.to(DEV) if t is not None else None) for k, t in x.items()}
+    o, S = fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=mode,
+                      phi="elu1", eps=w.eps)
+    fw.check()
+    with pytest.raises(fw.FwError):
+        fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=mode,
+                   phi="elu1", eps=w.eps, algo="chunked")
+    c = {k: t.cpu() for k, t in x.items()}
+    o_ref, S_ref = oracle.falcon2(c["q"], c["k"], c["v"], c["beta"], c["lam"], c["S0"],
+                                  phi="elu1", eps=w.eps, inner=(mode == "falcon2a"))
+    gate_prefill(to64(o), o_ref, to64(S), S_ref, TOL[torch.bfloat16])
 
 
 @pytest.mark.parametrize("mode", ["falcon2", "falcon2a"])
