@@ -381,8 +381,17 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         }
         float *Am = reinterpret_cast<float *>(sm + (r < C ? OFF_A : OFF_B));
         const int t = r & (C - 1);
+        // lambda of row t of the next chunk, loaded a chunk ahead so that its global
+        // read is not on the staging's path
+        auto lam_of = [&](int cc) -> float {
+            const int64_t tok = (int64_t)cc * C + t;
+            return (r < C && cc < nch && tok < T) ? a.lam[chain * T + tok] : 0.f;
+        };
+        float lt_next = lam_of(0);
 #pragma unroll 1
         for (int c = 0; c < nch && ok; ++c) {
+            const float lt = lt_next;
+            lt_next = lam_of(c + 1);
             {
                 bool w = cwait(bar(B_GDONE), (uint32_t)c & 1u, limit, s_abort);
                 w = w && (c < 1 || cwait(bar(B_ABFREE), (uint32_t)(c - 1) & 1u, limit, s_abort));
@@ -399,7 +408,6 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                         make_float4(g[4 * e4], g[4 * e4 + 1], g[4 * e4 + 2], g[4 * e4 + 3]);
                 if (r < C && (t >> 4) == q) {   // the diagonal: |x_t|^2
                     const int64_t tok = (int64_t)c * C + t;
-                    const float lt = tok < T ? a.lam[chain * T + tok] : 0.f;
                     float n = 0.f;
 #pragma unroll
                     for (int e = 0; e < 16; ++e) n = (e == (t & 15)) ? g[e] : n;
