@@ -90,13 +90,16 @@ static_assert(OFF_VEC % 16 == 0 && OFF_BAR % 8 == 0 && OFF_B + (uint32_t)C * ABR
 enum {
     B_FULL0 = 0, B_EMPTY0 = B_FULL0 + NST, B_FULLY = B_EMPTY0 + NST, B_YFREE, B_FULLB, B_BFREE,
     B_GDONE, B_GFREE, B_ABRDY, B_ABFREE, B_SRDY, B_UVDONE, B_RRDY, B_SDONE, B_MDRAIN, B_NEVER,
-    B_PATCH, B_SSCL, B_COUNT
+    B_PATCH, B_SSCL, B_HDONE, B_HRDY, B_COUNT
 };
 static_assert(B_COUNT <= 32, "barrier area");
 
 // tensor-memory columns (128 lanes x 32 bit); the state is held transposed
 // (lane j), with a bf16 copy (two i per column), the A operand of U^T and V^T
 constexpr uint32_t COL_G = 0, COL_U = 64, COL_V = 128, COL_SB = 192, COL_S = 256;
+// [X_{c+1}; Q_{c+1}] X_c^T, the cross Gram that carries chunk c's state update into
+// chunk c+1's U and V
+constexpr uint32_t COL_H = 384;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint64_t kDrainNs = 2000000000ull;
@@ -198,7 +201,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t n = 1;
             if (i == B_YFREE || i == B_GFREE || i == B_ABRDY || i == B_ABFREE || i == B_SRDY ||
-                i == B_RRDY || i == B_SSCL)
+                i == B_RRDY || i == B_SSCL || i == B_HRDY)
                 n = 4;   // one arrival per warp of the publishing group
             if (i == B_BFREE) n = 8;   // the beta rows are read by both groups
             mbar_init(bar(i), n);
@@ -301,33 +304,87 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 mma_commit(bar(B_GDONE));
                 return true;
             };
+            const uint32_t id64 = idesc_bf16(128, 64, false, false);
             if (nch > 0) ok = issue_g(0);
-            for (int c = 0; c < nch && ok; ++c) {
-                const uint32_t st = xq(c % NST);
-                // U^T = S^T X^T (not for the additive write), V^T = S^T Q^T from the
-                // bf16 state copy of chunk c's start
-                if (!cwait(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
-                tc_fence_after();
-                {
-                    const uint32_t id = idesc_bf16(128, 64, false, false);
+            // chunk 0's U^T = S0^T X^T (not for the additive write), V^T = S0^T Q^T from
+            // the bf16 copy of the initial state
+            if (ok && nch > 0) {
+                if (!cwait(bar(B_SRDY), 0u, limit, s_abort)) ok = false;
+                if (ok) {
+                    tc_fence_after();
                     const uint32_t sa = tmem + COL_SB;
-                    const uint64_t dxk = sdesc_sw128(st + XQ_X0, 16, 1024);
-                    const uint64_t dqk = sdesc_sw128(st + XQ_Q0, 16, 1024);
+                    const uint64_t dxk = sdesc_sw128(xq(0) + XQ_X0, 16, 1024);
+                    const uint64_t dqk = sdesc_sw128(xq(0) + XQ_Q0, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
-                        if (!INNER) mma_bf16_ta(tmem + COL_U, sa + 8 * kk, dxk + off, id, kk > 0);
-                        mma_bf16_ta(tmem + COL_V, sa + 8 * kk, dqk + off, id, kk > 0);
+                        if (!INNER) mma_bf16_ta(tmem + COL_U, sa + 8 * kk, dxk + off, id64, kk > 0);
+                        mma_bf16_ta(tmem + COL_V, sa + 8 * kk, dqk + off, id64, kk > 0);
                     }
                     mma_commit(bar(B_UVDONE));
-                    CTRACE(c, 6);
                 }
-                // the next chunk's Gram while this chunk's channels run
-                if (c + 1 < nch && !issue_g(c + 1)) { ok = false; break; }
+            }
+            for (int c = 0; c < nch && ok; ++c) {
+                const uint32_t st = xq(c % NST);
+                const bool more = c + 1 < nch;
+                if (more) {
+                    const uint32_t stn = xq((c + 1) % NST);
+                    // the next chunk's Gram while this chunk's channels run, then the cross
+                    // Gram H = [X_{c+1}; Q_{c+1}] X_c^T (its region is free: the staging
+                    // group has read the previous one)
+                    if (!issue_g(c + 1)) { ok = false; break; }
+                    if (c >= 1 && !cwait(bar(B_HRDY), (uint32_t)(c - 1) & 1u, limit, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        const uint64_t dn = sdesc_sw128(stn + XQ_X0, 16, 1024);
+                        const uint64_t dc = sdesc_sw128(st + XQ_X0, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                            mma_bf16(tmem + COL_H, dn + off, dc + off, id64, kk > 0);
+                        }
+                        mma_commit(bar(B_HDONE));
+                    }
+                    // chunk c+1's U and V: S_{c+1} = diag(G_C) S_c + X_c^T Rw_c, so
+                    //   U^T = (diag(G_C) S_c)^T X_{c+1}^T + Rw_c^T (X_c X_{c+1}^T)
+                    // (V with Q_{c+1}).  The first part from the staging group's bf16 copy
+                    // of the pre-scaled state, once this chunk's channels have read U / V;
+                    // the second once the weights and H are staged.
+                    if (!cwait(bar(B_ABFREE), (uint32_t)c & 1u, limit, s_abort) ||
+                        !cwait(bar(B_SSCL), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        const uint32_t sa = tmem + COL_SB;
+                        const uint64_t dxk = sdesc_sw128(stn + XQ_X0, 16, 1024);
+                        const uint64_t dqk = sdesc_sw128(stn + XQ_Q0, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                            if (!INNER) mma_bf16_ta(tmem + COL_U, sa + 8 * kk, dxk + off, id64, kk > 0);
+                            mma_bf16_ta(tmem + COL_V, sa + 8 * kk, dqk + off, id64, kk > 0);
+                        }
+                    }
+                    if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort) ||
+                        !cwait(bar(B_HRDY), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        const uint64_t dr = sdesc_sw128(sb + OFF_RT, 16, 1024);
+                        const uint64_t dhx = sdesc_sw128(st + XQ_Q0, 16, 1024);   // H rows of X_{c+1}
+                        const uint64_t dhq = sdesc_sw128(st + XQ_Q1, 16, 1024);   // H rows of Q_{c+1}
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (!INNER) mma_bf16(tmem + COL_U, dr + kk * 2, dhx + kk * 2, id64, 1);
+                            mma_bf16(tmem + COL_V, dr + kk * 2, dhq + kk * 2, id64, 1);
+                        }
+                        mma_commit(bar(B_UVDONE));
+                        CTRACE(c, 6);
+                    }
+                } else {
+                    if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort) ||
+                        !cwait(bar(B_SSCL), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
+                    tc_fence_after();
+                }
                 // S^T += Rw^T X, onto the state pre-scaled by the chunk's decay
-                if (!cwait(bar(B_RRDY), (uint32_t)c & 1u, limit, s_abort) ||
-                    !cwait(bar(B_SSCL), (uint32_t)c & 1u, limit, s_abort)) { ok = false; break; }
-                tc_fence_after();
                 {
                     const uint32_t id_s = idesc_bf16(128, 128, false, true);
                     const uint64_t dr = sdesc_sw128(sb + OFF_RT, 16, 1024);
@@ -385,7 +442,9 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         // read is not on the staging's path
         auto lam_of = [&](int cc) -> float {
             const int64_t tok = (int64_t)cc * C + t;
-            return (r < C && cc < nch && tok < T) ? a.lam[chain * T + tok] : 0.f;
+            // a volatile read: issued here and kept in its register, not re-read at the use
+            return (r < C && cc < nch && tok < T)
+                       ? *static_cast<const volatile float *>(a.lam + chain * T + tok) : 0.f;
         };
         float lt_next = lam_of(0);
 #pragma unroll 1
@@ -398,19 +457,25 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 if (bar_or(BAR_SGRP, GROUP, !w)) { ok = false; break; }
             }
             tc_fence_after();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {   // 16 columns s at a time
-                float g[16];
-                tmem_ld16(tmem + lane_base + COL_G + 16 * q, g);
+            {
+                // the whole row in two 32-column loads and one wait
+                float ga[32], gb[32];
+                tmem_ld32x2(tmem + lane_base + COL_G, tmem + lane_base + COL_G + 32, ga, gb);
 #pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4)
-                    *reinterpret_cast<float4 *>(Am + t * ABROW + 16 * q + 4 * e4) =
-                        make_float4(g[4 * e4], g[4 * e4 + 1], g[4 * e4 + 2], g[4 * e4 + 3]);
-                if (r < C && (t >> 4) == q) {   // the diagonal: |x_t|^2
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    *reinterpret_cast<float4 *>(Am + t * ABROW + 4 * e4) =
+                        make_float4(ga[4 * e4], ga[4 * e4 + 1], ga[4 * e4 + 2], ga[4 * e4 + 3]);
+                    *reinterpret_cast<float4 *>(Am + t * ABROW + 32 + 4 * e4) =
+                        make_float4(gb[4 * e4], gb[4 * e4 + 1], gb[4 * e4 + 2], gb[4 * e4 + 3]);
+                }
+                if (r < C) {   // the diagonal: |x_t|^2
                     const int64_t tok = (int64_t)c * C + t;
                     float n = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) n = (e == (t & 15)) ? g[e] : n;
+                    for (int e = 0; e < 32; ++e) {
+                        n = (e == t) ? ga[e] : n;
+                        n = (e + 32 == t) ? gb[e] : n;
+                    }
                     // 0 where the token has no pair (past the chain's end, or the first
                     // token of a shifted pairing without k_init): its eta is 0
                     const bool pair = tok < T && (!shifted || tok > 0 || a.k_init != nullptr);
@@ -426,9 +491,13 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             }
             if (r == 0) CTRACE(c, 8);
             // this chunk's total decay of channel r, and the fp32 state (lane r) pre-scaled
-            // by it, once the state carry of the previous chunk has read the state
+            // by it with a bf16 copy (the A operand of the next chunk's U and V), once the
+            // previous chunk's state update is done and this chunk's U and V are formed
+            // (they read the previous copy)
             {
-                bool w = cwait(bar(B_SRDY), (uint32_t)c & 1u, limit, s_abort);
+                bool w = cwait(bar(B_UVDONE), (uint32_t)c & 1u, limit, s_abort);
+                w = w && (c == 0 ? cwait(bar(B_SRDY), 0u, limit, s_abort)
+                                 : cwait(bar(B_SDONE), (uint32_t)(c - 1) & 1u, limit, s_abort));
                 w = w && cwait(bar(B_FULLB), (uint32_t)c & 1u, limit, s_abort);
                 if (bar_or(BAR_SGRP, GROUP, !w)) { ok = false; break; }
             }
@@ -449,6 +518,10 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     for (int e = 0; e < 32; ++e) v[e] *= gtot;
                     tmem_st16(tmem + lane_base + COL_S + 32 * q, v);
                     tmem_st16(tmem + lane_base + COL_S + 32 * q + 16, v + 16);
+                    float pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(v[2 * e], v[2 * e + 1]));
+                    tmem_st16(tmem + lane_base + COL_SB + 16 * q, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -457,6 +530,25 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     mbar_arrive(bar(B_SSCL));
                     mbar_arrive(bar(B_BFREE));
                 }
+            }
+            // H = [X_{c+1}; Q_{c+1}] X_c^T as bf16 K-major rows (row r: r < 64 the next
+            // keys', else the next queries') into this chunk's Q tile, which V^T has read
+            if (c + 1 < nch) {
+                const bool w = cwait(bar(B_HDONE), (uint32_t)c & 1u, limit, s_abort);
+                if (bar_or(BAR_SGRP, GROUP, !w)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t hb = xq(c % NST) + (r < C ? XQ_Q0 : XQ_Q1);
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {   // 16 columns s at a time
+                    float g[16];
+                    tmem_ld16(tmem + lane_base + COL_H + 16 * q, g);
+                    st_row8(hb + sw128((uint32_t)t, (uint32_t)(2 * q)), g);
+                    st_row8(hb + sw128((uint32_t)t, (uint32_t)(2 * q + 1)), g + 8);
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_HRDY));
             }
         }
         if (!ok && r == 0) fail_now();
@@ -702,30 +794,20 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                 tma_store_3d(&tmo, sb + OFF_OUT, 0, (int)tok0, (int)chain);
                 bulk_commit();
             }
-            // state carry: once the update is done, the bf16 copy for the next chunk
-            // (the last chunk writes S_T)
-            if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
-            if (j == 0) CTRACE(c, 3);
-            tc_fence_after();
-            const bool last = (c + 1 == nch);
+            // the last chunk writes S_T once its state update is done (the next chunk's
+            // U and V come from the staging group's bf16 copy and the cross Gram)
+            if (c + 1 == nch) {
+                if (!gwait(bar(B_SDONE), (uint32_t)c & 1u)) { ok = false; break; }
+                if (j == 0) CTRACE(c, 3);
+                tc_fence_after();
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float v[32];
-                tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
-                if (last) {
+                for (int q = 0; q < 4; ++q) {
+                    float v[32];
+                    tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) a.S_T[(chain * D + 32 * q + e) * D + j] = v[e];
-                } else {
-                    float pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = __uint_as_float(pack_bf16(v[2 * e], v[2 * e + 1]));
-                    tmem_st16(tmem + lane_base + COL_SB + 16 * q, pk);
                 }
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0 && !last) mbar_arrive(bar(B_SRDY));
             if (j == 0) CTRACE(c, 4);
         }
         if (!ok && j == 0) fail_now();
