@@ -16,7 +16,11 @@
 //   S_C[:, j] = G_{C-1} S0[:, j] + X^T (D[C-1, .] eta r).
 // The shared matrix products run on tcgen05 (the Gram [X;Q] X^T; U^T = S^T X^T
 // and V^T = S^T Q^T with the state transposed in tensor memory, one lane per
-// value channel; the state update S^T += Rw^T X).  Each channel's recurrence
+// value channel; the state update S^T += Rw^T X).  From the second chunk on, U
+// and V do not wait for the state update: with S_{c+1} = diag(G_C) S_c +
+// X_c^T Rw_c, U^T(c+1) = (diag(G_C) S_c)^T X_{c+1}^T + Rw_c^T (X_c X_{c+1}^T)
+// (V with Q_{c+1}), from a bf16 copy of the pre-scaled state and the cross
+// Gram [X_{c+1}; Q_{c+1}] X_c^T formed during chunk c.  Each channel's recurrence
 // over the chunk is one thread: the sums over earlier tokens are block-factored
 // over blocks of NB tokens, D[t-1, s] = P[t-1] (block totals between) Suf[s] for
 // s in an earlier block, so with the weights zhat_s = eta_s r_s brought to the
@@ -33,13 +37,14 @@
 //               pair; the row before the sequence reads as zero) and Q tiles,
 //               64 x 128 bf16, 128-byte swizzle, in a two-stage ring; the V
 //               tile; the chunk's beta rows (64 x 128 fp32, one bulk copy).
-//   warp 1      MMA issuer: Gram, U^T / V^T, state update.
+//   warp 1      MMA issuer: Gram, cross Gram, U^T / V^T, state update.
 //   warp 2      tensor-memory allocation.
 //   warps 4-7   staging group: the Gram tile from tensor memory to fp32 A and B
-//               in shared memory, 1 / (|x_t|^2 + lambda_t + eps), and the fp32
-//               state pre-scaled by each channel's chunk decay.
+//               in shared memory, 1 / (|x_t|^2 + lambda_t + eps), the fp32
+//               state pre-scaled by each channel's chunk decay with its bf16
+//               copy, and the cross Gram as bf16 rows in the chunk's Q tile.
 //   warps 8-11  channel group (thread j = value channel j = tensor-memory lane
-//               j): gates, the recurrence above, the outputs, the state carry.
+//               j): gates, the recurrence above, the outputs, the weights, S_T.
 // Every wait is bounded: on expiry the kernel records an error, the other roles
 // stop at their next wait, copies and MMAs in flight are drained, tensor memory
 // is freed and the kernel exits.
