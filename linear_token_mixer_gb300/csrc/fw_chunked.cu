@@ -33,7 +33,10 @@
 //               triangular solve, -W^T staging.
 //   warps 8-11  state group: R staging, state carry (fp32 in tensor memory,
 //               with a bf16 copy in tensor memory as the A operand of R^T and
-//               O1^T), outputs o_t = G_t O1_t + O2_t.
+//               O1^T), outputs o_t = G_t O1_t + O2_t, stored by each thread
+//               straight to global memory (the four warps write one 256-byte
+//               row per token), so no staging tile or store wait sits on the
+//               state path.
 // All chunk products are tcgen05 MMAs with M = 128 (transposed forms keep d on
 // the M side), bf16 operands and fp32 accumulators in tensor memory.  The
 // triangular solve inverts the four 16x16 diagonal blocks by fp32 forward
@@ -196,7 +199,7 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
 template <bool GATED, bool FALCON, bool SPLIT_CARRY>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+               const __grid_constant__ CUtensorMap tmv,
                const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived from the shared array itself so that every
@@ -235,7 +238,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         for (int i = 0; i < B_COUNT; ++i) {
             uint32_t n = 1;
             if (falcon && (i == B_TRDY || i == B_WRDY || i == B_GGO)) n = KGROUP / 32;
-            if (i == B_SRDY || i == B_SSCL || i == B_RRDY || i == B_RFREE) n = GROUP / 32;
+            if (i == B_SRDY || i == B_SSCL || i == B_RRDY || i == B_RFREE || i == B_OFREE) n = GROUP / 32;
             mbar_init(bar(i), n);
         }
         fence_mbar_init();
@@ -246,7 +249,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
-        tma_prefetch_desc(&tmo);
     }
     tc_fence_before();
     __syncthreads();
@@ -1017,7 +1019,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const bool ok = wait_bar(bb, parity, limit, s_abort);
             return !bar_or(BAR_SG, GROUP, !ok);
         };
-        auto gsync = [&]() { bar_sync(BAR_SG, GROUP); };
         bool ok = true;
 
         // bf16 copy of 32 state entries (i = i0 .. i0+31 of column j): the A operand
@@ -1063,9 +1064,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             const int b = c % NST;   // gate block
             const int64_t tok0 = (int64_t)c * C;
             if (gated) {
-                // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand);
-                //      the output store of chunk c-1 has read the R^T buffer by then
-                if (srow == 0) { TRACE(c, 31); bulk_wait_read0(); }
+                // ---- R^T -> bf16 rows j (A operand) and diag(w)-scaled copy (B operand)
+                if (srow == 0) TRACE(c, 31);
                 {
                     bool w = wait_bar(bar(B_RDONE), (uint32_t)c & 1u, limit, s_abort);
                     w = w && wait_bar(bar(B_GV0 + b), (uint32_t)(c / NST) & 1u, limit, s_abort);
@@ -1104,9 +1104,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (srow == 0) TRACE(c, 11);
             }
 
-            // ---- state carry (linear attention: the output store of chunk c-1 has read
-            //      its staging tile before this chunk's is written)
-            if (srow == 0) bulk_wait_read0();
+            // ---- state carry
             const bool last = (c + 1 == nch);
             {
                 bool w = wait_bar(bar(B_SDONE), (uint32_t)c & 1u, limit, s_abort);
@@ -1184,12 +1182,13 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 if (srow == 0) TRACE(c, 13);
             }
 
-            // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t, staged as a [t][j] bf16 tile
-            //      in the R^T buffer (free once S(c) and O2(c) are done: s_done),
-            //      then one tensor store (rows past T are not written)
+            // ---- outputs o_t = G_t (S0^T q_t) + (P R)_t, bf16, thread j writing column
+            //      j of each token's row (rows past T are not written); each warp then
+            //      frees its lanes of O1 and O2 for the next chunk's products
             {
                 const float *gv = reinterpret_cast<const float *>(sm + OFF_SGV);
-                __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RA) + srow;
+                __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T + tok0) * D + srow;
+                const int tlim = T - tok0 < (int64_t)C ? (int)(T - tok0) : C;
 #pragma unroll 1
                 for (int h = 0; h < 4; ++h) {   // (a rolled loop: short code beside the other roles')
                     float o1[16], o2[16];
@@ -1203,23 +1202,16 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int t = 16 * h + 4 * e4 + e;
-                            ot[t * D] = __float2bfloat16_rn(fmaf(gg[e], o1[4 * e4 + e], o2[4 * e4 + e]));
+                            if (t < tlim) ot[t * D] = __float2bfloat16_rn(fmaf(gg[e], o1[4 * e4 + e], o2[4 * e4 + e]));
                         }
                     }
                 }
             }
-            fence_proxy_async();
             tc_fence_before();
-            gsync();
-            if (srow == 0) {
-                tma_store_3d(&tmo, sb + OFF_RA, 0, (int)tok0, (int)chain);
-                bulk_commit();
-                TRACE(c, 14);
-                mbar_arrive(bar(B_OFREE));
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_OFREE));   // each warp its lanes of O1, O2
         }
         if (!ok && srow == 0) fail_now();
-        if (srow == 0) bulk_wait0();   // no output store in flight at exit
     }
 
     // every role meets here; tensor memory is released last
@@ -1245,19 +1237,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [n_chains][T][128] bf16 viewed as a 3-D tensor (d, T, chain); boxes of box_d x 64:
-// 64 x 64 with the 128-byte swizzle for the tile loads, 128 x 64 plain for the
-// output store.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t box_d = 64,
-              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
+// [n_chains][T][128] bf16 viewed as a 3-D tensor (d, T, chain); 64 x 64 boxes with
+// the 128-byte swizzle for the tile loads.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)nc};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {box_d, (cuuint32_t)C, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1271,7 +1261,7 @@ bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t b
 bool chunked_supported(const PrefillArgs &a) {
     if (a.mode != FW_LINATTN && a.phi == FW_PHI_ELU1) return false;
     // a step per value channel gives every channel its own triangular system:
-    // Falcon-2 / 2A run on the per-token kernel
+    // Falcon-2 / 2A run on the per-channel chunked kernel (or the per-token one)
     if (a.mode == FW_FALCON2 || a.mode == FW_FALCON2A) return false;
     return a.dtype == FW_BF16 && a.d == D && a.T <= (int64_t)INT32_MAX - C &&
            a.n_chains <= (int64_t)INT32_MAX;
@@ -1285,10 +1275,9 @@ extern "C" int fw_debug_read_trace(unsigned long long *dst, int n) {
 #endif
 
 cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
-        !make_map(&tv, a.v, a.T, a.n_chains) ||
-        !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map(&tv, a.v, a.T, a.n_chains))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1307,7 +1296,7 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)SMEM_ALLOC)) != cudaSuccess)
         return e;
-    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
+    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 

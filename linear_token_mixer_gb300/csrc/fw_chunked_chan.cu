@@ -44,7 +44,10 @@
 //               state pre-scaled by each channel's chunk decay with its bf16
 //               copy, and the cross Gram as bf16 rows in the chunk's Q tile.
 //   warps 8-11  channel group (thread j = value channel j = tensor-memory lane
-//               j): gates, the recurrence above, the outputs, the weights, S_T.
+//               j): gates, the recurrence above, the weights, S_T, and the
+//               outputs, stored by each thread straight to global memory as
+//               they are formed (the four warps write one 256-byte row per
+//               token), so no chunk-end store or its wait is on the path.
 // Every wait is bounded: on expiry the kernel records an error, the other roles
 // stop at their next wait, copies and MMAs in flight are drained, tensor memory
 // is freed and the kernel exits.
@@ -78,8 +81,7 @@ constexpr int ABROW = 68;                  // row stride of A and B (64 + 4: con
 constexpr uint32_t OFF_A = 112 * KB;       // X X^T, fp32 [t][s]
 constexpr uint32_t OFF_B = OFF_A + (uint32_t)C * ABROW * 4;   // Q X^T, fp32 [t][s]
 constexpr uint32_t OFF_RT = 147 * KB;      // (weights * r)^T, bf16 rows j (K-major A operand)
-constexpr uint32_t OFF_OUT = OFF_RT + 16 * KB;   // output tile, bf16 [t][j]
-constexpr uint32_t OFF_Z = OFF_OUT + 16 * KB;    // zhat per channel, fp32 rows j of ZROW floats
+constexpr uint32_t OFF_Z = OFF_RT + 16 * KB;     // zhat per channel, fp32 rows j of ZROW floats
 constexpr int ZROW = 68;                   // 64 + 4 (16-byte groups spread over the banks)
 constexpr int HTP = 36;                    // row stride of the H transposes (8 HTP = 8 mod 32: no conflicts)
 constexpr uint32_t OFF_HT = OFF_Z + (uint32_t)D * ZROW * 4;    // per channel warp: H_A, H_B [8][HTP]
@@ -176,8 +178,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
 template <bool INNER, bool RBW>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
-            const PrefillArgs a) {
+            const __grid_constant__ CUtensorMap tmv, const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived from the shared array itself (shared-space loads)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -219,7 +220,6 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
-        tma_prefetch_desc(&tmo);
     }
     tc_fence_before();
     __syncthreads();
@@ -561,7 +561,6 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         // ================================================================ channel group
         const int j = tid - CG_W0 * 32;   // value channel == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        auto gsync = [&]() { bar_sync(BAR_CGRP, GROUP); };
         auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool w = cwait(bb, parity, limit, s_abort);
             return !bar_or(BAR_CGRP, GROUP, !w);
@@ -572,7 +571,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
         float *zrow = reinterpret_cast<float *>(sm + OFF_Z) + j * ZROW;
         const int jw0 = j & ~31;   // first channel of this warp
         float *hts = reinterpret_cast<float *>(sm + OFF_HT) + (j >> 5) * (2 * NB * HTP);
-        __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_OUT) + j;
+        __nv_bfloat16 *const og = reinterpret_cast<__nv_bfloat16 *>(a.o) + chain * T * D + j;
         // V tile element (t, j): 128-byte swizzled rows, two 64-column halves
         const uint16_t *ysm = reinterpret_cast<const uint16_t *>(sm + OFF_Y + (j >= 64 ? 8 * KB : 0));
         const uint32_t ych = (uint32_t)((j & 63) >> 3), yin = (uint32_t)(j & 7) * 2u;
@@ -599,8 +598,8 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
 #pragma unroll 1
         for (int c = 0; c < nch && ok; ++c) {
             const int64_t tok0 = (int64_t)c * C;
-            // the previous output store has read the output tile
-            if (j == 0) bulk_wait_read0();
+            __nv_bfloat16 *const ot = og + tok0 * D;   // row t of the chunk: ot[t * D]
+            const int tlim = T - tok0 < (int64_t)C ? (int)(T - tok0) : C;   // rows past T are not written
             {
                 bool w = cwait(bar(B_ABRDY), (uint32_t)c & 1u, limit, s_abort);
                 w = w && cwait(bar(B_UVDONE), (uint32_t)c & 1u, limit, s_abort);
@@ -751,7 +750,7 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
                     float o;
                     if (rbw) o = gm * vv[tl] + ct * hb[tl] + inb;
                     else o = gacc * vv[tl] + gam[tl] * (ct * hb[tl] + inb) + brow[tl] * wv[tl];
-                    ot[t * D] = __float2bfloat16_rn(o);
+                    if (t < tlim) ot[t * D] = __float2bfloat16_rn(o);
                 }
                 if (j == 0 && (tb == 0 || tb == 7)) CTRACE(c, tb == 0 ? 12 : 15);
                 // the block is done: its own tokens take the suffix products to its
@@ -792,13 +791,6 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_RRDY));
             if (j == 0) CTRACE(c, 2);
-            // the chunk's outputs: one tensor store (rows past T are not written)
-            fence_proxy_async();
-            gsync();
-            if (j == 0) {
-                tma_store_3d(&tmo, sb + OFF_OUT, 0, (int)tok0, (int)chain);
-                bulk_commit();
-            }
             // the last chunk writes S_T once its state update is done (the next chunk's
             // U and V come from the staging group's bf16 copy and the cross Gram)
             if (c + 1 == nch) {
@@ -816,7 +808,6 @@ chan_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUt
             if (j == 0) CTRACE(c, 4);
         }
         if (!ok && j == 0) fail_now();
-        if (j == 0) bulk_wait0();   // no output store in flight at exit
     }
 
     // every role meets here; tensor memory is released last
@@ -843,17 +834,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [n_chains][T][128] bf16 viewed as (d, T, chain): 64 x 64 boxes with the 128-byte
-// swizzle for the tile loads, 128 x 64 plain for the output store.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc, uint32_t box_d = 64,
-              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
+// swizzle for the tile loads.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int64_t nc) {
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)nc};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {box_d, (cuuint32_t)C, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)C, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -875,10 +865,9 @@ extern "C" int fw_debug_read_chan_trace(unsigned long long *dst, int n) {
 #endif
 
 cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
-        !make_map(&tv, a.v, a.T, a.n_chains) ||
-        !make_map(&to, a.o, a.T, a.n_chains, (uint32_t)D, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !make_map(&tv, a.v, a.T, a.n_chains))
         return cudaErrorInvalidValue;
     const bool rbw = (a.flags & FW_FLAG_RBW) != 0;
     auto kern = a.mode == FW_FALCON2A ? (rbw ? chan_kernel<true, true> : chan_kernel<true, false>)
@@ -886,7 +875,7 @@ cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, to, a);
+    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 
