@@ -289,6 +289,20 @@ void fw_set_wait_limit_us(long long us);
  * No GPU fault is involved. */
 void fw_debug_force_timeout(int on);
 
+/* Testing hook for the two-segment form of the chunked prefill (Falcon-1, 1A,
+ * linear attention; bf16, d = 128).  With few chains and a long sequence the
+ * chunked launch splits each chain at a chunk boundary near T/2 and runs, at
+ * once, the first segment from S0, the second from a zero state, and the second
+ * again from S = I with zero targets; since the state map of a segment is affine
+ * in its initial state (S_t = Phi_t S_mid + S_t^0), a second kernel then adds
+ * S_mid^T (Phi_t^T q_t) to the second segment's outputs and forms
+ * S_T = Phi_T S_mid + S_T^0.  mode 0 (default): the launch decides (at most a
+ * third of the SMs hold a chain and T >= 4096); 1: split whenever T spans two
+ * chunks; -1: never.  Applies to later calls.  The split draws its workspace
+ * (bf16 n_chains x (T - T/2) x 128 and fp32 3 x n_chains x 128 x 128) from a
+ * stream-ordered pool; without it the call runs unsplit. */
+void fw_debug_segment_split(int mode);
+
 #ifdef __cplusplus
 }
 #endif

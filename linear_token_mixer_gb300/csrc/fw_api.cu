@@ -16,6 +16,7 @@ thread_local int g_last_cuda_error = 0;
 constexpr long long kDefaultWaitUs = 2000000;  // 2 s
 std::atomic<long long> g_wait_us{kDefaultWaitUs};
 std::atomic<int> g_force_timeout{0};
+std::atomic<int> g_seg_pref{0};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
@@ -178,6 +179,8 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     a.dtype = dtype; a.mode = mode; a.phi = phi; a.eps = eps; a.flags = flags;
     a.wait_ns = g_wait_us.load() * 1000LL;
     a.force_timeout = g_force_timeout.load();
+    a.seg_pref = g_seg_pref.load();
+    a.seg_t0 = 0; a.o_aux = nullptr; a.s_aux = nullptr;
 
     const bool chunk_ok = per_channel(mode) ? chunked_chan_supported(a) : chunked_supported(a);
     if (algo == FW_ALGO_CHUNKED && !chunk_ok) return FW_ERR_UNSUPPORTED;
@@ -429,3 +432,5 @@ extern "C" void fw_set_wait_limit_us(long long us) {
 }
 
 extern "C" void fw_debug_force_timeout(int on) { g_force_timeout.store(on ? 1 : 0); }
+
+extern "C" void fw_debug_segment_split(int mode) { g_seg_pref.store(mode > 0 ? 1 : mode < 0 ? -1 : 0); }

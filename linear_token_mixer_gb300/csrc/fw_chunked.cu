@@ -196,7 +196,7 @@ __device__ __forceinline__ void frag_b32(const float *M, int k0, int n0, int lan
 // GATED: eta, gamma and decays (not linear attention); FALCON: the residual
 // write (L, T, W).  Each mode is its own instantiation, so no role's loop
 // carries another mode's code.
-template <bool GATED, bool FALCON, bool SPLIT_CARRY>
+template <bool GATED, bool FALCON, bool SPLIT_CARRY, bool SEGS>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv,
@@ -208,9 +208,19 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int64_t chain = blockIdx.x;
-    const int64_t T = a.T;
+    // Two-segment form (a.seg_t0 > 0, three CTAs per chain): role 0 runs tokens
+    // [0, seg_t0) from S0, role 1 tokens [seg_t0, T) from a zero state, role 2 the
+    // same tokens from S = I with zero targets (its outputs are Phi_t^T q_t and its
+    // final state Phi_T); segment_fixup_kernel combines them.
+    // (SEGS: a separate instantiation, so the one-segment kernels carry none of it)
+    const int64_t T_all = a.T;
+    constexpr bool segs = SEGS;
+    const int role = segs ? (int)((int64_t)blockIdx.x / a.n_chains) : 0;
+    const int64_t chain = segs ? (int64_t)blockIdx.x % a.n_chains : (int64_t)blockIdx.x;
+    const int64_t t_base = role == 0 ? 0 : a.seg_t0;   // first token of this CTA's segment
+    const int64_t T = segs ? (role == 0 ? a.seg_t0 : T_all - a.seg_t0) : T_all;   // its length
     const int nch = (int)((T + C - 1) / C);
+    const void *const k_init = role == 0 ? a.k_init : nullptr;
     constexpr bool gated = GATED;                                  // eta, gamma, decays
     constexpr bool falcon = FALCON;                                // residual: L, T, W
     const bool shifted = gated && !(a.flags & FW_FLAG_SAME_PAIR);  // x_t = phi(k_{t-1})
@@ -244,6 +254,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         fence_mbar_init();
         *s_abort = 0;
     }
+    if (role == 2) {   // zero targets: the V tiles are never loaded
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = tid; i < (int)(16 * KB / 16); i += NTHREADS) {
+            reinterpret_cast<float4 *>(sm + OFF_Y0)[i] = z4;
+            if (!gated) {
+                reinterpret_cast<float4 *>(sm + OFF_Y1)[i] = z4;
+                reinterpret_cast<float4 *>(sm + OFF_TF)[i] = z4;
+            }
+        }
+        fence_proxy_async();
+    }
     if (warp == 3) tmem_alloc(sb + OFF_MISC + 4, TMEM_COLS);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmq);
@@ -272,14 +293,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const int b = cx % NST;
                     if (cx < NST || mbar_test(bar(B_EMPTY0 + b), (uint32_t)((cx / NST) - 1) & 1u)) {
                         const uint32_t st = xq(b);
-                        const int y = cx * C;
+                        const int y = (int)(t_base + (int64_t)cx * C);
                         const uint32_t full = bar(B_FULL0 + b);
-                        mbar_expect_tx(full, gated ? 32 * KB : 48 * KB);
+                        mbar_expect_tx(full, (gated || role == 2) ? 32 * KB : 48 * KB);
                         tma_load_3d(st + XQ_X0, &tmk, 0, y - shift, (int)chain, full);
                         tma_load_3d(st + XQ_X1, &tmk, 64, y - shift, (int)chain, full);
                         tma_load_3d(st + XQ_Q0, &tmq, 0, y, (int)chain, full);
                         tma_load_3d(st + XQ_Q1, &tmq, 64, y, (int)chain, full);
-                        if (!gated) {
+                        if (!gated && role != 2) {
                             const uint32_t yv = yv_of(b);
                             tma_load_3d(yv, &tmv, 0, y, (int)chain, full);
                             tma_load_3d(yv + 8 * KB, &tmv, 64, y, (int)chain, full);
@@ -292,10 +313,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 }
                 if (gated && cy < nch && cy < cx &&
                     (cy == 0 || mbar_test(bar(B_YFREE), (uint32_t)(cy - 1) & 1u))) {
-                    const int y = cy * C;
-                    mbar_expect_tx(bar(B_FULLY), 16 * KB);
-                    tma_load_3d(sb + OFF_Y0, &tmv, 0, y, (int)chain, bar(B_FULLY));
-                    tma_load_3d(sb + OFF_Y0 + 8 * KB, &tmv, 64, y, (int)chain, bar(B_FULLY));
+                    const int y = (int)(t_base + (int64_t)cy * C);
+                    if (role == 2) {
+                        mbar_arrive(bar(B_FULLY));   // zero targets: the tile stays zero
+                    } else {
+                        mbar_expect_tx(bar(B_FULLY), 16 * KB);
+                        tma_load_3d(sb + OFF_Y0, &tmv, 0, y, (int)chain, bar(B_FULLY));
+                        tma_load_3d(sb + OFF_Y0 + 8 * KB, &tmv, 64, y, (int)chain, bar(B_FULLY));
+                    }
                     ++ny;
                     ++cy;
                     progressed = true;
@@ -517,8 +542,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             for (int u = 0; u < 2; ++u) {
                 const int64_t tok = (int64_t)cc * C + lane + 32 * u;
                 if (gated && cc < nch && tok < T) {
-                    nb[u] = a.beta[chain * T + tok];
-                    nl[u] = a.lam[chain * T + tok];
+                    nb[u] = a.beta[chain * T_all + t_base + tok];
+                    nl[u] = a.lam[chain * T_all + t_base + tok];
                 }
             }
         };
@@ -529,7 +554,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             float *vg = vec(b);
             bool w = wait_bar(bar(B_FULL0 + b), (uint32_t)(cc / NST) & 1u, limit, s_abort);
             // chunk 0's first key row is patched with phi(k_init) before the Gram is released
-            if (gated && cc == 0 && a.k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
+            if (gated && cc == 0 && k_init) w = w && wait_bar(bar(B_GGO), 0u, limit, s_abort);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             if (lane == 0) TRACE(cc, 21);
             if (gated) {
@@ -584,7 +609,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     gam[u] = 1.f;
                     if (tok < T) {
                         // the same-step pair writes from the first token on
-                        const bool pair = !shifted || (tok > 0) || (a.k_init != nullptr);
+                        const bool pair = !shifted || (t_base + tok > 0) || (k_init != nullptr);
                         eta[u] = pair ? __fdividef(nb[u], n[u] + nl[u] + a.eps) : 0.f;
                         gam[u] = 1.f - eta[u] * nl[u];
                     }
@@ -673,8 +698,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     const int t = kidx >> 2, qq = kidx & 3;
                     const uint32_t roff = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
                     for (int which = 0; which < (gated ? 1 : 2); ++which) {
-                        const int64_t src = (int64_t)cc * C + t - ((which == 0 && shifted) ? 1 : 0);
-                        if (src < 0 || src >= T) continue;
+                        const int64_t src = t_base + (int64_t)cc * C + t - ((which == 0 && shifted) ? 1 : 0);
+                        if (src < 0 || src >= T_all) continue;
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int cidx = 4 * qq + m;   // 0..15: block (cidx >> 3), chunk (cidx & 7)
@@ -690,11 +715,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     }
                     wrote = true;
                 }
-                if (gated && cc == 0 && a.k_init) {
+                if (gated && cc == 0 && k_init) {
                     if (kidx < 16) {
                         const int hb = kidx >> 3, c16 = kidx & 7;
                         const uint4 u = *reinterpret_cast<const uint4 *>(
-                            static_cast<const __nv_bfloat16 *>(a.k_init) + chain * D + hb * 64 + c16 * 8);
+                            static_cast<const __nv_bfloat16 *>(k_init) + chain * D + hb * 64 + c16 * 8);
                         float f[8];
                         unpack8(u, f);
 #pragma unroll
@@ -1014,6 +1039,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
     } else if (warp >= SG_W0 && warp < KG2_W0) {
         // ================================================================ state group
         const int srow = tid - SG_W0 * 32;         // == TMEM lane of this thread
+        // the final state: S_T, or (two segments) this role's slot of the workspace
+        float *const sdst = segs ? a.s_aux + (int64_t)role * a.n_chains * D * D : a.S_T;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         auto gwait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool ok = wait_bar(bb, parity, limit, s_abort);
@@ -1043,7 +1070,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                 float v[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    v[e] = a.S0 ? a.S0[(chain * D + 32 * q + e) * D + srow] : 0.f;
+                    v[e] = role == 2 ? (32 * q + e == srow ? 1.f : 0.f)
+                         : (role == 0 && a.S0) ? a.S0[(chain * D + 32 * q + e) * D + srow] : 0.f;
                 put_sb(32 * q, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] *= gC0;
@@ -1122,7 +1150,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     float v[32];
                     tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a.S_T[(chain * D + 32 * q + e) * D + srow] = v[e];
+                    for (int e = 0; e < 32; ++e) sdst[(chain * D + 32 * q + e) * D + srow] = v[e];
                 }
             } else if constexpr (SPLIT_CARRY) {
                 // (few chains: the state path's latency sets the period)
@@ -1187,7 +1215,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
             //      frees its lanes of O1 and O2 for the next chunk's products
             {
                 const float *gv = reinterpret_cast<const float *>(sm + OFF_SGV);
-                __nv_bfloat16 *ot = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T + tok0) * D + srow;
+                __nv_bfloat16 *ot = role == 2
+                    ? reinterpret_cast<__nv_bfloat16 *>(a.o_aux) + (chain * T + tok0) * D + srow
+                    : reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + t_base + tok0) * D + srow;
                 const int tlim = T - tok0 < (int64_t)C ? (int)(T - tok0) : C;
 #pragma unroll 1
                 for (int h = 0; h < 4; ++h) {   // (a rolled loop: short code beside the other roles')
@@ -1221,6 +1251,143 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// ---------------------------------------------------------------- two segments
+// Second kernel of the two-segment form.  The state map over the second segment is
+// affine in its initial state: S_t = Phi_t S_mid + S_t^0, so the true outputs are
+// o_t = o_t^0 + S_mid^T (Phi_t^T q_t) (the zero-start run wrote o_t^0 in place, the
+// transition run Phi_t^T q_t to the workspace) and S_T = Phi_T S_mid + S_T^0.
+// Output CTAs: FX_TILES tiles of 64 tokens of one chain; S_mid^T is staged once as
+// bf16 and each tile's product runs on warp-level bf16 MMAs (fp32 accumulation),
+// then o is read, added to and written in whole rows.  The last 4 CTAs per chain
+// form S_T (32 rows each) in fp32.
+constexpr int FX_THREADS = 256, FX_ROWS = 64, FX_TILES = 4;
+constexpr int FX_LDB = 136;   // bf16 row stride of S_mid^T and the tile (128 + 8)
+constexpr int FX_LDF = 132;   // fp32 row stride of the product tile
+constexpr uint32_t FX_SMEM = (uint32_t)(D * FX_LDB * 2 + FX_ROWS * FX_LDB * 2 + FX_ROWS * FX_LDF * 4);
+
+__global__ void __launch_bounds__(FX_THREADS)
+segment_fixup_kernel(const PrefillArgs a, int64_t n_out_ctas) {
+    extern __shared__ __align__(16) uint8_t fsm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n = a.n_chains, T_all = a.T, T1 = T_all - a.seg_t0;
+    const float *Smid = a.s_aux, *Sz = a.s_aux + n * D * D, *Phi = a.s_aux + 2 * n * D * D;
+    if ((int64_t)blockIdx.x >= n_out_ctas) {
+        // S_T rows 32r .. 32r+31 of one chain; thread: row i, columns j0 .. j0+15
+        const int64_t bx = (int64_t)blockIdx.x - n_out_ctas;
+        const int64_t chain = bx >> 2;
+        const int i = 32 * (int)(bx & 3) + (tid >> 3), j0 = 16 * (tid & 7);
+        const float *ph = Phi + (chain * D + i) * D;
+        const float *sm0 = Smid + chain * D * D + j0;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = Sz[(chain * D + i) * D + j0 + e];
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float p = ph[k];
+            const float4 *s4 = reinterpret_cast<const float4 *>(sm0 + (int64_t)k * D);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = s4[q];
+                acc[4 * q] = fmaf(p, v.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(p, v.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(p, v.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(p, v.w, acc[4 * q + 3]);
+            }
+        }
+        float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + i) * D + j0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        return;
+    }
+    const int64_t per_chain = (T1 + FX_ROWS * FX_TILES - 1) / (FX_ROWS * FX_TILES);
+    const int64_t chain = (int64_t)blockIdx.x / per_chain;
+    const int64_t tb = ((int64_t)blockIdx.x % per_chain) * FX_ROWS * FX_TILES;   // within the segment
+    __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(fsm);   // [j][i] = S_mid[i][j]
+    __nv_bfloat16 *sO = sS + D * FX_LDB;                           // [t][i]: Phi_t^T q_t
+    float *sA = reinterpret_cast<float *>(sO + FX_ROWS * FX_LDB);  // [t][j]: the product
+    for (int idx = tid; idx < D * D; idx += FX_THREADS)
+        sS[(idx & 127) * FX_LDB + (idx >> 7)] = __float2bfloat16_rn(Smid[chain * D * D + idx]);
+    const int mt = warp & 3, nh = warp >> 2, g = lane >> 2, t4 = lane & 3;
+    for (int tile = 0; tile < FX_TILES; ++tile) {
+        const int64_t t0 = tb + (int64_t)tile * FX_ROWS;
+        if (t0 >= T1) break;
+        const __nv_bfloat16 *oa = reinterpret_cast<const __nv_bfloat16 *>(a.o_aux) + (chain * T1 + t0) * D;
+        __syncthreads();   // the previous tile's reads of sO and sA are done
+        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {   // 16-byte pieces
+            const int r = idx >> 4, c8 = idx & 15;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t0 + r < T1) v = *reinterpret_cast<const uint4 *>(oa + (int64_t)r * D + 8 * c8);
+            *reinterpret_cast<uint4 *>(sO + r * FX_LDB + 8 * c8) = v;
+        }
+        __syncthreads();
+        // warp: rows 16 mt .. +15, columns 64 nh .. +63, k = i in 8 steps of 16
+        float acc[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t fa[4];
+            const int ar = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), ac = 16 * ks + 8 * (lane >> 4);
+            ldmatrix_x4(smem_u32(sO + ar * FX_LDB + ac), fa);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const __nv_bfloat16 *bp = sS + (64 * nh + 8 * nt + g) * FX_LDB + 16 * ks + 2 * t4;
+                mma_bf16_16x8x16(acc[nt], fa[0], fa[1], fa[2], fa[3], *reinterpret_cast<const uint32_t *>(bp),
+                                 *reinterpret_cast<const uint32_t *>(bp + 8));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int j = 64 * nh + 8 * nt + 2 * t4, r = 16 * mt + g;
+            *reinterpret_cast<float2 *>(sA + r * FX_LDF + j) = make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2 *>(sA + (r + 8) * FX_LDF + j) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+        __syncthreads();
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + a.seg_t0 + t0) * D;
+        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {   // whole rows, 8 values a thread
+            const int r = idx >> 4, c8 = idx & 15;
+            if (t0 + r >= T1) continue;
+            uint4 *op = reinterpret_cast<uint4 *>(o + (int64_t)r * D + 8 * c8);
+            const uint4 u = *op;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const float *pa = sA + r * FX_LDF + 8 * c8;
+            uint32_t outw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16(w[e]);
+                outw[e] = pack_bf16(f.x + pa[2 * e], f.y + pa[2 * e + 1]);
+            }
+            *op = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        }
+    }
+}
+
+// Private stream-ordered pool for the two-segment workspace, one per device; it
+// keeps its memory between calls.
+cudaMemPool_t segment_pool(int dev) {
+    static std::mutex m;
+    static cudaMemPool_t pools[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(m);
+    if (!pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[dev] = p;
+    }
+    return pools[dev];
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1284,20 +1451,60 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    // With chains on at most about 55 % of the SMs (a chain per SM), the state path's
+    // Few long chains: each runs as two segments at once (three CTAs per chain),
+    // when at most a third of the SMs hold a chain and T >= 4096, or as the test
+    // hook asks; the split is at a chunk boundary.
+    PrefillArgs b = a;
+    const int64_t nchk = (a.T + C - 1) / C;
+    void *ws = nullptr;
+    if (a.seg_pref >= 0 && nchk >= 2 &&
+        (a.seg_pref > 0 || (3 * a.n_chains <= (int64_t)sms && a.T >= 4096))) {
+        const int64_t t0 = (int64_t)C * (nchk / 2);
+        const size_t n_o = (size_t)a.n_chains * (size_t)(a.T - t0) * D * 2;   // a multiple of 256
+        const size_t n_s = (size_t)3 * (size_t)a.n_chains * D * D * 4;
+        cudaMemPool_t pool = segment_pool(dev);
+        if (pool && cudaMallocFromPoolAsync(&ws, n_o + n_s, pool, s) == cudaSuccess) {
+            b.seg_t0 = t0;
+            b.o_aux = ws;
+            b.s_aux = reinterpret_cast<float *>(static_cast<char *>(ws) + n_o);
+        } else {
+            cudaGetLastError();   // no workspace: the call runs unsplit
+            ws = nullptr;
+        }
+    }
+    const int64_t ctas = b.seg_t0 > 0 ? 3 * a.n_chains : a.n_chains;
+    // With CTAs on at most about 55 % of the SMs (one per SM), the state path's
     // serial chain sets each chain's period, and the decay scaling of the state
     // moves off it (measured crossover between 80 and 96 chains on 152 SMs).
-    const bool split = 20 * a.n_chains <= 11 * (int64_t)sms;
-    auto kern = a.mode == FW_LINATTN ? chunked_kernel<false, false, false>
-              : a.mode == FW_FALCON1 ? (split ? chunked_kernel<true, true, true>
-                                              : chunked_kernel<true, true, false>)
-                                     : (split ? chunked_kernel<true, false, true>
-                                              : chunked_kernel<true, false, false>);
+    const bool split = 20 * ctas <= 11 * (int64_t)sms;
+    const bool segs = b.seg_t0 > 0;
+    auto kern = a.mode == FW_LINATTN
+                    ? (segs ? chunked_kernel<false, false, false, true> : chunked_kernel<false, false, false, false>)
+              : a.mode == FW_FALCON1
+                    ? (split ? (segs ? chunked_kernel<true, true, true, true> : chunked_kernel<true, true, true, false>)
+                             : (segs ? chunked_kernel<true, true, false, true> : chunked_kernel<true, true, false, false>))
+                    : (split ? (segs ? chunked_kernel<true, false, true, true> : chunked_kernel<true, false, true, false>)
+                             : (segs ? chunked_kernel<true, false, false, true> : chunked_kernel<true, false, false, false>));
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)SMEM_ALLOC)) != cudaSuccess)
-        return e;
-    kern<<<(unsigned)a.n_chains, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, a);
-    return cudaGetLastError();
+                                  (int)SMEM_ALLOC)) == cudaSuccess) {
+        kern<<<(unsigned)ctas, NTHREADS, SMEM_ALLOC, s>>>(tq, tk, tv, b);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess && b.seg_t0 > 0) {
+        const int64_t per_chain = (a.T - b.seg_t0 + FX_ROWS * FX_TILES - 1) / (FX_ROWS * FX_TILES);
+        const int64_t n_out = a.n_chains * per_chain;
+        e = cudaFuncSetAttribute(segment_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)FX_SMEM);
+        if (e == cudaSuccess) {
+            segment_fixup_kernel<<<(unsigned)(n_out + 4 * a.n_chains), FX_THREADS, FX_SMEM, s>>>(b, n_out);
+            e = cudaGetLastError();
+        }
+    }
+    if (ws) {
+        const cudaError_t ef = cudaFreeAsync(ws, s);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e;
 }
 
 }  // namespace fw

@@ -30,6 +30,11 @@ struct PrefillArgs {
     int *err;          // device error word
     long long wait_ns; // limit of every bounded device wait, nanoseconds
     int force_timeout; // testing hook: wait on a barrier nothing arrives on
+    int seg_pref;      // two-segment split of few long chains: 0 auto, 1 always, -1 never
+    // Set by the chunked launch when it splits each chain at token seg_t0 (> 0):
+    int64_t seg_t0;
+    void *o_aux;       // outputs of the transition run, bf16 [n_chains][T - seg_t0][d]
+    float *s_aux;      // S at the split, S_T from a zero start, transition: fp32 [3][n_chains][d][d]
 };
 
 struct StepArgs {

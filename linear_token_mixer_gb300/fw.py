@@ -50,7 +50,7 @@ class fw_window(ctypes.Structure):
 EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_step_ex", "fw_window_prefill",
            "fw_window_step", "fw_check",
            "fw_status_string", "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us",
-           "fw_debug_force_timeout")
+           "fw_debug_force_timeout", "fw_debug_segment_split")
 
 _lib = None
 
@@ -83,6 +83,8 @@ def lib():
         L.fw_set_wait_limit_us.restype = None
         L.fw_debug_force_timeout.argtypes = [I]
         L.fw_debug_force_timeout.restype = None
+        L.fw_debug_segment_split.argtypes = [I]
+        L.fw_debug_segment_split.restype = None
         for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_step_ex, L.fw_window_prefill,
                   L.fw_window_step, L.fw_check, L.fw_version, L.fw_last_cuda_error):
             f.restype = I
