@@ -1151,6 +1151,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
                     tmem_ld32(tmem + lane_base + COL_S + 32 * q, v);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) sdst[(chain * D + 32 * q + e) * D + srow] = v[e];
+                    if (segs && role == 0) {   // and row j of S_mid^T in bf16, for the fix-up's products
+                        uint4 *bt = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(
+                                        a.s_aux + 3 * a.n_chains * D * D) + (chain * D + srow) * D + 32 * q);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            bt[u] = make_uint4(pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
+                                               pack_bf16(v[8 * u + 4], v[8 * u + 5]), pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+                    }
                 }
             } else if constexpr (SPLIT_CARRY) {
                 // (few chains: the state path's latency sets the period)
@@ -1258,71 +1266,101 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 // affine in its initial state: S_t = Phi_t S_mid + S_t^0, so the true outputs are
 // o_t = o_t^0 + S_mid^T (Phi_t^T q_t) (the zero-start run wrote o_t^0 in place, the
 // transition run Phi_t^T q_t to the workspace) and S_T = Phi_T S_mid + S_T^0.
-// Output CTAs: FX_TILES tiles of 64 tokens of one chain; S_mid^T is staged once as
-// bf16 and each tile's product runs on warp-level bf16 MMAs (fp32 accumulation),
-// then o is read, added to and written in whole rows.  The last 4 CTAs per chain
-// form S_T (32 rows each) in fp32.
-constexpr int FX_THREADS = 256, FX_ROWS = 64, FX_TILES = 4;
-constexpr int FX_LDB = 136;   // bf16 row stride of S_mid^T and the tile (128 + 8)
+// m CTAs per chain, two per SM: CTA k of a chain forms rows k, k + m, ... of S_T
+// in fp32, then stages S_mid^T (bf16, written by the first segment's CTA) once and
+// takes the chain's 64-token tiles k, k + m, ...: the tile of Phi_t^T q_t arrives
+// by cp.async into one of two buffers while the previous tile is worked on, the
+// product runs on warp-level bf16 MMAs (fp32 accumulation), and o is read ahead
+// of the products, added to and written in whole rows.
+constexpr int FX_THREADS = 256, FX_ROWS = 64;
+constexpr int FX_LDB = 136;   // bf16 row stride of S_mid^T and the tiles (128 + 8)
 constexpr int FX_LDF = 132;   // fp32 row stride of the product tile
-constexpr uint32_t FX_SMEM = (uint32_t)(D * FX_LDB * 2 + FX_ROWS * FX_LDB * 2 + FX_ROWS * FX_LDF * 4);
+constexpr uint32_t FX_SMEM = (uint32_t)(D * FX_LDB * 2 + 2 * FX_ROWS * FX_LDB * 2 + FX_ROWS * FX_LDF * 4);
 
-__global__ void __launch_bounds__(FX_THREADS)
-segment_fixup_kernel(const PrefillArgs a, int64_t n_out_ctas) {
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(FX_THREADS, 2)
+segment_fixup_kernel(const PrefillArgs a, int m) {
     extern __shared__ __align__(16) uint8_t fsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = a.n_chains, T_all = a.T, T1 = T_all - a.seg_t0;
     const float *Smid = a.s_aux, *Sz = a.s_aux + n * D * D, *Phi = a.s_aux + 2 * n * D * D;
-    if ((int64_t)blockIdx.x >= n_out_ctas) {
-        // S_T rows 32r .. 32r+31 of one chain; thread: row i, columns j0 .. j0+15
-        const int64_t bx = (int64_t)blockIdx.x - n_out_ctas;
-        const int64_t chain = bx >> 2;
-        const int i = 32 * (int)(bx & 3) + (tid >> 3), j0 = 16 * (tid & 7);
-        const float *ph = Phi + (chain * D + i) * D;
-        const float *sm0 = Smid + chain * D * D + j0;
-        float acc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = Sz[(chain * D + i) * D + j0 + e];
-#pragma unroll 4
-        for (int k = 0; k < D; ++k) {
-            const float p = ph[k];
-            const float4 *s4 = reinterpret_cast<const float4 *>(sm0 + (int64_t)k * D);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = s4[q];
-                acc[4 * q] = fmaf(p, v.x, acc[4 * q]);
-                acc[4 * q + 1] = fmaf(p, v.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(p, v.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(p, v.w, acc[4 * q + 3]);
-            }
-        }
-        float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + i) * D + j0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-        return;
-    }
-    const int64_t per_chain = (T1 + FX_ROWS * FX_TILES - 1) / (FX_ROWS * FX_TILES);
-    const int64_t chain = (int64_t)blockIdx.x / per_chain;
-    const int64_t tb = ((int64_t)blockIdx.x % per_chain) * FX_ROWS * FX_TILES;   // within the segment
+    const __nv_bfloat16 *SmidT = reinterpret_cast<const __nv_bfloat16 *>(a.s_aux + 3 * n * D * D);
+    const int64_t chain = (int64_t)blockIdx.x / m;
+    const int k = (int)((int64_t)blockIdx.x % m);
     __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(fsm);   // [j][i] = S_mid[i][j]
-    __nv_bfloat16 *sO = sS + D * FX_LDB;                           // [t][i]: Phi_t^T q_t
-    float *sA = reinterpret_cast<float *>(sO + FX_ROWS * FX_LDB);  // [t][j]: the product
-    for (int idx = tid; idx < D * D; idx += FX_THREADS)
-        sS[(idx & 127) * FX_LDB + (idx >> 7)] = __float2bfloat16_rn(Smid[chain * D * D + idx]);
-    const int mt = warp & 3, nh = warp >> 2, g = lane >> 2, t4 = lane & 3;
-    for (int tile = 0; tile < FX_TILES; ++tile) {
-        const int64_t t0 = tb + (int64_t)tile * FX_ROWS;
-        if (t0 >= T1) break;
+    __nv_bfloat16 *sO = sS + D * FX_LDB;                           // two tiles [t][i]: Phi_t^T q_t
+    float *sA = reinterpret_cast<float *>(sO + 2 * FX_ROWS * FX_LDB);   // [t][j]: the product
+    const uint32_t sS_u = smem_u32(sS), sO_u = smem_u32(sO);
+
+    for (int idx = tid; idx < D * 16; idx += FX_THREADS)   // 16-byte pieces of the rows j
+        cp_async16(sS_u + (uint32_t)(((idx >> 4) * FX_LDB + 8 * (idx & 15)) * 2),
+                   SmidT + (chain * D + (idx >> 4)) * D + 8 * (idx & 15));
+    cp_async_commit();
+    const int64_t ntile = (T1 + FX_ROWS - 1) / FX_ROWS;
+    auto load_tile = [&](int64_t tile, int buf) {   // rows past the segment's end are not read
+        const int64_t t0 = tile * FX_ROWS;
         const __nv_bfloat16 *oa = reinterpret_cast<const __nv_bfloat16 *>(a.o_aux) + (chain * T1 + t0) * D;
-        __syncthreads();   // the previous tile's reads of sO and sA are done
-        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {   // 16-byte pieces
+        const uint32_t base = sO_u + (uint32_t)(buf * FX_ROWS * FX_LDB * 2);
+        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {
             const int r = idx >> 4, c8 = idx & 15;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t0 + r < T1) v = *reinterpret_cast<const uint4 *>(oa + (int64_t)r * D + 8 * c8);
-            *reinterpret_cast<uint4 *>(sO + r * FX_LDB + 8 * c8) = v;
+            if (t0 + r < T1) cp_async16(base + (uint32_t)((r * FX_LDB + 8 * c8) * 2), oa + (int64_t)r * D + 8 * c8);
         }
-        __syncthreads();
+        cp_async_commit();
+    };
+    if (k < ntile) load_tile(k, 0);
+
+    // S_T = Phi_T S_mid + S_T^0, rows i = k, k + m, ...: thread (row slot, 8 columns)
+    {
+        const int j0 = 8 * (tid & 15);
+        for (int i = k + m * (tid >> 4); i < D; i += m * (FX_THREADS >> 4)) {
+            const float *ph = Phi + (chain * D + i) * D;
+            const float *sm0 = Smid + chain * D * D + j0;
+            const float4 z0 = *reinterpret_cast<const float4 *>(Sz + (chain * D + i) * D + j0);
+            const float4 z1 = *reinterpret_cast<const float4 *>(Sz + (chain * D + i) * D + j0 + 4);
+            float acc[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll 4
+            for (int kk = 0; kk < D; ++kk) {
+                const float p = ph[kk];
+                const float4 v0 = *reinterpret_cast<const float4 *>(sm0 + (int64_t)kk * D);
+                const float4 v1 = *reinterpret_cast<const float4 *>(sm0 + (int64_t)kk * D + 4);
+                acc[0] = fmaf(p, v0.x, acc[0]); acc[1] = fmaf(p, v0.y, acc[1]);
+                acc[2] = fmaf(p, v0.z, acc[2]); acc[3] = fmaf(p, v0.w, acc[3]);
+                acc[4] = fmaf(p, v1.x, acc[4]); acc[5] = fmaf(p, v1.y, acc[5]);
+                acc[6] = fmaf(p, v1.z, acc[6]); acc[7] = fmaf(p, v1.w, acc[7]);
+            }
+            float4 *dst = reinterpret_cast<float4 *>(a.S_T + (chain * D + i) * D + j0);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+
+    const int mt = warp & 3, nh = warp >> 2, g = lane >> 2, t4 = lane & 3;
+    int buf = 0;
+    for (int64_t tile = k; tile < ntile; tile += m, buf ^= 1) {
+        if (tile + m < ntile) {
+            load_tile(tile + m, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();   // this tile (and S_mid^T) landed for every thread
+        const int64_t t0 = tile * FX_ROWS;
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + a.seg_t0 + t0) * D;
+        uint4 ov[4];   // o^0 of this tile, read ahead of the products
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = tid + u * FX_THREADS, r = idx >> 4, c8 = idx & 15;
+            ov[u] = t0 + r < T1 ? *reinterpret_cast<const uint4 *>(o + (int64_t)r * D + 8 * c8)
+                                : make_uint4(0u, 0u, 0u, 0u);
+        }
         // warp: rows 16 mt .. +15, columns 64 nh .. +63, k = i in 8 steps of 16
+        const __nv_bfloat16 *tb = sO + buf * FX_ROWS * FX_LDB;
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -1332,7 +1370,7 @@ segment_fixup_kernel(const PrefillArgs a, int64_t n_out_ctas) {
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t fa[4];
             const int ar = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), ac = 16 * ks + 8 * (lane >> 4);
-            ldmatrix_x4(smem_u32(sO + ar * FX_LDB + ac), fa);
+            ldmatrix_x4(smem_u32(tb + ar * FX_LDB + ac), fa);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const __nv_bfloat16 *bp = sS + (64 * nh + 8 * nt + g) * FX_LDB + 16 * ks + 2 * t4;
@@ -1346,14 +1384,12 @@ segment_fixup_kernel(const PrefillArgs a, int64_t n_out_ctas) {
             *reinterpret_cast<float2 *>(sA + r * FX_LDF + j) = make_float2(acc[nt][0], acc[nt][1]);
             *reinterpret_cast<float2 *>(sA + (r + 8) * FX_LDF + j) = make_float2(acc[nt][2], acc[nt][3]);
         }
-        __syncthreads();
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + a.seg_t0 + t0) * D;
-        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {   // whole rows, 8 values a thread
-            const int r = idx >> 4, c8 = idx & 15;
+        __syncthreads();   // the product is in sA; this tile's buffer is free for the prefetch after next
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {   // whole rows, 8 values a thread
+            const int idx = tid + u * FX_THREADS, r = idx >> 4, c8 = idx & 15;
             if (t0 + r >= T1) continue;
-            uint4 *op = reinterpret_cast<uint4 *>(o + (int64_t)r * D + 8 * c8);
-            const uint4 u = *op;
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const uint32_t w[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
             const float *pa = sA + r * FX_LDF + 8 * c8;
             uint32_t outw[4];
 #pragma unroll
@@ -1361,9 +1397,10 @@ segment_fixup_kernel(const PrefillArgs a, int64_t n_out_ctas) {
                 const float2 f = unpack_bf16(w[e]);
                 outw[e] = pack_bf16(f.x + pa[2 * e], f.y + pa[2 * e + 1]);
             }
-            *op = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            *reinterpret_cast<uint4 *>(o + (int64_t)r * D + 8 * c8) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         }
     }
+    cp_async_wait<0>();   // no copy in flight at exit
 }
 
 // Private stream-ordered pool for the two-segment workspace, one per device; it
@@ -1461,7 +1498,8 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
         (a.seg_pref > 0 || (3 * a.n_chains <= (int64_t)sms && a.T >= 4096))) {
         const int64_t t0 = (int64_t)C * (nchk / 2);
         const size_t n_o = (size_t)a.n_chains * (size_t)(a.T - t0) * D * 2;   // a multiple of 256
-        const size_t n_s = (size_t)3 * (size_t)a.n_chains * D * D * 4;
+        // S_mid, S_T from zero and Phi_T in fp32, then S_mid^T in bf16
+        const size_t n_s = (size_t)3 * (size_t)a.n_chains * D * D * 4 + (size_t)a.n_chains * D * D * 2;
         cudaMemPool_t pool = segment_pool(dev);
         if (pool && cudaMallocFromPoolAsync(&ws, n_o + n_s, pool, s) == cudaSuccess) {
             b.seg_t0 = t0;
@@ -1491,12 +1529,15 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
         e = cudaGetLastError();
     }
     if (e == cudaSuccess && b.seg_t0 > 0) {
-        const int64_t per_chain = (a.T - b.seg_t0 + FX_ROWS * FX_TILES - 1) / (FX_ROWS * FX_TILES);
-        const int64_t n_out = a.n_chains * per_chain;
+        // two CTAs per SM, an equal number per chain
+        const int64_t ntile = (a.T - b.seg_t0 + FX_ROWS - 1) / FX_ROWS;
+        int64_t m = 2 * (int64_t)sms / a.n_chains;
+        if (m > ntile) m = ntile;
+        if (m < 1) m = 1;
         e = cudaFuncSetAttribute(segment_fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)FX_SMEM);
         if (e == cudaSuccess) {
-            segment_fixup_kernel<<<(unsigned)(n_out + 4 * a.n_chains), FX_THREADS, FX_SMEM, s>>>(b, n_out);
+            segment_fixup_kernel<<<(unsigned)(a.n_chains * m), FX_THREADS, FX_SMEM, s>>>(b, (int)m);
             e = cudaGetLastError();
         }
     }
