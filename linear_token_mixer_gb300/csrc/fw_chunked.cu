@@ -1268,14 +1268,14 @@ chunked_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ 
 // transition run Phi_t^T q_t to the workspace) and S_T = Phi_T S_mid + S_T^0.
 // m CTAs per chain, two per SM: CTA k of a chain forms rows k, k + m, ... of S_T
 // in fp32, then stages S_mid^T (bf16, written by the first segment's CTA) once and
-// takes the chain's 64-token tiles k, k + m, ...: the tile of Phi_t^T q_t arrives
-// by cp.async into one of two buffers while the previous tile is worked on, the
-// product runs on warp-level bf16 MMAs (fp32 accumulation), and o is read ahead
-// of the products, added to and written in whole rows.
+// takes the chain's 64-token tiles k, k + m, ...: the next tile's Phi_t^T q_t and o
+// rows arrive by cp.async into the other of two buffers while a tile is worked on;
+// the product runs on warp-level bf16 MMAs (fp32 accumulation) and is added into
+// the staged o rows in shared memory, which then go out in whole rows.
 constexpr int FX_THREADS = 256, FX_ROWS = 64;
 constexpr int FX_LDB = 136;   // bf16 row stride of S_mid^T and the tiles (128 + 8)
-constexpr int FX_LDF = 132;   // fp32 row stride of the product tile
-constexpr uint32_t FX_SMEM = (uint32_t)(D * FX_LDB * 2 + 2 * FX_ROWS * FX_LDB * 2 + FX_ROWS * FX_LDF * 4);
+constexpr uint32_t FX_TILE = (uint32_t)(FX_ROWS * FX_LDB * 2);
+constexpr uint32_t FX_SMEM = (uint32_t)(D * FX_LDB * 2) + 4 * FX_TILE;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -1293,10 +1293,12 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
     const __nv_bfloat16 *SmidT = reinterpret_cast<const __nv_bfloat16 *>(a.s_aux + 3 * n * D * D);
     const int64_t chain = (int64_t)blockIdx.x / m;
     const int k = (int)((int64_t)blockIdx.x % m);
-    __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(fsm);   // [j][i] = S_mid[i][j]
-    __nv_bfloat16 *sO = sS + D * FX_LDB;                           // two tiles [t][i]: Phi_t^T q_t
-    float *sA = reinterpret_cast<float *>(sO + 2 * FX_ROWS * FX_LDB);   // [t][j]: the product
-    const uint32_t sS_u = smem_u32(sS), sO_u = smem_u32(sO);
+    // [j][i] = S_mid[i][j]; then two buffers of (Phi_t^T q_t [t][i], o [t][j])
+    __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(fsm);
+    const uint32_t sS_u = smem_u32(sS), sT_u = sS_u + (uint32_t)(D * FX_LDB * 2);
+    auto q_tile = [&](int buf) { return sT_u + (uint32_t)(2 * buf) * FX_TILE; };
+    auto o_tile = [&](int buf) { return sT_u + (uint32_t)(2 * buf + 1) * FX_TILE; };
+    __nv_bfloat16 *const o_seg = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + a.seg_t0) * D;
 
     for (int idx = tid; idx < D * 16; idx += FX_THREADS)   // 16-byte pieces of the rows j
         cp_async16(sS_u + (uint32_t)(((idx >> 4) * FX_LDB + 8 * (idx & 15)) * 2),
@@ -1306,17 +1308,21 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
     auto load_tile = [&](int64_t tile, int buf) {   // rows past the segment's end are not read
         const int64_t t0 = tile * FX_ROWS;
         const __nv_bfloat16 *oa = reinterpret_cast<const __nv_bfloat16 *>(a.o_aux) + (chain * T1 + t0) * D;
-        const uint32_t base = sO_u + (uint32_t)(buf * FX_ROWS * FX_LDB * 2);
+        const __nv_bfloat16 *oo = o_seg + t0 * D;
         for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {
             const int r = idx >> 4, c8 = idx & 15;
-            if (t0 + r < T1) cp_async16(base + (uint32_t)((r * FX_LDB + 8 * c8) * 2), oa + (int64_t)r * D + 8 * c8);
+            if (t0 + r >= T1) continue;
+            const uint32_t off = (uint32_t)((r * FX_LDB + 8 * c8) * 2);
+            cp_async16(q_tile(buf) + off, oa + (int64_t)r * D + 8 * c8);
+            cp_async16(o_tile(buf) + off, oo + (int64_t)r * D + 8 * c8);
         }
         cp_async_commit();
     };
     if (k < ntile) load_tile(k, 0);
 
-    // S_T = Phi_T S_mid + S_T^0, rows i = k, k + m, ...: thread (row slot, 8 columns)
-    {
+    // S_T = Phi_T S_mid + S_T^0, rows i = k, k + m, ...: thread (row slot, 8 columns);
+    // latency-bound, so half the CTAs form it before their tiles and half after
+    auto state_rows = [&]() {
         const int j0 = 8 * (tid & 15);
         for (int i = k + m * (tid >> 4); i < D; i += m * (FX_THREADS >> 4)) {
             const float *ph = Phi + (chain * D + i) * D;
@@ -1324,7 +1330,7 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
             const float4 z0 = *reinterpret_cast<const float4 *>(Sz + (chain * D + i) * D + j0);
             const float4 z1 = *reinterpret_cast<const float4 *>(Sz + (chain * D + i) * D + j0 + 4);
             float acc[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-#pragma unroll 4
+#pragma unroll 8
             for (int kk = 0; kk < D; ++kk) {
                 const float p = ph[kk];
                 const float4 v0 = *reinterpret_cast<const float4 *>(sm0 + (int64_t)kk * D);
@@ -1338,7 +1344,8 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
             dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
-    }
+    };
+    if (!(k & 1)) state_rows();
 
     const int mt = warp & 3, nh = warp >> 2, g = lane >> 2, t4 = lane & 3;
     int buf = 0;
@@ -1350,17 +1357,8 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
             cp_async_wait<0>();
         }
         __syncthreads();   // this tile (and S_mid^T) landed for every thread
-        const int64_t t0 = tile * FX_ROWS;
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.o) + (chain * T_all + a.seg_t0 + t0) * D;
-        uint4 ov[4];   // o^0 of this tile, read ahead of the products
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int idx = tid + u * FX_THREADS, r = idx >> 4, c8 = idx & 15;
-            ov[u] = t0 + r < T1 ? *reinterpret_cast<const uint4 *>(o + (int64_t)r * D + 8 * c8)
-                                : make_uint4(0u, 0u, 0u, 0u);
-        }
         // warp: rows 16 mt .. +15, columns 64 nh .. +63, k = i in 8 steps of 16
-        const __nv_bfloat16 *tb = sO + buf * FX_ROWS * FX_LDB;
+        const __nv_bfloat16 *tq = sS + (D + 2 * buf * FX_ROWS) * FX_LDB;   // the q tile of buf
         float acc[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -1370,7 +1368,7 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t fa[4];
             const int ar = 16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1), ac = 16 * ks + 8 * (lane >> 4);
-            ldmatrix_x4(smem_u32(tb + ar * FX_LDB + ac), fa);
+            ldmatrix_x4(smem_u32(tq + ar * FX_LDB + ac), fa);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const __nv_bfloat16 *bp = sS + (64 * nh + 8 * nt + g) * FX_LDB + 16 * ks + 2 * t4;
@@ -1378,28 +1376,29 @@ segment_fixup_kernel(const PrefillArgs a, int m) {
                                  *reinterpret_cast<const uint32_t *>(bp + 8));
             }
         }
+        // o_t^0 + the product, in place in the staged o rows (each element one thread's)
+        __nv_bfloat16 *to = sS + (D + (2 * buf + 1) * FX_ROWS) * FX_LDB;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int j = 64 * nh + 8 * nt + 2 * t4, r = 16 * mt + g;
-            *reinterpret_cast<float2 *>(sA + r * FX_LDF + j) = make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2 *>(sA + (r + 8) * FX_LDF + j) = make_float2(acc[nt][2], acc[nt][3]);
-        }
-        __syncthreads();   // the product is in sA; this tile's buffer is free for the prefetch after next
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {   // whole rows, 8 values a thread
-            const int idx = tid + u * FX_THREADS, r = idx >> 4, c8 = idx & 15;
-            if (t0 + r >= T1) continue;
-            const uint32_t w[4] = {ov[u].x, ov[u].y, ov[u].z, ov[u].w};
-            const float *pa = sA + r * FX_LDF + 8 * c8;
-            uint32_t outw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16(w[e]);
-                outw[e] = pack_bf16(f.x + pa[2 * e], f.y + pa[2 * e + 1]);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t *pp = reinterpret_cast<uint32_t *>(to + (r + 8 * h) * FX_LDB + j);
+                const float2 f = unpack_bf16(*pp);
+                *pp = pack_bf16(f.x + acc[nt][2 * h], f.y + acc[nt][2 * h + 1]);
             }
-            *reinterpret_cast<uint4 *>(o + (int64_t)r * D + 8 * c8) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         }
+        __syncthreads();   // the sums are in place; this buffer is free for the prefetch after next
+        const int64_t t0 = tile * FX_ROWS;
+        for (int idx = tid; idx < FX_ROWS * 16; idx += FX_THREADS) {   // whole rows, 16 bytes a thread
+            const int r = idx >> 4, c8 = idx & 15;
+            if (t0 + r >= T1) continue;
+            *reinterpret_cast<uint4 *>(o_seg + (t0 + r) * D + 8 * c8) =
+                *reinterpret_cast<const uint4 *>(to + r * FX_LDB + 8 * c8);
+        }
+        __syncthreads();   // the rows are out before the next prefetch lands in this buffer
     }
+    if (k & 1) state_rows();
     cp_async_wait<0>();   // no copy in flight at exit
 }
 
