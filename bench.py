@@ -52,6 +52,7 @@ ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 KERNEL_SOURCES = {
     "chunked prefill": ("fw_chunked.cu", "fw_sm100.cuh", "fw_internal.cuh"),
+    "chunked prefill (two segments)": ("fw_chunked.cu", "fw_sm100.cuh", "fw_internal.cuh"),
     "chunked prefill (per channel)": ("fw_chunked_chan.cu", "fw_sm100.cuh", "fw_internal.cuh"),
     "recurrent (SIMT)": ("fw_recurrent.cu", "fw_internal.cuh"),
     "window prefill (SIMT)": ("fw_window_prefill.cu", "fw_window.cuh", "fw_sm100.cuh",
@@ -99,13 +100,15 @@ def algorithmic_bytes_prefill(w):
     return ht * per_ht + state * (2 if w.s0_std > 0 else 1)
 
 
-def prefill_kernel(w, algo="auto"):
+def prefill_kernel(w, algo="auto", sms=152):
     """The kernel fw_prefill picks for a workload, as the library dispatches it:
     a step per value channel (Falcon-2 / 2A) on the per-channel chunked kernel
     where it takes the call (bf16, d = 128, phi = identity), else on the staged
     per-token kernel; the other modes on the chunked tensor-core kernel where it
     takes the call (bf16, d = 128; Falcon-1 / 1A only with phi = identity), else
-    on the per-token kernel."""
+    on the per-token kernel.  The chunked kernel runs each chain as two segments
+    at once (plus a fix-up kernel) when at most a third of the sms SMs hold a
+    chain and T >= 4096."""
     if algo == "recurrent":
         return "recurrent (SIMT)"
     tc = w.dtype == torch.bfloat16 and w.d == 128
@@ -114,7 +117,11 @@ def prefill_kernel(w, algo="auto"):
             return "chunked prefill (per channel)"
         return "window prefill (SIMT)"
     chunked = tc and (w.mode == "linattn" or w.phi == "identity")
-    return "chunked prefill" if chunked else "recurrent (SIMT)"
+    if not chunked:
+        return "recurrent (SIMT)"
+    if 3 * w.B * w.H <= sms and w.T >= 4096:
+        return "chunked prefill (two segments)"
+    return "chunked prefill"
 
 
 def matmul_flops_prefill(w, C=64):
@@ -130,7 +137,7 @@ def matmul_flops_prefill(w, C=64):
     ht = w.B * w.H * w.T
     if k == "chunked prefill (per channel)":
         return ht * (4 * C * w.d + (6 if w.mode == "falcon2" else 4) * w.d * w.d)
-    if k != "chunked prefill":
+    if k not in ("chunked prefill", "chunked prefill (two segments)"):
         return None
     if w.mode == "falcon1":
         return ht * (10 * C * w.d + 6 * w.d * w.d)
@@ -638,7 +645,7 @@ def main():
     algo_bytes = algorithmic_bytes_prefill(w)
     achieved_gbs = algo_bytes / (kern_ms / 1e3) / 1e9
     kname = prefill_kernel(w)
-    if kname in ("chunked prefill", "chunked prefill (per channel)"):
+    if kname in ("chunked prefill", "chunked prefill (two segments)", "chunked prefill (per channel)"):
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm"],
                 "traffic": stored_traffic(kname, w.name),

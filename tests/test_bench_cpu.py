@@ -142,6 +142,9 @@ def test_headline_kernel_labels_follow_the_dispatch():
     assert bench.prefill_kernel(W["falcon1_bf16"]) == "chunked prefill"
     assert bench.prefill_kernel(W["linattn_bf16"]) == "chunked prefill"
     assert bench.prefill_kernel(W["falcon1_fp32"]) == "recurrent (SIMT)"
+    # few long chains: two segments at once (32 chains, T = 32768, 152 SMs)
+    assert bench.prefill_kernel(W["falcon1_long"]) == "chunked prefill (two segments)"
+    assert bench.prefill_kernel(W["falcon1_long"], sms=64) == "chunked prefill"
     assert bench.prefill_kernel(W["falcon1_bf16"].with_shape(phi="elu1")) == "recurrent (SIMT)"
     f2 = W["falcon2_bf16"]
     assert bench.prefill_kernel(f2) == "chunked prefill (per channel)"
