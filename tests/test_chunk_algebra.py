@@ -104,3 +104,45 @@ def test_chunked_form_with_nonpositive_decay():
     o, S = chunked_falcon1(q, k, v, beta, lam, S0, 1e-6, C)
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-9 * np.abs(o_ref).max())
     np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-9 * np.abs(S_ref).max())
+
+
+# ---------------------------------------------------------------- two segments
+
+def _run_mode(mode, q, k, v, beta, lam, S0, k_init, rbw, same_pair):
+    if mode == "linattn":
+        return oracle.linattn(q, k, v, S0=S0, phi="elu1", rbw=rbw)
+    return oracle.falcon1(q, k, v, beta, lam, S0=S0, k_init=k_init, eps=1e-6,
+                          inner=(mode == "falcon1a"), rbw=rbw, same_pair=same_pair)
+
+
+@pytest.mark.parametrize("mode,rbw,same_pair", [("falcon1", False, False), ("falcon1", True, False),
+                                                ("falcon1", False, True), ("falcon1a", False, False),
+                                                ("linattn", False, False), ("linattn", True, False)])
+def test_two_segment_affine_composition(mode, rbw, same_pair):
+    """The state map of a run of tokens is affine in its initial state
+    (S_t = Phi_t S_mid + S_t^0), which the chunked prefill's two-segment form
+    uses: split the chain at t0, run the second segment from a zero state and
+    again from S = I with zero targets (its outputs are Phi_t^T q_t, its final
+    state Phi_T); then o_t = o_t^0 + S_mid^T Phi_t^T q_t and
+    S_T = Phi_T S_mid + S_T^0 reproduce the whole run (the Falcon page §3.2
+    write and §4.3's additive write, the blog's linear-attention sum)."""
+    T, dk, dv, t0 = 57, 6, 5, 23
+    q = RNG.standard_normal((T, dk))
+    k = RNG.standard_normal((T, dk))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = RNG.standard_normal((T, dv))
+    beta = RNG.uniform(0.1, 1.95, T)   # gamma <= 0 on some tokens
+    lam = RNG.uniform(0.0, 0.6, T)
+    S0 = RNG.standard_normal((dk, dv)) * 0.3
+    o_full, S_full = _run_mode(mode, q, k, v, beta, lam, S0, None, rbw, same_pair)
+    o0, S_mid = _run_mode(mode, q[:t0], k[:t0], v[:t0], beta[:t0], lam[:t0], S0, None, rbw, same_pair)
+    # the second segment's first pair is (k_{t0-1}, v_t0) when keys are shifted
+    kin = k[t0 - 1] if (mode != "linattn" and not same_pair) else None
+    sl = slice(t0, T)
+    oz, Sz = _run_mode(mode, q[sl], k[sl], v[sl], beta[sl], lam[sl], None, kin, rbw, same_pair)
+    oi, Phi = _run_mode(mode, q[sl], k[sl], np.zeros((T - t0, dk)), beta[sl], lam[sl], np.eye(dk),
+                        kin, rbw, same_pair)
+    o = np.concatenate([o0, oz + oi @ S_mid])
+    S = Phi @ S_mid + Sz
+    np.testing.assert_allclose(o, o_full, rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(S, S_full, rtol=1e-10, atol=1e-10)

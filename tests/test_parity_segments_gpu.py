@@ -109,3 +109,25 @@ def test_segments_match_unsplit_kernel():
         L.fw_debug_segment_split(1)
     assert rel_l2(to64(o1), to64(o0)) <= 1e-2
     assert rel_l2(to64(S1), to64(S0)) <= 1e-2
+
+
+def test_segments_timeout_path_reports_and_recovers():
+    """A bounded wait that runs out in the segment launch is reported through
+    fw_check (FW_ERR_TIMEOUT; the fix-up then runs on what the aborted launch
+    left, in bounds), and the next call on the same context is correct."""
+    L = fw.lib()
+    w, x = _inputs("falcon1", 300, seed=17)
+    g = {k: (t.to(DEV) if t is not None else None) for k, t in x.items()}
+    L.fw_set_wait_limit_us(2000)
+    L.fw_debug_force_timeout(1)
+    try:
+        fw.prefill(g["q"], g["k"], g["v"], g["beta"], g["lam"], g["S0"], mode=w.mode, phi=w.phi,
+                   eps=w.eps, algo="chunked")
+        with pytest.raises(fw.FwError) as ei:
+            fw.check()
+        assert ei.value.status == -7
+    finally:
+        L.fw_debug_force_timeout(0)
+        L.fw_set_wait_limit_us(0)
+    fw.check()
+    _check(w, x)
