@@ -37,6 +37,9 @@
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or keeps them.  Rows are contiguous, row-major.
+ *     Its own workspace is taken only by the chunked prefill's two-segment
+ *     form (few long chains; see fw_debug_segment_split), stream-ordered on the
+ *     call's stream from a private pool that keeps its memory between calls.
  *   - q, k, v, o:  [B][H][T][d] (prefill) or [B][H][d] (step), element type
  *     FW_F32 (float) or FW_BF16 (bfloat16), d innermost.
  *   - beta, lambda: float [B][H][T] (prefill) or [B][H] (step); beta of
