@@ -142,7 +142,8 @@ enum {
     FW_ERR_TIMEOUT = -7,     /* a bounded device wait ran out (reported by fw_check) */
     FW_ERR_UNSUPPORTED = -8, /* FW_ALGO_CHUNKED asked for a call it does not support */
     FW_ERR_ARG = -9,         /* eps negative or not finite, or o aliases an input */
-    FW_ERR_DEVICE = -10      /* the current device is not an sm_103 GPU */
+    FW_ERR_DEVICE = -10,     /* the current device is not an sm_103 GPU */
+    FW_ERR_SCRATCH = -11     /* fw_prefill_noalloc: the call needs more than FW_SCRATCH_BYTES */
 };
 
 /*
@@ -188,6 +189,38 @@ int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta
                   const float *lambda, const float *S0, const void *k_init, void *o,
                   float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
                   fw_phi phi, float eps, unsigned flags, fw_algo algo, cudaStream_t stream);
+
+/*
+ * fw_prefill_noalloc -- fw_prefill_ex for callers that want no device memory
+ * allocated on their behalf.  The pages have no counterpart: this is a
+ * deployment detail of this library, not part of the method.
+ *
+ * Same arguments, validation and kernels as fw_prefill_ex.  The only call
+ * that needs workspace is the chunked prefill's two-segment form (few long
+ * chains, see fw_debug_segment_split); here it takes that workspace from one
+ * static device buffer of FW_SCRATCH_BYTES compiled into the library
+ * (file-scope, 256-byte aligned) instead of the stream-ordered pool, and
+ * nothing is allocated or freed.  A call whose two-segment form would need
+ * more than FW_SCRATCH_BYTES (n_chains x (T - T/2) x 256 bytes plus
+ * n_chains x 224 KiB) returns FW_ERR_SCRATCH and launches nothing; every
+ * other call runs exactly as fw_prefill_ex would.
+ *   - One buffer per device: calls that overlap on a device (two streams, two
+ *     host threads) race on it; order them.
+ *   - The first call on a device looks the buffer's address up
+ *     (cudaGetSymbolAddress) and sets kernel attributes: make one call
+ *     before capturing a stream.
+ *   - Nothing in the buffer has to start at zero: the segment launch writes
+ *     every byte the second kernel reads.
+ *   - The buffer is reserved when the library's module holding it loads
+ *     (with CUDA's default lazy loading, at the first call of this function).
+ * Returns FW_OK or a negative FW_ERR_* code.
+ */
+#define FW_SCRATCH_BYTES (144u * 1024u * 1024u)
+int fw_prefill_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                       const float *lambda, const float *S0, const void *k_init, void *o,
+                       float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
+                       fw_phi phi, float eps, unsigned flags, fw_algo algo,
+                       cudaStream_t stream);
 
 /*
  * fw_step -- one decode step for B*H independent states, S updated in place.

@@ -131,11 +131,14 @@ int check_window(const fw_window *in, const fw_window *out, int W, const WinExte
 
 using namespace fw;
 
-extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
-                             const float *lambda, const float *S0, const void *k_init, void *o,
-                             float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
-                             fw_phi phi, float eps, unsigned flags, fw_algo algo,
-                             cudaStream_t stream) {
+namespace {
+
+// fw_prefill_ex and fw_prefill_noalloc (noalloc: the two-segment form's
+// workspace from the static buffer, never from the pool)
+int prefill_impl(const void *q, const void *k, const void *v, const float *beta,
+                 const float *lambda, const float *S0, const void *k_init, void *o, float *S_T,
+                 const fw_shape *shape, fw_dtype dtype, fw_mode mode, fw_phi phi, float eps,
+                 unsigned flags, fw_algo algo, cudaStream_t stream, bool noalloc) {
     int st = check_common(shape, dtype, mode, phi, eps, flags);
     if (st != FW_OK) return st;
     if (window_mode(mode)) return FW_ERR_MODE;   // fw_window_prefill
@@ -181,6 +184,7 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     a.force_timeout = g_force_timeout.load();
     a.seg_pref = g_seg_pref.load();
     a.seg_t0 = 0; a.o_aux = nullptr; a.s_aux = nullptr;
+    a.scratch_only = 0; a.scratch = nullptr; a.scratch_bytes = 0;
 
     const bool chunk_ok = per_channel(mode) ? chunked_chan_supported(a) : chunked_supported(a);
     if (algo == FW_ALGO_CHUNKED && !chunk_ok) return FW_ERR_UNSUPPORTED;
@@ -205,10 +209,45 @@ extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const 
     } else if (algo == FW_ALGO_RECURRENT || !chunk_ok) {
         e = launch_recurrent(a, stream);
     } else {
+        if (noalloc) {
+            // the two-segment form's workspace: the static buffer, or nothing
+            int dev = 0, sms = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const size_t need = chunked_segment_bytes(a, sms);
+            if (need > 0) {
+                if (need > (size_t)FW_SCRATCH_BYTES) return FW_ERR_SCRATCH;
+                a.scratch = segment_scratch(dev, &e);
+                if (!a.scratch) return cuda_fail(e);
+                a.scratch_bytes = FW_SCRATCH_BYTES;
+            }
+            a.scratch_only = 1;
+        }
         e = launch_chunked(a, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return FW_OK;
+}
+
+}  // namespace
+
+extern "C" int fw_prefill_ex(const void *q, const void *k, const void *v, const float *beta,
+                             const float *lambda, const float *S0, const void *k_init, void *o,
+                             float *S_T, const fw_shape *shape, fw_dtype dtype, fw_mode mode,
+                             fw_phi phi, float eps, unsigned flags, fw_algo algo,
+                             cudaStream_t stream) {
+    return prefill_impl(q, k, v, beta, lambda, S0, k_init, o, S_T, shape, dtype, mode, phi, eps,
+                        flags, algo, stream, false);
+}
+
+extern "C" int fw_prefill_noalloc(const void *q, const void *k, const void *v, const float *beta,
+                                  const float *lambda, const float *S0, const void *k_init,
+                                  void *o, float *S_T, const fw_shape *shape, fw_dtype dtype,
+                                  fw_mode mode, fw_phi phi, float eps, unsigned flags,
+                                  fw_algo algo, cudaStream_t stream) {
+    return prefill_impl(q, k, v, beta, lambda, S0, k_init, o, S_T, shape, dtype, mode, phi, eps,
+                        flags, algo, stream, true);
 }
 
 extern "C" int fw_prefill(const void *q, const void *k, const void *v, const float *beta,
@@ -419,6 +458,7 @@ extern "C" const char *fw_status_string(int status) {
     case FW_ERR_UNSUPPORTED: return "FW_ERR_UNSUPPORTED: the chunked kernel does not take this call";
     case FW_ERR_ARG: return "FW_ERR_ARG: invalid eps or overlapping buffers";
     case FW_ERR_DEVICE: return "FW_ERR_DEVICE: the current device is not sm_103";
+    case FW_ERR_SCRATCH: return "FW_ERR_SCRATCH: the call needs more than FW_SCRATCH_BYTES of scratch";
     default: return "unknown status";
     }
 }

@@ -1477,6 +1477,30 @@ extern "C" int fw_debug_read_trace(unsigned long long *dst, int n) {
 }
 #endif
 
+// The two-segment plan: the split token (0: one segment), the workspace bytes and
+// the offset of the states in it.  The chain splits at the chunk boundary nearest
+// T/2 when at most a third of the SMs hold a chain and T >= 4096, or as the test
+// hook asks.
+static int64_t segment_plan(const PrefillArgs &a, int sms, size_t *bytes, size_t *n_o) {
+    const int64_t nchk = (a.T + C - 1) / C;
+    *bytes = 0;
+    *n_o = 0;
+    if (a.seg_pref < 0 || nchk < 2 ||
+        !(a.seg_pref > 0 || (3 * a.n_chains <= (int64_t)sms && a.T >= 4096)))
+        return 0;
+    const int64_t t0 = (int64_t)C * (nchk / 2);
+    *n_o = (size_t)a.n_chains * (size_t)(a.T - t0) * D * 2;   // a multiple of 256
+    // S_mid, S_T from zero and Phi_T in fp32, then S_mid^T in bf16
+    *bytes = *n_o + (size_t)3 * (size_t)a.n_chains * D * D * 4 + (size_t)a.n_chains * D * D * 2;
+    return t0;
+}
+
+size_t chunked_segment_bytes(const PrefillArgs &a, int sms) {
+    size_t bytes = 0, n_o = 0;
+    segment_plan(a, sms, &bytes, &n_o);
+    return bytes;
+}
+
 cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, a.q, a.T, a.n_chains) || !make_map(&tk, a.k, a.T, a.n_chains) ||
@@ -1487,26 +1511,31 @@ cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    // Few long chains: each runs as two segments at once (three CTAs per chain),
-    // when at most a third of the SMs hold a chain and T >= 4096, or as the test
-    // hook asks; the split is at a chunk boundary.
+    // Few long chains: each runs as two segments at once (three CTAs per chain).
+    // The workspace comes from the private pool, or (fw_prefill_noalloc) from the
+    // static buffer, whose size the API has checked.
     PrefillArgs b = a;
-    const int64_t nchk = (a.T + C - 1) / C;
-    void *ws = nullptr;
-    if (a.seg_pref >= 0 && nchk >= 2 &&
-        (a.seg_pref > 0 || (3 * a.n_chains <= (int64_t)sms && a.T >= 4096))) {
-        const int64_t t0 = (int64_t)C * (nchk / 2);
-        const size_t n_o = (size_t)a.n_chains * (size_t)(a.T - t0) * D * 2;   // a multiple of 256
-        // S_mid, S_T from zero and Phi_T in fp32, then S_mid^T in bf16
-        const size_t n_s = (size_t)3 * (size_t)a.n_chains * D * D * 4 + (size_t)a.n_chains * D * D * 2;
-        cudaMemPool_t pool = segment_pool(dev);
-        if (pool && cudaMallocFromPoolAsync(&ws, n_o + n_s, pool, s) == cudaSuccess) {
-            b.seg_t0 = t0;
-            b.o_aux = ws;
-            b.s_aux = reinterpret_cast<float *>(static_cast<char *>(ws) + n_o);
+    void *ws = nullptr;   // from the pool: freed after the launches
+    size_t need = 0, n_o = 0;
+    const int64_t t0 = segment_plan(a, sms, &need, &n_o);
+    if (t0 > 0) {
+        void *base = nullptr;
+        if (a.scratch_only) {
+            if (!a.scratch || need > a.scratch_bytes) return cudaErrorInvalidValue;
+            base = a.scratch;
         } else {
-            cudaGetLastError();   // no workspace: the call runs unsplit
-            ws = nullptr;
+            cudaMemPool_t pool = segment_pool(dev);
+            if (pool && cudaMallocFromPoolAsync(&ws, need, pool, s) == cudaSuccess) {
+                base = ws;
+            } else {
+                cudaGetLastError();   // no workspace: the call runs unsplit
+                ws = nullptr;
+            }
+        }
+        if (base) {
+            b.seg_t0 = t0;
+            b.o_aux = base;
+            b.s_aux = reinterpret_cast<float *>(static_cast<char *>(base) + n_o);
         }
     }
     const int64_t ctas = b.seg_t0 > 0 ? 3 * a.n_chains : a.n_chains;

@@ -35,6 +35,10 @@ struct PrefillArgs {
     int64_t seg_t0;
     void *o_aux;       // outputs of the transition run, bf16 [n_chains][T - seg_t0][d]
     float *s_aux;      // S at the split, S_T from a zero start, transition: fp32 [3][n_chains][d][d]
+    // fw_prefill_noalloc: the two-segment workspace comes from this buffer only
+    int scratch_only;
+    void *scratch;
+    size_t scratch_bytes;
 };
 
 struct StepArgs {
@@ -85,6 +89,12 @@ cudaError_t launch_decode(const StepArgs &a, cudaStream_t s);
 // Chunked tensor-core prefill.  supported() tells whether it takes the call.
 bool chunked_supported(const PrefillArgs &a);
 cudaError_t launch_chunked(const PrefillArgs &a, cudaStream_t s);
+// Bytes of workspace the chunked launch's two-segment form takes for this call
+// on a device with `sms` SMs (0: the call runs as one segment).
+size_t chunked_segment_bytes(const PrefillArgs &a, int sms);
+// Device address of the static buffer of fw_prefill_noalloc on device `dev`
+// (looked up once per device), or nullptr with the CUDA error in *e.
+void *segment_scratch(int dev, cudaError_t *e);
 // Chunked tensor-core prefill of the per-channel step (Falcon-2 / 2A).
 bool chunked_chan_supported(const PrefillArgs &a);
 cudaError_t launch_chunked_chan(const PrefillArgs &a, cudaStream_t s);

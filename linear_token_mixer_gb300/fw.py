@@ -26,7 +26,7 @@ DTYPES = {torch.float32: FW_F32, torch.bfloat16: FW_BF16}
 FW_OK = 0
 STATUS = {0: "FW_OK", -1: "FW_ERR_NULL", -2: "FW_ERR_SHAPE", -3: "FW_ERR_DTYPE",
           -4: "FW_ERR_ALIGN", -5: "FW_ERR_MODE", -6: "FW_ERR_CUDA", -7: "FW_ERR_TIMEOUT",
-          -8: "FW_ERR_UNSUPPORTED", -9: "FW_ERR_ARG", -10: "FW_ERR_DEVICE"}
+          -8: "FW_ERR_UNSUPPORTED", -9: "FW_ERR_ARG", -10: "FW_ERR_DEVICE", -11: "FW_ERR_SCRATCH"}
 
 
 class FwError(RuntimeError):
@@ -47,7 +47,7 @@ class fw_window(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("n", ctypes.c_void_p)]
 
 
-EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_step", "fw_step_ex", "fw_window_prefill",
+EXPORTS = ("fw_prefill", "fw_prefill_ex", "fw_prefill_noalloc", "fw_step", "fw_step_ex", "fw_window_prefill",
            "fw_window_step", "fw_check",
            "fw_status_string", "fw_version", "fw_last_cuda_error", "fw_set_wait_limit_us",
            "fw_debug_force_timeout", "fw_debug_segment_split")
@@ -68,6 +68,7 @@ def lib():
         L.fw_prefill.argtypes = [P, P, P, P, P, P, P, P, SP, I, I, I, F, P]
         U = ctypes.c_uint
         L.fw_prefill_ex.argtypes = [P, P, P, P, P, P, P, P, P, SP, I, I, I, F, U, I, P]
+        L.fw_prefill_noalloc.argtypes = L.fw_prefill_ex.argtypes
         L.fw_step.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, P]
         L.fw_step_ex.argtypes = [P, P, P, P, P, P, P, SP, I, I, I, F, U, P]
         WP = ctypes.POINTER(fw_window)
@@ -85,7 +86,8 @@ def lib():
         L.fw_debug_force_timeout.restype = None
         L.fw_debug_segment_split.argtypes = [I]
         L.fw_debug_segment_split.restype = None
-        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_step, L.fw_step_ex, L.fw_window_prefill,
+        for f in (L.fw_prefill, L.fw_prefill_ex, L.fw_prefill_noalloc, L.fw_step, L.fw_step_ex,
+                  L.fw_window_prefill,
                   L.fw_window_step, L.fw_check, L.fw_version, L.fw_last_cuda_error):
             f.restype = I
         _lib = L
@@ -113,26 +115,28 @@ def _flags(rbw, same_pair):
 
 def prefill(q, k, v, beta=None, lam=None, S0=None, *, mode="falcon1", phi="identity",
             eps=1e-6, k_init=None, algo="auto", o=None, S_T=None, stream=None, rbw=False,
-            same_pair=False):
+            same_pair=False, noalloc=False):
     """Run the recurrence over q, k, v [B, H, T, d] (fp32 or bf16).
 
     mode: "falcon1", "falcon1a", "falcon2", "falcon2a" or "linattn"; rbw reads
     before the write, same_pair pairs each key with its own value.  Returns
     (o [B,H,T,d] in q's dtype, S_T [B,H,d,d] fp32).  beta, lam [B,H,T] fp32 are
     required in the falcon modes (beta [B,H,T,d] for falcon2 / falcon2a).  S0
-    [B,H,d,d] fp32 or None."""
+    [B,H,d,d] fp32 or None.  noalloc: call fw_prefill_noalloc (the library's
+    workspace from its static buffer; pass o and S_T to allocate nothing here
+    either)."""
     B, H, T, d = q.shape
     if o is None:
         o = torch.empty_like(q)
     if S_T is None:
         S_T = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
     shp = fw_shape(B, H, T, d, v.shape[-1])
-    st = lib().fw_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
-                             _ptr(k_init), _ptr(o), _ptr(S_T), ctypes.byref(shp),
-                             DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi], float(eps),
-                             _flags(rbw, same_pair), ALGOS[algo], _stream(stream))
+    fn = lib().fw_prefill_noalloc if noalloc else lib().fw_prefill_ex
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(k_init), _ptr(o),
+            _ptr(S_T), ctypes.byref(shp), DTYPES.get(q.dtype, -1), MODES[mode], PHIS[phi],
+            float(eps), _flags(rbw, same_pair), ALGOS[algo], _stream(stream))
     if st != FW_OK:
-        raise FwError(st, "fw_prefill")
+        raise FwError(st, "fw_prefill_noalloc" if noalloc else "fw_prefill")
     return o, S_T
 
 

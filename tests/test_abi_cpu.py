@@ -85,6 +85,25 @@ def test_prefill_validation(L, kw, code):
 
 
 @no_gpu
+@pytest.mark.parametrize("kw", [
+    dict(shape=None), dict(q=None), dict(shape=(1, 1, 0, 64, 64)), dict(dtype=7), dict(mode=9),
+    dict(algo=5), dict(flags=4), dict(q=P[0] + 8), dict(eps=-1.0), dict(o=P[0]),
+    dict(k_init=P[5] + 16), dict(mode=2, beta=None), dict(), dict(mode=1, beta=None, lam=None),
+])
+def test_prefill_noalloc_validates_as_prefill_ex(L, kw):
+    # same arguments, same checks, same codes (a valid call stops at the device query here)
+    args = dict(q=P[0], k=P[1], v=P[2], beta=P[3], lam=P[4], S0=None, k_init=None, o=P[5],
+                S_T=P[6], shape=(1, 1, 8, 64, 64), dtype=1, mode=0, phi=0, eps=1e-6, flags=0, algo=0)
+    args.update(kw)
+    shp = fw.fw_shape(*args["shape"]) if args["shape"] is not None else None
+    st = L.fw_prefill_noalloc(args["q"], args["k"], args["v"], args["beta"], args["lam"], args["S0"],
+                              args["k_init"], args["o"], args["S_T"],
+                              ctypes.byref(shp) if shp is not None else None, args["dtype"],
+                              args["mode"], args["phi"], args["eps"], args["flags"], args["algo"], None)
+    assert st == call_prefill(L, **kw)
+
+
+@no_gpu
 def test_linattn_needs_no_gates(L):
     # beta/lambda may be NULL in linear-attention mode: validation passes and the
     # call fails only at the device query (there is no GPU here).
